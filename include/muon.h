@@ -1,0 +1,226 @@
+/*
+ * muon.h -- C ABI of the shape-fused Muon update for one GB300 (sm_103a).
+ *
+ * What the library computes, per parameter matrix (or per batch slice of a 3-D
+ * [E, rows, cols] parameter), all matrices of a step being independent:
+ *
+ *   M' = beta * M + G                                   (momentum)
+ *   X0 = M' / (||M'||_F + eps)                          (Frobenius normalisation)
+ *   if rows > cols: X0 = X0^T                           (iterate on the wide side)
+ *   k times: A = X X^T ; X = a X + (b A + c A A) X      (quintic Newton-Schulz)
+ *   O = X (transposed back if rows > cols)
+ *   P' = P * (1 - lr * wd) - lr * s(rows, cols) * O     (scaled, decayed write)
+ *
+ * Sources: «关于分布式Muon的想法整合及讨论» §1 (momentum, then approximate
+ * orthogonalisation of M used as the update direction), §2 (normalise M, Gram
+ * matrix, a series of matrix products), §6 (sum-of-squares normaliser, Gram
+ * matrix recomputed every round); «MindSpore HyperParallel X 盘古,Muon优化器实现
+ * 6倍性能跃升», 三大性能挑战 (5-10 iterations), Muon亲和的专家切分 (Fig. 4: the
+ * E slices of an expert tensor are independent), 矩阵融合优化 (Fig. 6-7:
+ * parameters sharing their trailing two dims run as one [B, M, N] batch; the
+ * unfused version is dominated by host dispatch and small alloc/free, which is
+ * why all allocation happens in muon_plan_create and a step is one CUDA-graph
+ * replay); HyperParallel-FSDP abstract (arXiv 2609.21594), contribution (3):
+ * shape-fused Newton-Schulz iterations.  The exact scalar forms of momentum,
+ * eps, weight decay and the scale s are readings: the pages give none.
+ *
+ * Conventions shared by every entry point:
+ *  - Device memory is row-major and contiguous.  One pointer per PARAMETER,
+ *    in the order given to muon_plan_create; a 3-D parameter is one pointer to
+ *    its [E, rows, cols] block.  The caller owns params, grads and momenta;
+ *    the plan owns its workspace, pointer tables and CUDA graphs.
+ *  - params and momenta are updated in place; grads are read only; the three
+ *    arrays of one parameter must not overlap each other or another parameter.
+ *  - Errors are returned as muon_status_t; no entry point aborts or throws.
+ *    Argument checks run before any launch.  muon_last_error() returns a
+ *    thread-local message for the last failing call of this thread.
+ *  - A plan is not thread-safe; distinct plans are independent.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All device work is stream-ordered on it.
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct muon_plan_s* muon_plan_t;
+
+typedef enum {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = 1,  /* bad shape, null pointer, bad option        */
+  MUON_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run        */
+  MUON_ERR_OOM = 3,          /* device or pinned-host allocation failed    */
+  MUON_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed          */
+  MUON_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out (see check) */
+} muon_status_t;
+
+/* Storage/compute mode of a plan.
+ * BF16: params and grads bf16, momenta fp32, Newton-Schulz on 16-bit tensor
+ *       core operands with fp32 accumulation.
+ * FP32: params, grads and momenta fp32; every product in fp32 FMA (no TF32). */
+typedef enum { MUON_MODE_BF16 = 0, MUON_MODE_FP32 = 1 } muon_mode_t;
+
+/* Operand type of the Newton-Schulz products in MUON_MODE_BF16.  FP16 (the
+ * default) keeps 3 more mantissa bits at the same tensor-core rate; BF16
+ * rounds X, A and the polynomial matrix to bf16 (larger error, grows with k). */
+typedef enum { MUON_NS_FP16 = 0, MUON_NS_BF16 = 1 } muon_ns_dtype_t;
+
+/* Shape-dependent scale s(rows, cols) of the update (a reading; the pages
+ * only say "scaled"): sqrt(max(1, rows/cols)), 0.2*sqrt(max(rows, cols)), 1. */
+typedef enum {
+  MUON_SCALE_SQRT_ASPECT = 0,
+  MUON_SCALE_RMS_0_2 = 1,
+  MUON_SCALE_NONE = 2
+} muon_scale_t;
+
+/* Kernel path of a shape group.  AUTO picks SKINNY for small min(rows, cols)
+ * (mma.sync fragments streamed through an L2-resident workspace, one
+ * two-CTA cluster per matrix), TENSOR (tcgen05 GEMMs) otherwise; FP32 mode
+ * always uses SIMT. */
+typedef enum {
+  MUON_PATH_AUTO = 0,
+  MUON_PATH_SKINNY = 1,
+  MUON_PATH_TENSOR = 2,
+  MUON_PATH_SIMT = 3
+} muon_path_t;
+
+/* ndim 2: dims = {rows, cols}; ndim 3: dims = {E, rows, cols}. */
+typedef struct {
+  int32_t ndim;
+  int32_t reserved_;
+  int64_t dims[3];
+} muon_shape_t;
+
+#define MUON_FLAG_KEEP_UPDATE  1u  /* keep O = X_k per member (fp32) for muon_debug_copy_update */
+#define MUON_FLAG_NO_GRAPH     2u  /* launch kernels one by one instead of a CUDA-graph replay  */
+#define MUON_FLAG_HOST_STAGING 4u  /* allocate device mirrors so muon_step_host can run         */
+#define MUON_FLAG_GROUP_TIMING 8u  /* record CUDA events around each group's kernels            */
+
+typedef struct {
+  int32_t mode;              /* muon_mode_t, default BF16                          */
+  int32_t scale;             /* muon_scale_t, default SQRT_ASPECT                  */
+  float eps;                 /* added to ||M'||_F, default 1e-7                    */
+  int32_t skinny_threshold;  /* largest min(rows,cols) for SKINNY; 0 = default 64  */
+  int32_t ns_dtype;          /* muon_ns_dtype_t, default FP16                      */
+  uint32_t flags;            /* MUON_FLAG_*                                        */
+  int32_t path_override;     /* muon_path_t for every group; AUTO = choose         */
+  int32_t max_streams;       /* groups run on up to this many graph branches; 0=4  */
+  int32_t reserved[8];       /* must be zero                                       */
+} muon_plan_options;
+
+typedef struct {
+  int64_t rows, cols;        /* the trailing dims every member shares              */
+  int64_t batch;             /* number of member matrices                         */
+  int64_t first_member;      /* index of the group's first member (see below)     */
+  int32_t transposed;        /* rows > cols: the iteration runs on the transpose  */
+  int32_t path;              /* muon_path_t chosen for the group                  */
+  int64_t workspace_bytes;   /* device bytes of the group's scratch               */
+} muon_group_info_t;
+
+/* Fills *opts with the defaults above.  Never fails for a non-null pointer. */
+MUON_API muon_status_t muon_default_options(muon_plan_options* opts);
+
+/* Host-only planning (no device is touched): buckets the parameters by exact
+ * trailing shape (rows, cols) in first-seen order, expanding a 3-D parameter
+ * into its E slices in E order («MindSpore HyperParallel X 盘古,Muon优化器实现
+ * 6倍性能跃升», 矩阵融合优化 Fig. 6 and Muon亲和的专家切分 Fig. 4).
+ * groups: caller array of group_cap entries (may be NULL when group_cap = 0);
+ * *n_groups receives the group count even when it exceeds group_cap.
+ * member_param / member_expert: caller arrays of member_cap entries (or NULL),
+ * filled in group order; *n_members receives the member count.
+ * *workspace_bytes (nullable) receives the device bytes muon_plan_create will
+ * allocate.  INVALID_ARG for ndim not in {2,3}, a dim < 1, n_params < 1,
+ * more than 2^31-1 members, or a bad option. */
+MUON_API muon_status_t muon_plan_describe(const muon_shape_t* shapes, int32_t n_params,
+                                          const muon_plan_options* opts,
+                                          muon_group_info_t* groups, int32_t group_cap,
+                                          int32_t* n_groups,
+                                          int32_t* member_param, int32_t* member_expert,
+                                          int64_t member_cap, int64_t* n_members,
+                                          size_t* workspace_bytes);
+
+/* Builds a plan on CUDA device `device`: the bucketing above, per-group path
+ * and tile choices (functions of (rows, cols) only, never of the batch size,
+ * so a matrix gets bit-identical results in any batch), and every device
+ * allocation the steps will need (workspace, pointer tables, pinned staging).
+ * opts may be NULL (defaults).  *out receives the plan; release it with
+ * muon_plan_destroy.  Errors: INVALID_ARG (as muon_plan_describe, or out
+ * NULL), OOM, CUDA, UNSUPPORTED (device is not sm_103). */
+MUON_API muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
+                                        const muon_plan_options* opts, int device,
+                                        muon_plan_t* out);
+
+/* One Muon step over every parameter of the plan (the update at the top of
+ * this file).  params[i]: bf16 (BF16 mode) or fp32 device pointer to
+ * parameter i, updated in place; grads[i]: same type, read only; momenta[i]:
+ * fp32, updated in place to M'.  beta, lr, wd: momentum, learning rate,
+ * decoupled weight decay.  ns_steps >= 0 (0 = no iteration: O = X0);
+ * (a, b, c): quintic coefficients.  Never allocates.  The first call with a
+ * given ns_steps captures and instantiates a CUDA graph (host work only);
+ * later calls copy the scalars and pointers into the plan's device table
+ * (one async H2D copy from pinned memory) and replay the graph on `stream`.
+ * Errors (nothing is launched): INVALID_ARG for a null plan/array/pointer,
+ * ns_steps < 0 or > 1000, or non-finite scalars; CUDA on a launch failure. */
+MUON_API muon_status_t muon_step(muon_plan_t plan, void* const* params,
+                                 const void* const* grads, float* const* momenta,
+                                 float beta, float lr, float wd, int32_t ns_steps,
+                                 float a, float b, float c, void* stream);
+
+/* The same step on HOST buffers (pinned or pageable): copies each parameter,
+ * gradient and momentum to the plan's device mirrors, runs muon_step on them,
+ * copies params and momenta back, and returns after `stream` has finished
+ * (results are in the host buffers on return).  Needs MUON_FLAG_HOST_STAGING
+ * at plan creation (UNSUPPORTED otherwise).  Contiguous host ranges of
+ * consecutive parameters are moved with one copy each. */
+MUON_API muon_status_t muon_step_host(muon_plan_t plan, void* const* host_params,
+                                      const void* const* host_grads,
+                                      float* const* host_momenta, float beta, float lr,
+                                      float wd, int32_t ns_steps, float a, float b,
+                                      float c, void* stream);
+
+/* Frees everything the plan owns (synchronises its device first).  NULL ok. */
+MUON_API muon_status_t muon_plan_destroy(muon_plan_t plan);
+
+/* Group / member introspection of a created plan (host only). */
+MUON_API int32_t muon_plan_num_groups(muon_plan_t plan);
+MUON_API muon_status_t muon_plan_group_info(muon_plan_t plan, int32_t group,
+                                            muon_group_info_t* info);
+MUON_API size_t muon_plan_workspace_bytes(muon_plan_t plan);
+
+/* Test hook: copies O = X_k of (param_index, expert) as fp32 [rows, cols]
+ * into dst_host (rows*cols floats) after synchronising the device.  Needs
+ * MUON_FLAG_KEEP_UPDATE (UNSUPPORTED otherwise); INVALID_ARG for a bad index. */
+MUON_API muon_status_t muon_debug_copy_update(muon_plan_t plan, int32_t param_index,
+                                              int64_t expert, float* dst_host);
+
+/* Device time of group `group`'s kernels in the most recent step, from CUDA
+ * events recorded inside the step (graph event-record nodes).  Waits for that
+ * step to finish.  Needs MUON_FLAG_GROUP_TIMING (UNSUPPORTED otherwise). */
+MUON_API muon_status_t muon_plan_group_elapsed_ms(muon_plan_t plan, int32_t group, float* ms);
+
+/* Synchronises the plan's device and reads its error word: MUON_OK, or
+ * MUON_ERR_TIMEOUT if any kernel of an earlier step gave up a bounded wait
+ * (the word is then cleared). */
+MUON_API muon_status_t muon_plan_check_error(muon_plan_t plan);
+
+MUON_API const char* muon_status_string(muon_status_t status);
+MUON_API const char* muon_last_error(void);
+/* Library version, e.g. "0.1.0". */
+MUON_API const char* muon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

@@ -1,0 +1,38 @@
+/*
+ * muon_testing.h -- test hooks of the Muon library (not needed by users).
+ *
+ * They run one building block of the TENSOR path on caller buffers so a test
+ * can compare it with an independent matrix product.  Unlike muon_step they
+ * may allocate (a few bytes of device scalars) and they synchronise `stream`.
+ */
+#ifndef MUON_GB300_TESTING_H
+#define MUON_GB300_TESTING_H
+
+#include "muon.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One batched tcgen05 product of a Newton-Schulz step («关于分布式Muon的想法整合
+ * 及讨论» §2: the Gram matrix and the products that follow it), on contiguous
+ * row-major device buffers of 16-bit elements (ns_dtype: muon_ns_dtype_t):
+ *   op 0 (Gram):   out[B][m][m] = y y^T / alpha^2,   y   [B][m][n]
+ *   op 1 (poly):   out[B][m][m] = pa I + pb a + pc a a,  a [B][m][m] (symmetric)
+ *   op 2 (update): out[B][m][n] = q y,               q   [B][m][m], y [B][m][n]
+ * Needs m % 8 == 0 and n % 8 == 0 (16-byte rows).  INVALID_ARG otherwise;
+ * CUDA on a failed launch; TIMEOUT if the kernel gave up a bounded wait. */
+MUON_API muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int32_t B, int64_t m,
+                                            int64_t n, const void* y, const void* a,
+                                            const void* q, void* out, float alpha, float pa,
+                                            float pb, float pc, void* stream);
+
+/* Number of skinny-path clusters (one per member of min dim m, 1..64) that the
+ * current device can hold at once for the given operand type; -1 on error. */
+MUON_API int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_TESTING_H */

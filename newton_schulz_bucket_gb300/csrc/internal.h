@@ -1,0 +1,112 @@
+// Internal host/device structures shared by the library's translation units.
+// Nothing here is part of the public C ABI (include/muon.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace muon {
+
+// Per-step scalars, rewritten in device memory before every step so that one
+// captured CUDA graph serves every step with the same ns_steps.
+struct StepScalars {
+  float beta, lr, wd, a, b, c;
+  int32_t ns_steps;
+  int32_t pad_;
+};
+
+// Per-member device pointers, rewritten before every step (the caller may
+// pass different buffers each step).  P and G are bf16 or fp32 by mode.
+struct MemberPtrs {
+  void* P;
+  const void* G;
+  float* M;
+};
+
+enum Path : int32_t { PATH_AUTO = 0, PATH_SKINNY = 1, PATH_TENSOR = 2, PATH_SIMT = 3 };
+// Element type of the Newton-Schulz iterate / Gram / polynomial buffers.
+enum NsType : int32_t { NS_F32 = 0, NS_F16 = 1, NS_BF16 = 2 };
+
+// Elements of one member handled by one CTA of the momentum pass; fixed so the
+// reduction tree (and thus the norm, bit for bit) depends only on the shape.
+constexpr int64_t kMomentumChunk = 16384;
+
+// Arguments of the per-group kernels, passed by value (baked into the graph).
+struct KArgs {
+  const StepScalars* sc;   // device
+  const MemberPtrs* mem;   // device, already offset to the group's first member
+  int32_t B;               // members in the group
+  int32_t rows, cols;      // parameter dims
+  int32_t m, n;            // min / max of (rows, cols)
+  int32_t T;               // rows > cols
+  int32_t mode_f32;        // 1: P, G fp32 ; 0: P, G bf16
+  int32_t ns_type;         // NsType of y0/y1/A/Q
+  int64_t n_pitch;         // row pitch (elements) of the m x n iterate
+  int64_t m_pitch;         // row pitch (elements) of the m x m Gram / polynomial
+  int32_t n_chunks;        // momentum chunks per member
+  float eps;               // added to ||M'||_F
+  float scale;             // s(rows, cols)
+  float alpha;             // power-of-two factor of the stored iterate (Y = alpha X)
+  void* y0;                // [B][m][n_pitch] (skinny path: fragment workspace)
+  void* y1;                // [B][m][n_pitch]
+  void* A;                 // [B][m][m_pitch]
+  void* Q;                 // [B][m][m_pitch]
+  float* part;             // [B][n_chunks] partial sums of squares
+  float* invn;             // [B] alpha / (||M'||_F + eps)
+  float* dbg;              // nullable: [B][rows][cols] fp32 copy of O
+  int* err;                // device error word
+};
+
+// Skinny path configuration of a group (a function of (rows, cols) only).
+struct SkinnyCfg {
+  int32_t cluster;   // CTAs per matrix
+  int32_t width;     // columns of the wide iterate owned by one CTA
+  int32_t threads;   // threads per CTA
+  int32_t mtiles;    // ceil(m / 16)
+  int32_t smem;      // unused (shared memory is fixed per instantiation)
+  int32_t blk;       // bytes of one 16-column block in the fragment workspace
+  int64_t ws_bytes;  // fragment workspace bytes per member
+};
+
+// ---- launchers (each returns the launch's cudaError_t) ----
+cudaError_t launch_momentum_partial(const KArgs& a, cudaStream_t s);
+cudaError_t launch_norm_finalize(const KArgs& a, cudaStream_t s);
+cudaError_t launch_normalize_cast(const KArgs& a, void* dst, cudaStream_t s);
+cudaError_t launch_write(const KArgs& a, const void* src, cudaStream_t s);
+
+// SIMT batched products (fp32 FMA) on the workspace type of `a`:
+//   gram:   A = (Y Y^T) / alpha^2
+//   poly:   Q = a I + b A + c A A
+//   update: Ydst = Q Ysrc
+cudaError_t launch_simt_gram(const KArgs& a, const void* y, cudaStream_t s);
+cudaError_t launch_simt_poly(const KArgs& a, cudaStream_t s);
+cudaError_t launch_simt_update(const KArgs& a, const void* ysrc, void* ydst, cudaStream_t s);
+
+// Skinny path: momentum kernel, then Newton-Schulz + write per member in one
+// cluster, iterate in a fragment-ordered workspace (a.y0).
+bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg);
+cudaError_t prepare_skinny(const KArgs& a, const SkinnyCfg& cfg);  // function attributes
+cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s);
+// Clusters of the skinny kernel that fit on the device at once (after prepare).
+int skinny_max_active_clusters(int ns_type, int mtiles);
+
+// TENSOR path: tcgen05 GEMMs fed by TMA.  Tensor maps are encoded once per
+// group at plan creation (they hold the workspace addresses).
+struct TcMaps {
+  CUtensorMap y_k128[2];  // iterate y0 / y1, K-major boxes of 128 rows
+  CUtensorMap y_ksq[2];   // iterate, K-major boxes of bn_sq rows (Gram B operand)
+  CUtensorMap y_mn[2];    // iterate, 64 x 64 boxes read N-contiguous (update B operand)
+  CUtensorMap a_k128, a_ksq, q_k128;
+  int bn_sq, bn_up;
+};
+cudaError_t tc_make_maps(const KArgs& a, TcMaps* t);
+cudaError_t prepare_tc(int ns_type);  // function attributes
+cudaError_t launch_tc_gram(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
+cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, cudaStream_t s);
+// Y[1 - src] = Q Y[src]
+cudaError_t launch_tc_update(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
+
+}  // namespace muon

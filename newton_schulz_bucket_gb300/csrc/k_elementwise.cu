@@ -1,0 +1,219 @@
+// Elementwise passes:
+//   momentum + partial sums of squares (every path), norm finalisation,
+//   normalise + cast (+ transpose to the wide orientation), and the scaled,
+//   decayed write (TENSOR / SIMT paths).
+// Momentum M' = beta M + G and the sum-of-squares normaliser follow
+// «关于分布式Muon的想法整合及讨论» §1, §2 and §6; the write
+// P' = P (1 - lr wd) - lr s O is the scaled, weight-decayed update.
+#include "common.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename TP>
+__device__ __forceinline__ void load8(const TP* p, float* f);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float* f) {
+  bf16x8_to_f32(ldg_nc(p), f);
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float* f) {
+  u4_to_f4x2(ldg_nc(p), ldg_nc(p + 4), f);
+}
+
+// One CTA = one fixed chunk of one member: M' = beta M + G (stored), and the
+// chunk's sum of squares of M' (fixed-order tree) into part[b][chunk].
+template <typename TG>
+__global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
+  __shared__ float red[33];
+  const int b = blockIdx.y;
+  const int64_t total = (int64_t)a.rows * a.cols;
+  const int64_t start = (int64_t)blockIdx.x * kMomentumChunk;
+  const int64_t end = min(start + kMomentumChunk, total);
+  const MemberPtrs mp = a.mem[b];
+  const TG* G = static_cast<const TG*>(mp.G);
+  float* M = mp.M;
+  const float beta = a.sc->beta;
+  float acc = 0.f;
+  const bool vec = aligned16(G) && aligned16(M);
+  int64_t i0 = start;
+  if (vec) {
+    constexpr int U = 4;  // 4 x 8 elements in flight per thread
+    const int64_t stride = (int64_t)8 * kThreads;
+    int64_t i = start + 8 * threadIdx.x;
+    for (; i + (U - 1) * stride + 8 <= end; i += U * stride) {
+      float g[U][8], m[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        load8<TG>(G + i + u * stride, g[u]);
+        u4_to_f4x2(ld_cs(M + i + u * stride), ld_cs(M + i + u * stride + 4), m[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          m[u][e] = fmaf(beta, m[u][e], g[u][e]);
+          acc = fmaf(m[u][e], m[u][e], acc);
+        }
+        st_cs(M + i + u * stride, f4_to_u4(m[u]));
+        st_cs(M + i + u * stride + 4, f4_to_u4(m[u] + 4));
+      }
+    }
+    for (; i + 8 <= end; i += stride) {
+      float g[8], m[8];
+      load8<TG>(G + i, g);
+      u4_to_f4x2(ld_cs(M + i), ld_cs(M + i + 4), m);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        m[e] = fmaf(beta, m[e], g[e]);
+        acc = fmaf(m[e], m[e], acc);
+      }
+      st_cs(M + i, f4_to_u4(m));
+      st_cs(M + i + 4, f4_to_u4(m + 4));
+    }
+    i0 = start + ((end - start) / 8) * 8;  // scalar tail below
+  }
+  for (int64_t i = i0 + threadIdx.x; i < end; i += kThreads) {
+    float v = fmaf(beta, M[i], to_f32(G[i]));
+    M[i] = v;
+    acc = fmaf(v, v, acc);
+  }
+  const float s = block_sum(acc, red);
+  if (threadIdx.x == 0) a.part[(int64_t)b * a.n_chunks + blockIdx.x] = s;
+}
+
+// invn[b] = alpha / (sqrt(sum of partials) + eps), partials summed in a fixed
+// order so the result depends only on the member's data.
+__global__ void __launch_bounds__(kThreads) k_norm_finalize(KArgs a) {
+  __shared__ float red[33];
+  const int b = blockIdx.x;
+  const float* p = a.part + (int64_t)b * a.n_chunks;
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < a.n_chunks; i += kThreads) acc += p[i];
+  const float s = block_sum(acc, red);
+  if (threadIdx.x == 0) a.invn[b] = a.alpha / (sqrtf(s) + a.eps);
+}
+
+// Y[b] = cast(M'[b] * invn[b]) in the wide orientation: Y is m x n with row
+// pitch n_pitch; for T (rows > cols) Y = M'^T.  64 x 64 tiles through shared
+// memory so both the read of M' and the write of Y are coalesced.
+template <typename TY>
+__global__ void __launch_bounds__(kThreads) k_normalize_cast(KArgs a, TY* __restrict__ Y) {
+  __shared__ float tile[64][65];
+  const int b = blockIdx.z;
+  const float* Mp = a.mem[b].M;
+  const float inv = a.invn[b];
+  TY* Yb = Y + (int64_t)b * a.m * a.n_pitch;
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;  // tile origin (parameter coords)
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+  for (int rr = ty; rr < 64; rr += 4) {
+    const int r = r0 + rr, c = c0 + tx;
+    tile[rr][tx] = (r < a.rows && c < a.cols) ? Mp[(int64_t)r * a.cols + c] * inv : 0.f;
+  }
+  __syncthreads();
+  if (!a.T) {
+    for (int rr = ty; rr < 64; rr += 4) {
+      const int r = r0 + rr, c = c0 + tx;
+      if (r < a.rows && c < a.cols) Yb[(int64_t)r * a.n_pitch + c] = from_f32<TY>(tile[rr][tx]);
+    }
+  } else {
+    // Y[c][r] = M'[r][c]: Y row index = parameter column
+    for (int cc = ty; cc < 64; cc += 4) {
+      const int c = c0 + cc, r = r0 + tx;
+      if (r < a.rows && c < a.cols) Yb[(int64_t)c * a.n_pitch + r] = from_f32<TY>(tile[tx][cc]);
+    }
+  }
+}
+
+// P' = P (1 - lr wd) - lr s O, O = Y / alpha read back in the parameter's
+// orientation.  Optional fp32 copy of O for the test hook.
+template <typename TY, typename TP>
+__global__ void __launch_bounds__(kThreads) k_write(KArgs a, const TY* __restrict__ Y) {
+  __shared__ float tile[64][65];
+  const int b = blockIdx.z;
+  TP* P = static_cast<TP*>(a.mem[b].P);
+  const TY* Yb = Y + (int64_t)b * a.m * a.n_pitch;
+  const float lr = a.sc->lr, wd = a.sc->wd;
+  const float decay = 1.f - lr * wd;
+  const float coef = lr * a.scale / a.alpha;  // alpha is a power of two
+  const float inv_alpha = 1.f / a.alpha;
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  if (a.T) {
+    // stage the Y tile Y[c0..c0+64)[r0..r0+64) so reads are coalesced along r
+    for (int cc = ty; cc < 64; cc += 4) {
+      const int c = c0 + cc, r = r0 + tx;
+      tile[tx][cc] = (r < a.rows && c < a.cols) ? to_f32(Yb[(int64_t)c * a.n_pitch + r]) : 0.f;
+    }
+    __syncthreads();
+  }
+  float* dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+  for (int rr = ty; rr < 64; rr += 4) {
+    const int r = r0 + rr, c = c0 + tx;
+    if (r >= a.rows || c >= a.cols) continue;
+    const float y = a.T ? tile[rr][tx] : to_f32(Yb[(int64_t)r * a.n_pitch + c]);
+    const int64_t idx = (int64_t)r * a.cols + c;
+    const float p = to_f32(P[idx]);
+    P[idx] = from_f32<TP>(fmaf(-coef, y, p * decay));
+    if (dbg) dbg[idx] = y * inv_alpha;
+  }
+}
+
+dim3 tiles_of(const KArgs& a) {
+  return dim3((a.cols + 63) / 64, (a.rows + 63) / 64, a.B);
+}
+
+}  // namespace
+
+cudaError_t launch_momentum_partial(const KArgs& a, cudaStream_t s) {
+  dim3 grid(a.n_chunks, a.B);
+  if (a.mode_f32)
+    k_momentum_partial<float><<<grid, kThreads, 0, s>>>(a);
+  else
+    k_momentum_partial<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const KArgs& a, cudaStream_t s) {
+  k_norm_finalize<<<a.B, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_normalize_cast(const KArgs& a, void* dst, cudaStream_t s) {
+  switch (a.ns_type) {
+    case NS_F32: k_normalize_cast<float><<<tiles_of(a), kThreads, 0, s>>>(a, (float*)dst); break;
+    case NS_F16: k_normalize_cast<__half><<<tiles_of(a), kThreads, 0, s>>>(a, (__half*)dst); break;
+    default:
+      k_normalize_cast<__nv_bfloat16><<<tiles_of(a), kThreads, 0, s>>>(a, (__nv_bfloat16*)dst);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_write(const KArgs& a, const void* src, cudaStream_t s) {
+  const dim3 g = tiles_of(a);
+  if (a.mode_f32) {
+    switch (a.ns_type) {
+      case NS_F32: k_write<float, float><<<g, kThreads, 0, s>>>(a, (const float*)src); break;
+      case NS_F16: k_write<__half, float><<<g, kThreads, 0, s>>>(a, (const __half*)src); break;
+      default: k_write<__nv_bfloat16, float><<<g, kThreads, 0, s>>>(a, (const __nv_bfloat16*)src);
+    }
+  } else {
+    switch (a.ns_type) {
+      case NS_F32:
+        k_write<float, __nv_bfloat16><<<g, kThreads, 0, s>>>(a, (const float*)src);
+        break;
+      case NS_F16:
+        k_write<__half, __nv_bfloat16><<<g, kThreads, 0, s>>>(a, (const __half*)src);
+        break;
+      default:
+        k_write<__nv_bfloat16, __nv_bfloat16><<<g, kThreads, 0, s>>>(
+            a, (const __nv_bfloat16*)src);
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace muon

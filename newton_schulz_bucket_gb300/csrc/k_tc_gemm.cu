@@ -1,0 +1,515 @@
+// tcgen05 / TMEM / TMA batched GEMMs of one Newton-Schulz step (TENSOR path).
+//
+//   GRAM:   A  = (Y Y^T) / alpha^2          M = N = m, K = n   (Gram matrix)
+//   POLY:   Q  = a I + b A + c (A A)        M = N = K = m      (step polynomial)
+//   UPDATE: Y' = Q Y                        M = m, N = n, K = m
+// «关于分布式Muon的想法整合及讨论» §2: the iteration is a Gram matrix and a series
+// of matrix products; §6: A is rebuilt from the new X every round.  Writing
+// aX + (bA + cAA)X as (aI + bA + cAA)X folds the axpy into the polynomial
+// matrix, so each step is three dense products with fused epilogues.
+//
+// Design (sm_103a): persistent CTAs (one per SM), 192 threads:
+//   warp 0      TMA producer: 128-byte-swizzled tiles into a 4-stage ring;
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128,
+//               N=BN, K=16, fp16/bf16 operands, fp32 accumulators in TMEM);
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               fused scale / polynomial / cast, stores.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1.  Every wait is bounded: on timeout the kernel sets the plan's error
+// word and all roles leave their loops.
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int BM = 128, BK = 64, kStages = 4, kThreads = 192;
+constexpr long long kWaitCycles = 1ll << 32;  // ~2 s at 2 GHz
+
+enum TcOp { TC_GRAM = 0, TC_POLY = 1, TC_UPDATE = 2 };
+
+struct TcArgs {
+  int B, M, N, K;
+  int tiles_m, tiles_n;
+  int64_t ldc, sC;        // output row pitch / batch stride (elements)
+  void* C;
+  const void* aux;        // POLY: the A matrix (same layout as C)
+  const StepScalars* sc;
+  float scale;            // GRAM: 1 / alpha^2
+  int* err;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if another role aborted or the wait ran out (then the
+// error word gets bit `code` and every role is told to stop).
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(err, code);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---- TMA ----
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t mbar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(mbar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// ---- tcgen05 ----
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 version bits.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, A/B fp16 (0) or bf16
+// (1), A K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t fmt, int M, int N, bool b_mn_major) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int BN>
+struct TcSmem {
+  static constexpr uint32_t kA = BM * BK * 2;          // 16 KB
+  static constexpr uint32_t kB = BN * BK * 2;          // 32 KB (BN = 256)
+  static constexpr uint32_t kStage = kA + kB;
+  static constexpr uint32_t kBars = kStages * kStage;  // barrier area offset
+  static constexpr uint32_t kTotal = kBars + 256 + 1024;  // + barriers + alignment slack
+};
+
+__device__ __forceinline__ void decode_tile(int t, const TcArgs& p, int& b, int& tm, int& tn) {
+  // grouped order: 8 tile-rows share a sweep over the tile-columns, so the
+  // tiles in flight reuse a compact set of operand panels through L2
+  constexpr int GM = 8;
+  const int per_b = p.tiles_m * p.tiles_n;
+  b = t / per_b;
+  int r = t - b * per_b;
+  const int group = r / (GM * p.tiles_n);
+  const int first = group * GM;
+  const int gsz = min(p.tiles_m - first, GM);
+  r -= group * GM * p.tiles_n;
+  tm = first + r % gsz;
+  tn = r / gsz;
+}
+
+template <typename TY>
+__device__ __forceinline__ void store_row32(TY* dst, const float* v, int nvalid) {
+  if (nvalid >= 32) {
+    uint4 u[4];
+    uint32_t* w = reinterpret_cast<uint32_t*>(u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      TY lo = from_f32<TY>(v[2 * i]), hi = from_f32<TY>(v[2 * i + 1]);
+      w[i] = (uint32_t)(*reinterpret_cast<uint16_t*>(&lo)) |
+             ((uint32_t)(*reinterpret_cast<uint16_t*>(&hi)) << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst)[i] = u[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) dst[i] = from_f32<TY>(v[i]);
+  }
+}
+
+template <typename TY, int OP, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              TcArgs p) {
+  using L = TcSmem<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  // bars: full[kStages], empty[kStages], tfull[2], tempty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = saddr(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+  constexpr uint32_t kCols = 2 * BN;  // two accumulators
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 128); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&mapA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&mapB) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(tmem_slot)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.B * p.tiles_m * p.tiles_n;
+  const int kblocks = (p.K + BK - 1) / BK;
+  constexpr bool kMN = OP == TC_UPDATE;  // B operand is N-contiguous (MN-major)
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer ----
+      int s = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int b, tm, tn;
+        decode_tile(t, p, b, tm, tn);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err, 1)) goto producer_done;
+          mbar_expect_tx(full(s), L::kStage);
+          const uint32_t sa = saddr(smem + s * L::kStage);
+          const uint32_t sb = sa + L::kA;
+          tma_load_3d(sa, &mapA, full(s), kb * BK, tm * BM, b);
+          if (kMN) {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_3d(sb + c * (64 * BK * 2), &mapB, full(s), tn * BN + c * 64, kb * BK, b);
+          } else {
+            tma_load_3d(sb, &mapB, full(s), kb * BK, tn * BN, b);
+          }
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer ----
+      constexpr uint32_t idesc =
+          instr_desc(std::is_same<TY, __nv_bfloat16>::value ? 1u : 0u, BM, BN, kMN);
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        if (!mbar_wait(tempty(acc), aph ^ 1, abort_flag, p.err, 2)) goto mma_done;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full(s), ph, abort_flag, p.err, 4)) goto mma_done;
+          tc_fence_after();
+          const uint32_t sa = saddr(smem + s * L::kStage);
+          const uint32_t sb = sa + L::kA;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = kMN ? smem_desc(sb + kk * 2048, 64 * BK * 2, 1024)
+                                    : smem_desc(sb + kk * 32, 16, 1024);
+            umma(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+          }
+          umma_commit(empty(s));  // frees the stage once these MMAs retire
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+        umma_commit(tfull(acc));
+        if (++acc == 2) { acc = 0; aph ^= 1; }
+      }
+    mma_done:;
+    }
+  } else {  // ---- epilogue: warps 2..5, one accumulator row per thread ----
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    float ca = 0.f, cb = 0.f, cc = 0.f;
+    if (OP == TC_POLY) { ca = p.sc->a; cb = p.sc->b; cc = p.sc->c; }
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int b, tm, tn;
+      decode_tile(t, p, b, tm, tn);
+      if (!mbar_wait(tfull(acc), aph, abort_flag, p.err, 8)) break;
+      tc_fence_after();
+      const int row = tm * BM + row_in_tile;
+      TY* crow = static_cast<TY*>(p.C) + (int64_t)b * p.sC + (int64_t)row * p.ldc;
+      const TY* arow = OP == TC_POLY ? static_cast<const TY*>(p.aux) + (int64_t)b * p.sC +
+                                           (int64_t)row * p.ldc
+                                     : nullptr;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(acc * BN + ch * 32);
+        tmem_ld32(taddr, r);
+        const int col0 = tn * BN + ch * 32;
+        if (row >= p.M || col0 >= p.N) continue;
+        const int nvalid = min(32, p.N - col0);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if (OP == TC_GRAM) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= p.scale;
+        } else if (OP == TC_POLY) {
+          float av[32];
+          if (nvalid == 32) {
+            const uint4* src = reinterpret_cast<const uint4*>(arow + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 u = src[q];
+              const TY* h = reinterpret_cast<const TY*>(&u);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) av[q * 8 + e] = to_f32(h[e]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) av[i] = i < nvalid ? to_f32(arow[col0 + i]) : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = fmaf(cc, v[i], cb * av[i]);
+            if (col0 + i == row) v[i] += ca;
+          }
+        }
+        store_row32<TY>(crow + col0, v, nvalid);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty(acc));
+      if (++acc == 2) { acc = 0; aph ^= 1; }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// 3-D map over [B][rows][inner] (logical extents; pitch in elements), 128-byte
+// swizzle, zero fill outside the extents.
+cudaError_t make_map(CUtensorMap* m, const void* base, int ns_type, int64_t inner, int64_t rows,
+                     int64_t B, int64_t pitch, uint32_t box0, uint32_t box1) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)(pitch * 2), (cuuint64_t)(rows * pitch * 2)};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, ns_type == NS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <typename TY, int OP, int BN>
+cudaError_t run(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& p, cudaStream_t s,
+                bool prepare) {
+  auto fn = k_tc_gemm<TY, OP, BN>;
+  if (prepare)
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TcSmem<BN>::kTotal);
+  const int tiles = p.B * p.tiles_m * p.tiles_n;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  fn<<<grid, kThreads, TcSmem<BN>::kTotal, s>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+template <int OP, int BN>
+cudaError_t run_t(int ns_type, const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& p,
+                  cudaStream_t s, bool prep) {
+  return ns_type == NS_BF16 ? run<__nv_bfloat16, OP, BN>(ma, mb, p, s, prep)
+                            : run<__half, OP, BN>(ma, mb, p, s, prep);
+}
+
+template <int OP>
+cudaError_t run_bn(int bn, int ns_type, const CUtensorMap& ma, const CUtensorMap& mb,
+                   const TcArgs& p, cudaStream_t s, bool prep) {
+  return bn == 256 ? run_t<OP, 256>(ns_type, ma, mb, p, s, prep)
+                   : run_t<OP, 128>(ns_type, ma, mb, p, s, prep);
+}
+
+TcArgs base_args(const KArgs& a) {
+  TcArgs p{};
+  p.B = a.B;
+  p.sc = a.sc;
+  p.err = a.err;
+  return p;
+}
+
+int tc_bn_square(int64_t m) { return m >= 256 ? 256 : 128; }
+int tc_bn_update(int64_t n) { return n >= 256 ? 256 : 128; }
+
+}  // namespace
+
+cudaError_t tc_make_maps(const KArgs& a, TcMaps* t) {
+  const int bs = tc_bn_square(a.m), bu = tc_bn_update(a.n);
+  void* ys[2] = {a.y0, a.y1};
+  cudaError_t e;
+  for (int i = 0; i < 2; ++i) {
+    if ((e = make_map(&t->y_k128[i], ys[i], a.ns_type, a.n, a.m, a.B, a.n_pitch, 64, 128))) return e;
+    if ((e = make_map(&t->y_ksq[i], ys[i], a.ns_type, a.n, a.m, a.B, a.n_pitch, 64, bs))) return e;
+    if ((e = make_map(&t->y_mn[i], ys[i], a.ns_type, a.n, a.m, a.B, a.n_pitch, 64, 64))) return e;
+  }
+  if ((e = make_map(&t->a_k128, a.A, a.ns_type, a.m, a.m, a.B, a.m_pitch, 64, 128))) return e;
+  if ((e = make_map(&t->a_ksq, a.A, a.ns_type, a.m, a.m, a.B, a.m_pitch, 64, bs))) return e;
+  if ((e = make_map(&t->q_k128, a.Q, a.ns_type, a.m, a.m, a.B, a.m_pitch, 64, 128))) return e;
+  t->bn_sq = bs;
+  t->bn_up = bu;
+  return cudaSuccess;
+}
+
+cudaError_t prepare_tc(int ns_type) {
+  const CUtensorMap m{};
+  const TcArgs p{};
+  cudaError_t e;
+  for (int bn : {128, 256}) {
+    if ((e = run_bn<TC_GRAM>(bn, ns_type, m, m, p, nullptr, true))) return e;
+    if ((e = run_bn<TC_POLY>(bn, ns_type, m, m, p, nullptr, true))) return e;
+    if ((e = run_bn<TC_UPDATE>(bn, ns_type, m, m, p, nullptr, true))) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc_gram(const KArgs& a, const TcMaps& t, int src, cudaStream_t s) {
+  TcArgs p = base_args(a);
+  p.M = a.m; p.N = a.m; p.K = a.n;
+  p.tiles_m = (a.m + BM - 1) / BM;
+  p.tiles_n = (a.m + t.bn_sq - 1) / t.bn_sq;
+  p.ldc = a.m_pitch; p.sC = (int64_t)a.m * a.m_pitch;
+  p.C = a.A;
+  p.scale = 1.f / (a.alpha * a.alpha);
+  return run_bn<TC_GRAM>(t.bn_sq, a.ns_type, t.y_k128[src], t.y_ksq[src], p, s, false);
+}
+
+cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, cudaStream_t s) {
+  TcArgs p = base_args(a);
+  p.M = a.m; p.N = a.m; p.K = a.m;
+  p.tiles_m = (a.m + BM - 1) / BM;
+  p.tiles_n = (a.m + t.bn_sq - 1) / t.bn_sq;
+  p.ldc = a.m_pitch; p.sC = (int64_t)a.m * a.m_pitch;
+  p.C = a.Q;
+  p.aux = a.A;
+  return run_bn<TC_POLY>(t.bn_sq, a.ns_type, t.a_k128, t.a_ksq, p, s, false);
+}
+
+cudaError_t launch_tc_update(const KArgs& a, const TcMaps& t, int src, cudaStream_t s) {
+  TcArgs p = base_args(a);
+  p.M = a.m; p.N = a.n; p.K = a.m;
+  p.tiles_m = (a.m + BM - 1) / BM;
+  p.tiles_n = (a.n + t.bn_up - 1) / t.bn_up;
+  p.ldc = a.n_pitch; p.sC = (int64_t)a.m * a.n_pitch;
+  p.C = src == 0 ? a.y1 : a.y0;
+  return run_bn<TC_UPDATE>(t.bn_up, a.ns_type, t.q_k128, t.y_mn[src], p, s, false);
+}
+
+}  // namespace muon

@@ -1,0 +1,721 @@
+// Host planner and executor behind the C ABI (include/muon.h).
+//
+// Planning buckets parameters by exact trailing shape («MindSpore HyperParallel
+// X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化, Fig. 6: parameters whose
+// trailing two dims agree are stacked into one [B, M, N] batch; Muon亲和的专家
+// 切分, Fig. 4: the E slices of an expert tensor are independent members).
+// The same article traces the unfused iteration's cost to host dispatch,
+// small alloc/free and stream synchronisation, so every allocation happens at
+// plan creation and a step is one async copy of scalars + pointers followed by
+// one CUDA-graph replay.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/muon.h"
+#include "internal.h"
+
+namespace muon {
+namespace {
+
+thread_local std::string g_last_error;
+
+muon_status_t fail(muon_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (expr);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(e_ == cudaErrorMemoryAllocation ? MUON_ERR_OOM : MUON_ERR_CUDA,       \
+                  "%s failed: %s", #expr, cudaGetErrorString(e_));                      \
+  } while (0)
+
+constexpr int kRingSlots = 4;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct GroupPlan {
+  int64_t rows = 0, cols = 0, batch = 0, first_member = 0;
+  int32_t transposed = 0, path = PATH_AUTO;
+  int64_t m = 0, n = 0, n_pitch = 0, m_pitch = 0, n_chunks = 0;
+  int32_t ns_type = NS_F16;
+  float alpha = 1.f, scale = 1.f;
+  SkinnyCfg sk{};
+  TcMaps tc{};          // TENSOR path: TMA descriptors of the workspace
+  size_t off_y0 = 0, off_y1 = 0, off_a = 0, off_q = 0, off_part = 0, off_invn = 0, off_dbg = 0;
+  size_t ws_bytes = 0;  // this group's scratch (from the group base)
+  size_t base = 0;      // offset of the group's scratch in the plan workspace
+  double cost = 0;      // flops-ish estimate, for stream assignment
+};
+
+struct PlanDesc {
+  muon_plan_options opt{};
+  std::vector<GroupPlan> groups;
+  std::vector<int32_t> member_param, member_expert;
+  std::vector<int64_t> param_E, param_rows, param_cols;
+  size_t ws_bytes = 0;      // total device scratch incl. tables
+  size_t off_scalars = 0;   // StepScalars + MemberPtrs table
+  size_t off_err = 0;
+  size_t pb_bytes = 0;      // bytes of the per-step parameter block
+};
+
+size_t ns_esize(int32_t t) { return t == NS_F32 ? 4 : 2; }
+
+muon_status_t check_options(const muon_plan_options& o) {
+  if (o.mode != MUON_MODE_BF16 && o.mode != MUON_MODE_FP32)
+    return fail(MUON_ERR_INVALID_ARG, "mode %d is not a muon_mode_t", o.mode);
+  if (o.scale < MUON_SCALE_SQRT_ASPECT || o.scale > MUON_SCALE_NONE)
+    return fail(MUON_ERR_INVALID_ARG, "scale %d is not a muon_scale_t", o.scale);
+  if (!(o.eps >= 0.f) || !std::isfinite(o.eps))
+    return fail(MUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (o.ns_dtype != MUON_NS_FP16 && o.ns_dtype != MUON_NS_BF16)
+    return fail(MUON_ERR_INVALID_ARG, "ns_dtype %d is not a muon_ns_dtype_t", o.ns_dtype);
+  if (o.path_override < MUON_PATH_AUTO || o.path_override > MUON_PATH_SIMT)
+    return fail(MUON_ERR_INVALID_ARG, "path_override %d is not a muon_path_t", o.path_override);
+  if (o.mode == MUON_MODE_FP32 && o.path_override != MUON_PATH_AUTO &&
+      o.path_override != MUON_PATH_SIMT)
+    return fail(MUON_ERR_INVALID_ARG, "FP32 mode runs only the SIMT (fp32 FMA) path");
+  if (o.max_streams < 0 || o.max_streams > 16)
+    return fail(MUON_ERR_INVALID_ARG, "max_streams must be in [0, 16]");
+  if (o.skinny_threshold < -1 || o.skinny_threshold > 64)
+    return fail(MUON_ERR_INVALID_ARG, "skinny_threshold must be in [-1, 64]");
+  if (o.flags & ~(MUON_FLAG_KEEP_UPDATE | MUON_FLAG_NO_GRAPH | MUON_FLAG_HOST_STAGING |
+                  MUON_FLAG_GROUP_TIMING))
+    return fail(MUON_ERR_INVALID_ARG, "unknown flag bits 0x%x", o.flags);
+  for (int i = 0; i < 8; ++i)
+    if (o.reserved[i] != 0) return fail(MUON_ERR_INVALID_ARG, "reserved option fields must be 0");
+  return MUON_OK;
+}
+
+float scale_of(int32_t mode, int64_t rows, int64_t cols) {
+  switch (mode) {
+    case MUON_SCALE_SQRT_ASPECT:
+      return (float)std::sqrt(std::max(1.0, (double)rows / (double)cols));
+    case MUON_SCALE_RMS_0_2:
+      return (float)(0.2 * std::sqrt((double)std::max(rows, cols)));
+    default:
+      return 1.f;
+  }
+}
+
+// Power of two nearest sqrt(n): the stored iterate Y = alpha X keeps its
+// entries near 1 in magnitude, far from fp16's subnormal range.
+float alpha_of(int64_t n) {
+  const double e = std::round(0.5 * std::log2((double)n));
+  return (float)std::ldexp(1.0, (int)e);
+}
+
+muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
+                         const muon_plan_options* opts, PlanDesc* d) {
+  muon_plan_options o;
+  muon_default_options(&o);
+  if (opts) o = *opts;
+  if (muon_status_t st = check_options(o)) return st;
+  d->opt = o;
+  if (!shapes || n_params < 1) return fail(MUON_ERR_INVALID_ARG, "need n_params >= 1 shapes");
+  std::map<std::pair<int64_t, int64_t>, int> index;
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> members;
+  int64_t total_members = 0;
+  for (int32_t p = 0; p < n_params; ++p) {
+    const muon_shape_t& s = shapes[p];
+    int64_t E, r, c;
+    if (s.ndim == 2) { E = 1; r = s.dims[0]; c = s.dims[1]; }
+    else if (s.ndim == 3) { E = s.dims[0]; r = s.dims[1]; c = s.dims[2]; }
+    else return fail(MUON_ERR_INVALID_ARG, "parameter %d: ndim %d (need 2 or 3)", p, s.ndim);
+    if (E < 1 || r < 1 || c < 1)
+      return fail(MUON_ERR_INVALID_ARG, "parameter %d has an empty dim", p);
+    if (r > (1 << 30) || c > (1 << 30) || r * c > ((int64_t)1 << 40))
+      return fail(MUON_ERR_UNSUPPORTED, "parameter %d is too large", p);
+    d->param_E.push_back(E); d->param_rows.push_back(r); d->param_cols.push_back(c);
+    total_members += E;
+    if (total_members > INT32_MAX) return fail(MUON_ERR_INVALID_ARG, "too many members");
+    auto key = std::make_pair(r, c);
+    auto it = index.find(key);
+    int g;
+    if (it == index.end()) {
+      g = (int)members.size();
+      index[key] = g;
+      members.emplace_back();
+      GroupPlan gp;
+      gp.rows = r; gp.cols = c;
+      d->groups.push_back(gp);
+    } else {
+      g = it->second;
+    }
+    for (int64_t e = 0; e < E; ++e) members[g].push_back({p, (int32_t)e});
+  }
+  size_t off = 0;
+  int64_t first = 0;
+  const bool f32 = o.mode == MUON_MODE_FP32;
+  const int32_t thr = o.skinny_threshold == 0 ? 64 : o.skinny_threshold;
+  for (size_t g = 0; g < d->groups.size(); ++g) {
+    GroupPlan& gp = d->groups[g];
+    gp.batch = (int64_t)members[g].size();
+    if (gp.batch > 65535)
+      return fail(MUON_ERR_UNSUPPORTED, "group %zu has %lld members (max 65535)", g,
+                  (long long)gp.batch);
+    gp.first_member = first;
+    first += gp.batch;
+    for (auto& pe : members[g]) {
+      d->member_param.push_back(pe.first);
+      d->member_expert.push_back(pe.second);
+    }
+    gp.transposed = gp.rows > gp.cols;
+    gp.m = std::min(gp.rows, gp.cols);
+    gp.n = std::max(gp.rows, gp.cols);
+    gp.ns_type = f32 ? NS_F32 : (o.ns_dtype == MUON_NS_BF16 ? NS_BF16 : NS_F16);
+    gp.alpha = f32 ? 1.f : alpha_of(gp.n);
+    gp.scale = scale_of(o.scale, gp.rows, gp.cols);
+    gp.n_pitch = (int64_t)align_up((size_t)gp.n, 8);
+    gp.m_pitch = (int64_t)align_up((size_t)gp.m, 8);
+    gp.n_chunks = (gp.rows * gp.cols + kMomentumChunk - 1) / kMomentumChunk;
+    const double mm = (double)gp.m, nn = (double)gp.n;
+    gp.cost = (double)gp.batch * (4 * mm * mm * nn + 2 * mm * mm * mm + 14 * mm * nn);
+    // path
+    int32_t path = o.path_override;
+    if (f32) {
+      path = PATH_SIMT;
+    } else if (path == PATH_AUTO) {
+      const bool sk = thr > 0 && skinny_config((int32_t)gp.rows, (int32_t)gp.cols, thr, &gp.sk);
+      path = sk ? PATH_SKINNY : PATH_TENSOR;
+    } else if (path == PATH_SKINNY) {
+      if (!skinny_config((int32_t)gp.rows, (int32_t)gp.cols, 64, &gp.sk))
+        return fail(MUON_ERR_UNSUPPORTED, "group %zu [%lld,%lld] does not fit the skinny path", g,
+                    (long long)gp.rows, (long long)gp.cols);
+    }
+    gp.path = path;
+    // scratch
+    size_t o2 = 0;
+    if (path == PATH_SKINNY) {
+      gp.off_y0 = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.sk.ws_bytes, kAlign);
+      gp.off_part = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.n_chunks * 4, kAlign);
+    } else {
+      const size_t es = ns_esize(gp.ns_type);
+      const size_t yb = (size_t)gp.batch * gp.m * gp.n_pitch * es;
+      const size_t ab = (size_t)gp.batch * gp.m * gp.m_pitch * es;
+      gp.off_y0 = o2; o2 = align_up(o2 + yb, kAlign);
+      gp.off_y1 = o2; o2 = align_up(o2 + yb, kAlign);
+      gp.off_a = o2;  o2 = align_up(o2 + ab, kAlign);
+      gp.off_q = o2;  o2 = align_up(o2 + ab, kAlign);
+      gp.off_part = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.n_chunks * 4, kAlign);
+      gp.off_invn = o2; o2 = align_up(o2 + (size_t)gp.batch * 4, kAlign);
+    }
+    if (o.flags & MUON_FLAG_KEEP_UPDATE) {
+      gp.off_dbg = o2;
+      o2 = align_up(o2 + (size_t)gp.batch * gp.rows * gp.cols * 4, kAlign);
+    }
+    gp.ws_bytes = o2;
+    gp.base = off;
+    off = align_up(off + o2, kAlign);
+  }
+  d->off_scalars = off;
+  d->pb_bytes = align_up(sizeof(StepScalars), 16) + (size_t)first * sizeof(MemberPtrs);
+  off = align_up(off + d->pb_bytes, kAlign);
+  d->off_err = off;
+  off = align_up(off + 16, kAlign);
+  d->ws_bytes = off;
+  return MUON_OK;
+}
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+struct muon_plan_s {
+  PlanDesc d;
+  int device = 0;
+  unsigned char* ws = nullptr;        // device scratch
+  unsigned char* pinned = nullptr;    // kRingSlots parameter blocks
+  cudaEvent_t slot_ev[kRingSlots] = {};
+  int slot = 0;
+  cudaStream_t cap = nullptr;
+  std::vector<cudaStream_t> aux;
+  cudaEvent_t fork_ev = nullptr;
+  std::vector<cudaEvent_t> join_ev;
+  std::map<int32_t, cudaGraphExec_t> graphs;
+  std::vector<cudaEvent_t> t_start, t_stop;  // per group, MUON_FLAG_GROUP_TIMING
+  bool capturing = false;
+  // host staging (muon_step_host)
+  unsigned char* stage_p = nullptr;
+  unsigned char* stage_g = nullptr;
+  float* stage_m = nullptr;
+  std::vector<size_t> stage_off;      // element offset of each parameter
+};
+
+namespace {
+
+KArgs make_args(const muon_plan_s* p, const GroupPlan& g) {
+  KArgs a{};
+  unsigned char* base = p->ws + g.base;
+  a.sc = reinterpret_cast<const StepScalars*>(p->ws + p->d.off_scalars);
+  a.mem = reinterpret_cast<const MemberPtrs*>(p->ws + p->d.off_scalars +
+                                              align_up(sizeof(StepScalars), 16)) +
+          g.first_member;
+  a.B = (int32_t)g.batch;
+  a.rows = (int32_t)g.rows; a.cols = (int32_t)g.cols;
+  a.m = (int32_t)g.m; a.n = (int32_t)g.n;
+  a.T = g.transposed;
+  a.mode_f32 = p->d.opt.mode == MUON_MODE_FP32;
+  a.ns_type = g.ns_type;
+  a.n_pitch = g.n_pitch; a.m_pitch = g.m_pitch;
+  a.n_chunks = (int32_t)g.n_chunks;
+  a.eps = p->d.opt.eps;
+  a.scale = g.scale;
+  a.alpha = g.alpha;
+  a.y0 = base + g.off_y0;
+  a.part = reinterpret_cast<float*>(base + g.off_part);
+  if (g.path != PATH_SKINNY) {
+    a.y1 = base + g.off_y1;
+    a.A = base + g.off_a; a.Q = base + g.off_q;
+    a.invn = reinterpret_cast<float*>(base + g.off_invn);
+  }
+  a.dbg = (p->d.opt.flags & MUON_FLAG_KEEP_UPDATE) ? reinterpret_cast<float*>(base + g.off_dbg)
+                                                   : nullptr;
+  a.err = reinterpret_cast<int*>(p->ws + p->d.off_err);
+  return a;
+}
+
+// Enqueue one group's whole step on stream s.
+cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int32_t k,
+                                  cudaStream_t s) {
+  const KArgs a = make_args(p, g);
+  cudaError_t e;
+  if ((e = launch_momentum_partial(a, s))) return e;
+  if (g.path == PATH_SKINNY) return launch_skinny(a, g.sk, s);
+  if ((e = launch_norm_finalize(a, s))) return e;
+  if ((e = launch_normalize_cast(a, a.y0, s))) return e;
+  if (g.path == PATH_TENSOR) {
+    int src = 0;
+    for (int32_t it = 0; it < k; ++it) {
+      if ((e = launch_tc_gram(a, g.tc, src, s))) return e;
+      if ((e = launch_tc_poly(a, g.tc, s))) return e;
+      if ((e = launch_tc_update(a, g.tc, src, s))) return e;
+      src ^= 1;
+    }
+    return launch_write(a, src == 0 ? a.y0 : a.y1, s);
+  }
+  void* ys = a.y0;
+  void* yd = a.y1;
+  for (int32_t it = 0; it < k; ++it) {
+    if ((e = launch_simt_gram(a, ys, s))) return e;
+    if ((e = launch_simt_poly(a, s))) return e;
+    if ((e = launch_simt_update(a, ys, yd, s))) return e;
+    std::swap(ys, yd);
+  }
+  return launch_write(a, ys, s);
+}
+
+cudaError_t record(const muon_plan_s* p, cudaEvent_t ev, cudaStream_t s) {
+  return p->capturing ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                      : cudaEventRecord(ev, s);
+}
+
+cudaError_t enqueue_group(const muon_plan_s* p, size_t gi, int32_t k, cudaStream_t s) {
+  const bool timed = !p->t_start.empty();
+  cudaError_t e;
+  if (timed && (e = record(p, p->t_start[gi], s))) return e;
+  if ((e = enqueue_group_kernels(p, p->d.groups[gi], k, s))) return e;
+  if (timed && (e = record(p, p->t_stop[gi], s))) return e;
+  return cudaSuccess;
+}
+
+muon_status_t enqueue_all(muon_plan_s* p, int32_t k, cudaStream_t s, bool fork) {
+  std::vector<size_t> order(p->d.groups.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) {
+    return p->d.groups[x].cost > p->d.groups[y].cost;
+  });
+  const size_t ns = fork ? std::min(order.size(), p->aux.size() + 1) : 1;
+  if (ns > 1) {
+    CUDA_TRY(cudaEventRecord(p->fork_ev, s));
+    for (size_t i = 0; i + 1 < ns; ++i) CUDA_TRY(cudaStreamWaitEvent(p->aux[i], p->fork_ev, 0));
+  }
+  for (size_t i = 0; i < order.size(); ++i) {
+    const size_t lane = i % ns;
+    cudaStream_t st = lane == 0 ? s : p->aux[lane - 1];
+    cudaError_t e = enqueue_group(p, order[i], k, st);
+    if (e != cudaSuccess)
+      return fail(MUON_ERR_CUDA, "launch for group %zu failed: %s", order[i], cudaGetErrorString(e));
+  }
+  if (ns > 1) {
+    for (size_t i = 0; i + 1 < ns; ++i) {
+      CUDA_TRY(cudaEventRecord(p->join_ev[i], p->aux[i]));
+      CUDA_TRY(cudaStreamWaitEvent(s, p->join_ev[i], 0));
+    }
+  }
+  return MUON_OK;
+}
+
+muon_status_t get_graph(muon_plan_s* p, int32_t k, cudaGraphExec_t* out) {
+  auto it = p->graphs.find(k);
+  if (it != p->graphs.end()) { *out = it->second; return MUON_OK; }
+  CUDA_TRY(cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal));
+  p->capturing = true;
+  muon_status_t st = enqueue_all(p, k, p->cap, true);
+  p->capturing = false;
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(p->cap, &graph);
+  if (st != MUON_OK) { if (graph) cudaGraphDestroy(graph); return st; }
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "stream capture failed: %s", cudaGetErrorString(e));
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  p->graphs[k] = exec;
+  *out = exec;
+  return MUON_OK;
+}
+
+void destroy_plan(muon_plan_s* p) {
+  if (!p) return;
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  for (auto& kv : p->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& ev : p->slot_ev) if (ev) cudaEventDestroy(ev);
+  for (auto ev : p->t_start) cudaEventDestroy(ev);
+  for (auto ev : p->t_stop) cudaEventDestroy(ev);
+  if (p->fork_ev) cudaEventDestroy(p->fork_ev);
+  for (auto ev : p->join_ev) cudaEventDestroy(ev);
+  for (auto st : p->aux) cudaStreamDestroy(st);
+  if (p->cap) cudaStreamDestroy(p->cap);
+  if (p->ws) cudaFree(p->ws);
+  if (p->pinned) cudaFreeHost(p->pinned);
+  if (p->stage_p) cudaFree(p->stage_p);
+  if (p->stage_g) cudaFree(p->stage_g);
+  if (p->stage_m) cudaFree(p->stage_m);
+  delete p;
+}
+
+size_t p_esize(const muon_plan_s* p) { return p->d.opt.mode == MUON_MODE_FP32 ? 4 : 2; }
+
+int64_t param_elems(const PlanDesc& d, int32_t i) {
+  return d.param_E[i] * d.param_rows[i] * d.param_cols[i];
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status_t muon_default_options(muon_plan_options* o) {
+  if (!o) return fail(MUON_ERR_INVALID_ARG, "options pointer is NULL");
+  std::memset(o, 0, sizeof *o);
+  o->mode = MUON_MODE_BF16;
+  o->scale = MUON_SCALE_SQRT_ASPECT;
+  o->eps = 1e-7f;
+  o->skinny_threshold = 0;
+  o->ns_dtype = MUON_NS_FP16;
+  o->flags = 0;
+  o->path_override = MUON_PATH_AUTO;
+  o->max_streams = 0;
+  return MUON_OK;
+}
+
+muon_status_t muon_plan_describe(const muon_shape_t* shapes, int32_t n_params,
+                                 const muon_plan_options* opts, muon_group_info_t* groups,
+                                 int32_t group_cap, int32_t* n_groups, int32_t* member_param,
+                                 int32_t* member_expert, int64_t member_cap, int64_t* n_members,
+                                 size_t* workspace_bytes) {
+  PlanDesc d;
+  if (muon_status_t st = build_desc(shapes, n_params, opts, &d)) return st;
+  if (n_groups) *n_groups = (int32_t)d.groups.size();
+  if (groups)
+    for (int32_t g = 0; g < group_cap && g < (int32_t)d.groups.size(); ++g) {
+      const GroupPlan& gp = d.groups[g];
+      groups[g] = muon_group_info_t{gp.rows, gp.cols, gp.batch, gp.first_member,
+                                    gp.transposed, gp.path, (int64_t)gp.ws_bytes};
+    }
+  const int64_t nm = (int64_t)d.member_param.size();
+  if (n_members) *n_members = nm;
+  for (int64_t i = 0; i < member_cap && i < nm; ++i) {
+    if (member_param) member_param[i] = d.member_param[i];
+    if (member_expert) member_expert[i] = d.member_expert[i];
+  }
+  if (workspace_bytes) *workspace_bytes = d.ws_bytes;
+  return MUON_OK;
+}
+
+muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
+                               const muon_plan_options* opts, int device, muon_plan_t* out) {
+  if (!out) return fail(MUON_ERR_INVALID_ARG, "out pointer is NULL");
+  *out = nullptr;
+  muon_plan_s* p = new (std::nothrow) muon_plan_s();
+  if (!p) return fail(MUON_ERR_OOM, "host allocation failed");
+  if (muon_status_t st = build_desc(shapes, n_params, opts, &p->d)) { delete p; return st; }
+  p->device = device;
+  auto bail = [&](muon_status_t s) { destroy_plan(p); return s; };
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+    return bail(fail(MUON_ERR_INVALID_ARG, "device %d is not available", device));
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess)
+    return bail(fail(MUON_ERR_CUDA, "cudaGetDeviceProperties failed"));
+  if (prop.major != 10 || prop.minor != 3)
+    return bail(fail(MUON_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                     device, prop.major, prop.minor));
+#define PLAN_TRY(expr)                                                                    \
+  do {                                                                                    \
+    cudaError_t e_ = (expr);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return bail(fail(e_ == cudaErrorMemoryAllocation ? MUON_ERR_OOM : MUON_ERR_CUDA,    \
+                       "%s failed: %s", #expr, cudaGetErrorString(e_)));                  \
+  } while (0)
+  PLAN_TRY(cudaSetDevice(device));
+  PLAN_TRY(cudaMalloc(&p->ws, p->d.ws_bytes));
+  PLAN_TRY(cudaMemset(p->ws, 0, p->d.ws_bytes));
+  PLAN_TRY(cudaHostAlloc(&p->pinned, kRingSlots * p->d.pb_bytes, cudaHostAllocDefault));
+  for (auto& ev : p->slot_ev) PLAN_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+  PLAN_TRY(cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking));
+  const int nstreams = p->d.opt.max_streams == 0 ? 4 : p->d.opt.max_streams;
+  const int naux = std::min<int>(nstreams, (int)p->d.groups.size()) - 1;
+  for (int i = 0; i < naux; ++i) {
+    cudaStream_t s;
+    PLAN_TRY(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    p->aux.push_back(s);
+    cudaEvent_t ev;
+    PLAN_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    p->join_ev.push_back(ev);
+  }
+  PLAN_TRY(cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming));
+  if (p->d.opt.flags & MUON_FLAG_GROUP_TIMING) {
+    for (size_t g = 0; g < p->d.groups.size(); ++g) {
+      cudaEvent_t e0, e1;
+      PLAN_TRY(cudaEventCreate(&e0));
+      p->t_start.push_back(e0);
+      PLAN_TRY(cudaEventCreate(&e1));
+      p->t_stop.push_back(e1);
+    }
+  }
+  bool tc_ready[3] = {false, false, false};
+  for (GroupPlan& g : p->d.groups) {
+    if (g.path == PATH_SKINNY) PLAN_TRY(prepare_skinny(make_args(p, g), g.sk));
+    if (g.path == PATH_TENSOR) {
+      if (!tc_ready[g.ns_type]) {
+        PLAN_TRY(prepare_tc(g.ns_type));
+        tc_ready[g.ns_type] = true;
+      }
+      PLAN_TRY(tc_make_maps(make_args(p, g), &g.tc));
+    }
+  }
+  if (p->d.opt.flags & MUON_FLAG_HOST_STAGING) {
+    size_t tot = 0;
+    for (int32_t i = 0; i < (int32_t)p->d.param_E.size(); ++i) {
+      p->stage_off.push_back(tot);
+      tot += align_up((size_t)param_elems(p->d, i), 64);
+    }
+    PLAN_TRY(cudaMalloc(&p->stage_p, tot * p_esize(p)));
+    PLAN_TRY(cudaMalloc(&p->stage_g, tot * p_esize(p)));
+    PLAN_TRY(cudaMalloc(&p->stage_m, tot * 4));
+  }
+  PLAN_TRY(cudaDeviceSynchronize());
+#undef PLAN_TRY
+  *out = p;
+  return MUON_OK;
+}
+
+muon_status_t muon_step(muon_plan_t p, void* const* params, const void* const* grads,
+                        float* const* momenta, float beta, float lr, float wd, int32_t ns_steps,
+                        float a, float b, float c, void* stream) {
+  if (!p) return fail(MUON_ERR_INVALID_ARG, "plan is NULL");
+  if (!params || !grads || !momenta) return fail(MUON_ERR_INVALID_ARG, "NULL pointer array");
+  if (ns_steps < 0 || ns_steps > 1000)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps %d out of [0, 1000]", ns_steps);
+  const float sc[6] = {beta, lr, wd, a, b, c};
+  for (float v : sc)
+    if (!std::isfinite(v)) return fail(MUON_ERR_INVALID_ARG, "non-finite step scalar");
+  const int32_t np = (int32_t)p->d.param_E.size();
+  for (int32_t i = 0; i < np; ++i)
+    if (!params[i] || !grads[i] || !momenta[i])
+      return fail(MUON_ERR_INVALID_ARG, "parameter %d has a NULL pointer", i);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaSetDevice(p->device));
+  // fill the next pinned slot once its previous copy has been consumed
+  const int slot = p->slot;
+  p->slot = (p->slot + 1) % kRingSlots;
+  CUDA_TRY(cudaEventSynchronize(p->slot_ev[slot]));
+  unsigned char* host = p->pinned + (size_t)slot * p->d.pb_bytes;
+  StepScalars ss{beta, lr, wd, a, b, c, ns_steps, 0};
+  std::memcpy(host, &ss, sizeof ss);
+  MemberPtrs* mp = reinterpret_cast<MemberPtrs*>(host + align_up(sizeof(StepScalars), 16));
+  const size_t pes = p_esize(p);
+  for (size_t i = 0; i < p->d.member_param.size(); ++i) {
+    const int32_t pi = p->d.member_param[i];
+    const int64_t e = p->d.member_expert[i];
+    const int64_t off = e * p->d.param_rows[pi] * p->d.param_cols[pi];
+    mp[i].P = static_cast<unsigned char*>(params[pi]) + off * pes;
+    mp[i].G = static_cast<const unsigned char*>(grads[pi]) + off * pes;
+    mp[i].M = momenta[pi] + off;
+  }
+  CUDA_TRY(cudaMemcpyAsync(p->ws + p->d.off_scalars, host, p->d.pb_bytes, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaEventRecord(p->slot_ev[slot], s));
+  if (p->d.opt.flags & MUON_FLAG_NO_GRAPH) return enqueue_all(p, ns_steps, s, false);
+  cudaGraphExec_t exec;
+  if (muon_status_t st = get_graph(p, ns_steps, &exec)) return st;
+  CUDA_TRY(cudaGraphLaunch(exec, s));
+  return MUON_OK;
+}
+
+muon_status_t muon_step_host(muon_plan_t p, void* const* hp, const void* const* hg,
+                             float* const* hm, float beta, float lr, float wd, int32_t ns_steps,
+                             float a, float b, float c, void* stream) {
+  if (!p) return fail(MUON_ERR_INVALID_ARG, "plan is NULL");
+  if (!(p->d.opt.flags & MUON_FLAG_HOST_STAGING))
+    return fail(MUON_ERR_UNSUPPORTED, "plan was created without MUON_FLAG_HOST_STAGING");
+  if (!hp || !hg || !hm) return fail(MUON_ERR_INVALID_ARG, "NULL pointer array");
+  const int32_t np = (int32_t)p->d.param_E.size();
+  for (int32_t i = 0; i < np; ++i)
+    if (!hp[i] || !hg[i] || !hm[i])
+      return fail(MUON_ERR_INVALID_ARG, "parameter %d has a NULL pointer", i);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaSetDevice(p->device));
+  const size_t pes = p_esize(p);
+  std::vector<void*> dp(np), dg(np);
+  std::vector<float*> dm(np);
+  for (int32_t i = 0; i < np; ++i) {
+    dp[i] = p->stage_p + p->stage_off[i] * pes;
+    dg[i] = p->stage_g + p->stage_off[i] * pes;
+    dm[i] = p->stage_m + p->stage_off[i];
+  }
+  // one copy per run of parameters whose host buffers are back to back
+  auto copy_runs = [&](auto host_at, auto dev_at, size_t es, cudaMemcpyKind kind) -> muon_status_t {
+    int32_t i = 0;
+    while (i < np) {
+      int32_t j = i + 1;
+      size_t bytes = (size_t)param_elems(p->d, i) * es;
+      while (j < np && (const unsigned char*)host_at(j) == (const unsigned char*)host_at(i) + bytes &&
+             (const unsigned char*)dev_at(j) == (const unsigned char*)dev_at(i) + bytes) {
+        bytes += (size_t)param_elems(p->d, j) * es;
+        ++j;
+      }
+      if (kind == cudaMemcpyHostToDevice)
+        CUDA_TRY(cudaMemcpyAsync((void*)dev_at(i), host_at(i), bytes, kind, s));
+      else
+        CUDA_TRY(cudaMemcpyAsync((void*)host_at(i), dev_at(i), bytes, kind, s));
+      i = j;
+    }
+    return MUON_OK;
+  };
+  muon_status_t st;
+  if ((st = copy_runs([&](int32_t i) { return (const void*)hp[i]; },
+                      [&](int32_t i) { return (const void*)dp[i]; }, pes, cudaMemcpyHostToDevice)))
+    return st;
+  if ((st = copy_runs([&](int32_t i) { return (const void*)hg[i]; },
+                      [&](int32_t i) { return (const void*)dg[i]; }, pes, cudaMemcpyHostToDevice)))
+    return st;
+  if ((st = copy_runs([&](int32_t i) { return (const void*)hm[i]; },
+                      [&](int32_t i) { return (const void*)dm[i]; }, 4, cudaMemcpyHostToDevice)))
+    return st;
+  if ((st = muon_step(p, dp.data(), (const void* const*)dg.data(), dm.data(), beta, lr, wd,
+                      ns_steps, a, b, c, stream)))
+    return st;
+  if ((st = copy_runs([&](int32_t i) { return (const void*)hp[i]; },
+                      [&](int32_t i) { return (const void*)dp[i]; }, pes, cudaMemcpyDeviceToHost)))
+    return st;
+  if ((st = copy_runs([&](int32_t i) { return (const void*)hm[i]; },
+                      [&](int32_t i) { return (const void*)dm[i]; }, 4, cudaMemcpyDeviceToHost)))
+    return st;
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return MUON_OK;
+}
+
+muon_status_t muon_plan_destroy(muon_plan_t p) {
+  destroy_plan(p);
+  return MUON_OK;
+}
+
+int32_t muon_plan_num_groups(muon_plan_t p) { return p ? (int32_t)p->d.groups.size() : 0; }
+
+muon_status_t muon_plan_group_info(muon_plan_t p, int32_t g, muon_group_info_t* info) {
+  if (!p || !info) return fail(MUON_ERR_INVALID_ARG, "NULL plan or info");
+  if (g < 0 || g >= (int32_t)p->d.groups.size()) return fail(MUON_ERR_INVALID_ARG, "bad group %d", g);
+  const GroupPlan& gp = p->d.groups[g];
+  *info = muon_group_info_t{gp.rows, gp.cols, gp.batch, gp.first_member,
+                            gp.transposed, gp.path, (int64_t)gp.ws_bytes};
+  return MUON_OK;
+}
+
+size_t muon_plan_workspace_bytes(muon_plan_t p) { return p ? p->d.ws_bytes : 0; }
+
+muon_status_t muon_debug_copy_update(muon_plan_t p, int32_t param_index, int64_t expert,
+                                     float* dst) {
+  if (!p || !dst) return fail(MUON_ERR_INVALID_ARG, "NULL plan or destination");
+  if (!(p->d.opt.flags & MUON_FLAG_KEEP_UPDATE))
+    return fail(MUON_ERR_UNSUPPORTED, "plan was created without MUON_FLAG_KEEP_UPDATE");
+  if (param_index < 0 || param_index >= (int32_t)p->d.param_E.size() || expert < 0 ||
+      expert >= p->d.param_E[param_index])
+    return fail(MUON_ERR_INVALID_ARG, "bad (param, expert) = (%d, %lld)", param_index,
+                (long long)expert);
+  for (const GroupPlan& g : p->d.groups) {
+    for (int64_t i = 0; i < g.batch; ++i) {
+      const int64_t mi = g.first_member + i;
+      if (p->d.member_param[mi] == param_index && p->d.member_expert[mi] == expert) {
+        CUDA_TRY(cudaSetDevice(p->device));
+        CUDA_TRY(cudaDeviceSynchronize());
+        const size_t n = (size_t)g.rows * g.cols;
+        CUDA_TRY(cudaMemcpy(dst, p->ws + g.base + g.off_dbg + i * n * 4, n * 4,
+                            cudaMemcpyDeviceToHost));
+        return MUON_OK;
+      }
+    }
+  }
+  return fail(MUON_ERR_INVALID_ARG, "member not found");
+}
+
+muon_status_t muon_plan_group_elapsed_ms(muon_plan_t p, int32_t g, float* ms) {
+  if (!p || !ms) return fail(MUON_ERR_INVALID_ARG, "NULL plan or output");
+  if (p->t_start.empty())
+    return fail(MUON_ERR_UNSUPPORTED, "plan was created without MUON_FLAG_GROUP_TIMING");
+  if (g < 0 || g >= (int32_t)p->d.groups.size()) return fail(MUON_ERR_INVALID_ARG, "bad group %d", g);
+  CUDA_TRY(cudaEventSynchronize(p->t_stop[g]));
+  CUDA_TRY(cudaEventElapsedTime(ms, p->t_start[g], p->t_stop[g]));
+  return MUON_OK;
+}
+
+muon_status_t muon_plan_check_error(muon_plan_t p) {
+  if (!p) return fail(MUON_ERR_INVALID_ARG, "plan is NULL");
+  CUDA_TRY(cudaSetDevice(p->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  int w = 0;
+  CUDA_TRY(cudaMemcpy(&w, p->ws + p->d.off_err, sizeof w, cudaMemcpyDeviceToHost));
+  if (w != 0) {
+    const int zero = 0;
+    CUDA_TRY(cudaMemcpy(p->ws + p->d.off_err, &zero, sizeof zero, cudaMemcpyHostToDevice));
+    return fail(MUON_ERR_TIMEOUT, "a kernel gave up a bounded wait (code 0x%x)", w);
+  }
+  return MUON_OK;
+}
+
+const char* muon_status_string(muon_status_t s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_OOM: return "MUON_ERR_OOM";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+  }
+  return "MUON_ERR_UNKNOWN";
+}
+
+const char* muon_last_error(void) { return g_last_error.c_str(); }
+
+const char* muon_version(void) { return "0.1.0"; }
+
+}  // extern "C"
