@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the shape-fused Muon step on GB300 (one JSON line on rank 0).
+
+Default workload: 74 parameters of shape [24, 10240] (bf16 params/grads, fp32
+momentum), 5 quintic Newton-Schulz steps -- the fused batch the pages profile
+(«MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化, Fig. 7).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+`value` is whole-job algorithmic throughput (GB/s of the compulsory G, M, M',
+P, P' traffic for workloads of memory-bound skinny groups; TFLOP/s of
+4 m^2 n + 2 m^3 per matrix per NS step otherwise) with inputs resident in HBM.
+Timing: CUDA events on the launching stream, W untimed warm-up steps, K timed
+steps, barrier + synchronize on both sides, max over ranks.  The inputs rotate
+over several seeded copies whose total exceeds the 129 MB L2, so no step
+starts with its inputs in L2.  `e2e` times the same step through
+muon_step_host (host buffers in pinned memory, host->device and device->host
+copies inside the timed region).  `--impl reference` times the CPU oracle on
+the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused Muon step ms & TFLOP/s (or GB/s) per shape group, % roofline, 1×GB300"
+DEFAULT_CONFIG = "c2_skinny_74x24x10240"
+L2_BYTES = 129 * 2 ** 20
+
+
+def algorithmic_work(shapes, mode, k):
+    """(bytes, flops) of one step: compulsory traffic (P, G read; M read+write;
+    P write) and the dense NS flops k (4 m^2 n + 2 m^3) per matrix."""
+    pb = 4 if mode == "fp32" else 2
+    byts, flops = 0, 0
+    for s in shapes:
+        E = s[0] if len(s) == 3 else 1
+        r, c = s[-2], s[-1]
+        m, n = min(r, c), max(r, c)
+        byts += E * r * c * (pb + 4 + 4 + pb + pb)
+        flops += E * k * (4 * m * m * n + 2 * m ** 3)
+    return byts, flops
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash(name):
+    path = os.path.join(ROOT, "newton_schulz_bucket_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] if os.path.exists(path) else None
+
+
+def ncu_traffic(kernel_file, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("source_sha256_16") != kernel_source_hash(kernel_file):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"muon_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(world, v):
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(v)], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return v
+
+
+def oracle_time(w, members, host_inputs):
+    """Seconds the CPU oracle needs for `members` (list of (param, expert))."""
+    import numpy as np
+    from oracle import muon_ref
+    f32 = lambda v: float(np.float32(v))
+    a, b, c = (f32(v) for v in w.coeffs)
+    t0 = time.perf_counter()
+    for (i, e) in members:
+        P, G, M = host_inputs(i, e)
+        muon_ref.muon_update_ref(P, G, M, f32(w.beta), f32(w.lr), f32(w.wd), w.ns_steps, a, b, c)
+    return time.perf_counter() - t0
+
+
+def sample_members(w, budget_s=12.0):
+    """Seeded sample of members sized so the oracle runs for about budget_s."""
+    import random
+    mem = [(i, e) for i, s in enumerate(w.shapes) for e in range(s[0] if len(s) == 3 else 1)]
+    rng = random.Random(1234)
+    order = mem[:]
+    rng.shuffle(order)
+    tot = 0.0
+    out = []
+    for (i, e) in order:
+        r, c = w.shapes[i][-2:]
+        m, n = min(r, c), max(r, c)
+        cost = w.ns_steps * (4 * m * m * n + 2 * m ** 3) / 2.5e10 + r * c * 1e-8
+        if out and tot + cost > budget_s:
+            break
+        out.append((i, e))
+        tot += cost
+    return out
+
+
+def host_member_inputs(w):
+    """Host fp64 inputs of single members drawn from the same laws (for timing
+    the oracle; the values need not match the GPU draw)."""
+    from newton_schulz_bucket_gb300 import workloads as W
+    cache = {}
+
+    def get(i, e):
+        if i not in cache:
+            sub = W.custom([w.shapes[i]], mode=w.mode, seed=w.seed + i)
+            P, G, M = W.make_tensors(sub, "cpu")
+            cache.clear()
+            cache[i] = [t.float().double().numpy() for t in (P[0], G[0], M[0])]
+        P, G, M = cache[i]
+        if P.ndim == 3:
+            return P[e], G[e], M[e]
+        return P, G, M
+    return get
+
+
+def headline(w, byts, flops, seconds):
+    """GB/s for workloads of skinny groups only, else TFLOP/s."""
+    from newton_schulz_bucket_gb300 import describe
+    paths = {g["path"] for g in describe(w.shapes, mode=w.mode)["groups"]}
+    if paths <= {"skinny"}:
+        return byts / seconds / 1e9, "GB/s"
+    return flops / seconds / 1e12, "TFLOP/s"
+
+
+def run_reference(args, w, world, rank):
+    """--impl reference: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
+    members = sample_members(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    frac = len(members) / sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
+    get = host_member_inputs(w)
+    for _ in range(args.warmup):
+        oracle_time(w, members[:1], get)
+    times = [oracle_time(w, members, get) for _ in range(args.steps)]
+    per_step = statistics.mean(times) / frac  # extrapolated to the whole workload
+    value, unit = headline(w, byts, flops, per_step)
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "ns_steps": w.ns_steps},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": f"{len(members)} of {round(len(members) / frac)} matrices "
+                                       "per step, extrapolated linearly by matrix count"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def describe_shapes(shapes):
+    from collections import Counter
+    c = Counter(tuple(s) for s in shapes)
+    return ", ".join(f"{n}x{list(s)}" for s, n in c.items())
+
+
+def run_e2e(args, w, pkg, torch, dev, local, byts, flops, world):
+    """Same step through muon_step_host: H2D of P, G, M and D2H of P', M'
+    inside the timed region."""
+    from newton_schulz_bucket_gb300 import workloads as W
+    P, G, M = W.make_tensors(w, dev)
+    hP = torch.cat([t.reshape(-1) for t in P]).cpu().pin_memory()
+    hG = torch.cat([t.reshape(-1) for t in G]).cpu().pin_memory()
+    hM = torch.cat([t.reshape(-1) for t in M]).cpu().pin_memory()
+    del P, G, M
+
+    def views(flat):
+        out, o = [], 0
+        for s in w.shapes:
+            n = math.prod(s)
+            out.append(flat[o:o + n].view(*s))
+            o += n
+        return out
+    vP, vG, vM = views(hP), views(hG), views(hM)
+    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, host_staging=True)
+    stream = torch.cuda.Stream(dev)
+    for _ in range(max(2, args.warmup // 2)):
+        plan.step_host(vP, vG, vM, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs, stream=stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    n = max(3, args.steps // 2)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n):
+        plan.step_host(vP, vG, vM, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = allmax(world, ev0.elapsed_time(ev1)) / n
+    plan.close()
+    v, u = headline(w, byts, flops, ms / 1e3)
+    pb = 2 if w.mode == "bf16" else 4
+    el = sum(math.prod(s) for s in w.shapes)
+    return {"value": v * world, "unit": u, "ms_per_step": ms,
+            "h2d_bytes_per_step": el * (pb + pb + 4), "d2h_bytes_per_step": el * (pb + 4)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--ns-steps", type=int, default=None)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from newton_schulz_bucket_gb300 import workloads as W
+    w = W.get(args.config, args.ns_steps)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        return
+
+    import torch
+    import newton_schulz_bucket_gb300 as pkg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
+    in_bytes = sum(math.prod(s) for s in w.shapes) * (8 if w.mode == "bf16" else 12)
+    n_sets = max(1, min(4, math.ceil(2 * L2_BYTES / in_bytes) + 1))
+    sets = [W.make_tensors(W.Workload(**{**w.__dict__, "seed": w.seed + 100 * j}), dev)
+            for j in range(n_sets)]
+    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, group_timing=True)
+    groups = plan.groups()
+    stream = torch.cuda.Stream(dev)
+    coeffs = w.coeffs
+
+    def step(j):
+        P, G, M = sets[j % n_sets]
+        plan.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=stream)
+
+    for j in range(args.warmup):
+        step(j)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    gtimes = [[] for _ in groups]
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        ev0.record(stream)
+        for j in range(args.steps):
+            step(j)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        ms_total = ev0.elapsed_time(ev1)
+        # per-group kernel times from events recorded inside the step graph
+        for j in range(min(args.steps, 2 * n_sets)):
+            step(j)
+            for g in range(len(groups)):
+                gtimes[g].append(plan.group_elapsed_ms(g))
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = allmax(world, ms_total)
+    ms_step = ms_total / args.steps
+    sec = ms_step / 1e3
+    value_1, unit = headline(w, byts, flops, sec)
+    value = value_1 * world  # every rank ran the same-sized workload (weak scaling)
+
+    peaks = load_peaks()
+    per_group = []
+    for g, info in enumerate(groups):
+        shp = [info["rows"], info["cols"]]
+        gb, gf = algorithmic_work([[info["batch"]] + shp], w.mode, w.ns_steps)
+        gms = statistics.mean(gtimes[g]) if gtimes[g] else None
+        ent = {"shape": shp, "batch": info["batch"], "path": info["path"], "ms": gms}
+        if gms:
+            ent["matrices_per_s"] = info["batch"] / (gms / 1e3)
+            if info["path"] == "skinny":
+                ach = gb / (gms / 1e3) / 1e9
+                ent.update({"GB_s": ach, "roofline_frac": ach / peaks["hbm_gbs"], "bound": "hbm"})
+            else:
+                ach = gf / (gms / 1e3) / 1e12
+                ent.update({"TFLOP_s": ach, "roofline_frac": ach / peaks["bf16_tflops_sustained"],
+                            "bound": "tensor"})
+        per_group.append(ent)
+
+    dom = max(range(len(groups)), key=lambda g: per_group[g]["ms"] or 0)
+    dg = per_group[dom]
+    if dg["path"] == "skinny":
+        roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dg.get("roofline_frac"),
+                "kernel": "skinny group (k_momentum_partial + k_skinny_ns)",
+                "traffic": ncu_traffic("k_skinny.cu", w.name),
+                "peak_source": peaks["source"] + " hbm_gbs (burst copy)"}
+    else:
+        roof = {"bound": "tensor", "achieved": dg.get("TFLOP_s"), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": dg.get("roofline_frac"),
+                "kernel": f"group {dg['shape']} chain (k_tc_gemm)",
+                "traffic": None, "peak_source": peaks["source"] + " bf16_tflops_sustained"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, pkg, torch, dev, local, byts, flops, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        members = sample_members(w, budget_s=12.0)
+        frac = len(members) / sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
+        get = host_member_inputs(w)
+        t = oracle_time(w, members, get) / frac
+        cv, cu = headline(w, byts, flops, t)
+        cpu = {"value": cv, "unit": cu, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{len(members)} matrices of the workload, extrapolated by matrix count",
+               "ms_per_step": t * 1e3}
+
+    launches = plan.kernels_per_step(w.ns_steps) * args.steps
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.mode == "bf16" else "f32",
+                "data": "synthetic: seeded Gaussian G, M0 (std 1e-3), P (std 0.02)",
+                "config": {"workload": w.name, "shapes": describe_shapes(w.shapes),
+                           "ns_steps": w.ns_steps, "coeffs": list(w.coeffs),
+                           "ns_operands": "fp16 (fp32 accumulate)",
+                           "l2": f"inputs rotate over {n_sets} seeded copies "
+                                 f"({n_sets * in_bytes / 1e6:.0f} MB > L2)",
+                           "parallelism": f"replicas x{world}"},
+                "matrices_per_s": sum(g["batch"] for g in groups) * world / sec,
+                "tflops": flops * world / sec / 1e12, "gbs": byts * world / sec / 1e9,
+                "per_group": per_group, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk.summary(),
+                "wall_s_timed": t_wall}
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+"""GPU parity: the C-ABI path against the CPU oracle on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import newton_schulz_bucket_gb300 as pkg
+from newton_schulz_bucket_gb300 import workloads as W
+
+from parity import F32, GpuRun, check_all
+
+pytestmark = pytest.mark.gpu
+
+
+def test_c1_fp32_64x128():
+    run = GpuRun(W.get("c1_fp32_64x128"))
+    assert run.plan.groups()[0]["path"] == "simt"
+    errs = check_all(run)
+    assert max(errs) <= 1e-4
+    run.close()
+
+
+def test_c2_skinny_74x24x10240_all_members():
+    run = GpuRun(W.get("c2_skinny_74x24x10240"))
+    g = run.plan.groups()
+    assert len(g) == 1 and g[0]["batch"] == 74 and g[0]["path"] == "skinny"
+    errs = check_all(run)
+    assert max(errs) <= 2e-2
+    run.close()
+
+
+SKINNY_SHAPES = [
+    [[24, 10240]],
+    [[3, 24, 1000]],             # ragged last CTA slice
+    [[10240, 24], [4096, 8]],    # transposed (rows > cols)
+    [[64, 7168]],                # m = 64
+    [[17, 333]],                 # odd dims: scalar (unaligned) access path
+    [[1, 64], [64, 1]],          # single row / column
+    [[48, 2048], [40, 96]],
+    [[5, 16], [16, 16]],
+    [[2, 33, 70]],               # 3-D, odd
+]
+
+
+@pytest.mark.parametrize("shapes", SKINNY_SHAPES, ids=lambda s: "x".join("_".join(map(str, t)) for t in s))
+def test_skinny_shapes(shapes):
+    run = GpuRun(W.custom(shapes, seed=7))
+    for g in run.plan.groups():
+        assert g["path"] == "skinny", g
+    check_all(run)
+    run.close()
+
+
+@pytest.mark.parametrize("shapes", [[[128, 384], [200, 130]], [[2, 70, 33]], [[256, 256]]])
+def test_simt_path_bf16_mode(shapes):
+    run = GpuRun(W.custom(shapes, seed=8), path="simt")
+    check_all(run)
+    run.close()
+
+
+@pytest.mark.parametrize("shapes", [[[24, 700], [700, 24]], [[9, 40]]])
+def test_fp32_mode_small(shapes):
+    run = GpuRun(W.custom(shapes, mode="fp32", g_std=1.0, p_std=1.0, seed=9))
+    check_all(run)
+    run.close()
+
+
+def test_bf16_ns_operands_k5():
+    w = W.custom([[24, 10240]] * 4 + [[64, 7168]], seed=10)
+    run = GpuRun(w, ns_dtype="bf16")
+    check_all(run)
+    run.close()
+
+
+def test_scale_mode_rms():
+    run = GpuRun(W.custom([[24, 4096], [4096, 24]], seed=11), scale="rms_0_2")
+    check_all(run, scale_mode="rms_0_2")
+    run.close()
+
+
+def test_ns_steps_zero_and_ten():
+    for k in (0, 10):
+        w = W.custom([[24, 10240], [3, 40, 640]], seed=12, ns_steps=k)
+        run = GpuRun(w)
+        check_all(run)
+        run.close()
+
+
+def test_zero_gradient_and_momentum():
+    w = W.custom([[24, 2048]], seed=13, g_std=0.0, m_zero=True)
+    run = GpuRun(w)
+    O = run.O(0)
+    assert np.all(O == 0)
+    want = (torch.tensor(run.p0(0), dtype=torch.float32) * F32(1 - F32(w.lr) * F32(w.wd)))
+    want = want.to(torch.bfloat16).double().numpy()
+    assert np.array_equal(run.p1(0), want) or np.max(np.abs(run.p1(0) - want)) <= \
+        np.max(np.abs(want)) * 2 ** -8
+    run.close()
+
+
+def _member_tensors(w, idx):
+    """Inputs of a sub-workload made of members `idx` of w (exact copies)."""
+    P, G, M = W.make_tensors(w, "cuda")
+    return [P[i].clone() for i in idx], [G[i].clone() for i in idx], [M[i].clone() for i in idx]
+
+
+def test_batch_invariance_bitwise():
+    """A member computed inside a batch of 74 equals the same member computed
+    alone, and inside a batch of 7, bit for bit (P', M' and O)."""
+    w = W.get("c2_skinny_74x24x10240")
+    full = GpuRun(w)
+    for idx in ([5], [0, 3, 5, 11, 40, 41, 73]):
+        sub = W.custom([w.shapes[i] for i in idx], seed=0)
+        sub.beta, sub.lr, sub.wd = w.beta, w.lr, w.wd
+        run = GpuRun(sub, tensors=_member_tensors(w, idx))
+        for j, i in enumerate(idx):
+            assert np.array_equal(run.p1(j), full.p1(i))
+            assert np.array_equal(run.m1(j), full.m1(i))
+            assert np.array_equal(run.O(j), full.O(i))
+        run.close()
+    full.close()
+
+
+def test_graph_replay_equals_direct_launch():
+    w = W.custom([[24, 10240]] * 3 + [[96, 200]] + [[2, 64, 64]], seed=14)
+    a = GpuRun(w)
+    b = GpuRun(w, no_graph=True)
+    for (i, e) in a.members:
+        assert np.array_equal(a.p1(i, e), b.p1(i, e))
+        assert np.array_equal(a.m1(i, e), b.m1(i, e))
+    a.close(); b.close()
+
+
+def test_three_steps_match_oracle_iterated():
+    from oracle import muon_ref
+    w = W.custom([[24, 4096], [4096, 24]], seed=15)
+    run = GpuRun(w, steps=3)
+    a, b, c = run.coeffs
+    for i, shp in enumerate(w.shapes):
+        P, M = run.p0(i), run.m0(i)
+        for _ in range(3):
+            P, M, O = muon_ref.muon_update_ref(P, run.g0(i), M, F32(w.beta), F32(w.lr), F32(w.wd),
+                                               w.ns_steps, a, b, c)
+            P = torch.tensor(P, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+            M = M.astype(np.float32).astype(np.float64)
+        assert np.max(np.abs(run.m1(i) - M)) <= 1e-5 * np.max(np.abs(M))
+        dP_ref, dP = P - run.p0(i), run.p1(i) - run.p0(i)
+        assert np.linalg.norm(dP - dP_ref) / np.linalg.norm(dP_ref) <= 3e-2
+    run.close()
+
+
+def test_step_host_equals_device_step():
+    w = W.custom([[24, 10240]] * 5 + [[2, 24, 10240]], seed=16)
+    P, G, M = W.make_tensors(w, "cuda")
+    hP = [t.cpu().pin_memory() for t in P]
+    hG = [t.cpu().pin_memory() for t in G]
+    hM = [t.cpu().pin_memory() for t in M]
+    dev = pkg.MuonPlan(w.shapes)
+    host = pkg.MuonPlan(w.shapes, host_staging=True)
+    c = tuple(F32(v) for v in w.coeffs)
+    dev.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, c)
+    host.step_host(hP, hG, hM, w.beta, w.lr, w.wd, w.ns_steps, c)
+    torch.cuda.synchronize()
+    for i in range(len(P)):
+        assert torch.equal(P[i].cpu(), hP[i])
+        assert torch.equal(M[i].cpu(), hM[i])
+    dev.close(); host.close()
+
+
+def test_group_timing_events():
+    w = W.custom([[24, 4096]] * 4 + [[256, 512]] * 2, seed=18)
+    P, G, M = W.make_tensors(w, "cuda")
+    plan = pkg.MuonPlan(w.shapes, group_timing=True)
+    plan.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs)
+    for g in range(len(plan.groups())):
+        assert 0.0 < plan.group_elapsed_ms(g) < 1000.0
+    plan.close()
+
+
+def test_argument_errors():
+    w = W.custom([[24, 512]], seed=17)
+    P, G, M = W.make_tensors(w, "cuda")
+    plan = pkg.MuonPlan(w.shapes)
+    with pytest.raises(ValueError):
+        plan.step([p.float() for p in P], G, M, 0.9, 0.1, 0.0)
+    with pytest.raises(ValueError):
+        plan.step(P, G, [m[:, :256] for m in M], 0.9, 0.1, 0.0)
+    with pytest.raises(pkg.MuonError) as ei:
+        plan.step(P, G, M, 0.9, 0.1, 0.0, ns_steps=-1)
+    assert ei.value.status == 1
+    with pytest.raises(pkg.MuonError):
+        plan.step(P, G, M, float("nan"), 0.1, 0.0)
+    with pytest.raises(pkg.MuonError) as ei:
+        plan.debug_update(0)
+    assert ei.value.status == 2  # plan made without keep_update
+    plan.step(P, G, M, 0.9, 0.1, 0.0)
+    plan.check_error()
+    plan.close()
