@@ -90,8 +90,9 @@ cudaError_t launch_simt_update(const KArgs& a, const void* ysrc, void* ydst, cud
 bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg);
 cudaError_t prepare_skinny(const KArgs& a, const SkinnyCfg& cfg);  // function attributes
 cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s);
-// Clusters of the skinny kernel that fit on the device at once (after prepare).
-int skinny_max_active_clusters(int ns_type, int mtiles);
+// Clusters of the skinny kernel for min dim m that fit on the device at once
+// (after prepare_skinny for that m).
+int skinny_max_active_clusters(int ns_type, int m);
 
 // TENSOR path: tcgen05 GEMMs fed by TMA.  Tensor maps are encoded once per
 // group at plan creation (they hold the workspace addresses).

@@ -120,7 +120,7 @@ template <> struct Mma<__nv_bfloat16> {
 // Gram tiles (m16 x n8) touching the upper triangle, in a fixed order.
 template <int MT>
 struct GramTiles {
-  static constexpr int count() {
+  __host__ __device__ static constexpr int count() {
     int c = 0;
     for (int mi = 0; mi < MT; ++mi)
       for (int nj = 0; nj < 2 * MT; ++nj)
@@ -128,16 +128,20 @@ struct GramTiles {
     return c;
   }
   static constexpr int N = count();
-  __device__ __forceinline__ static void tile(int t, int& mi, int& nj) {
+  __host__ __device__ static constexpr int code(int t) {  // mi * 16 + nj of the t-th tile
     int c = 0;
-#pragma unroll
     for (int a = 0; a < MT; ++a)
-#pragma unroll
       for (int b = 0; b < 2 * MT; ++b)
         if (b * 8 + 7 >= a * 16) {
-          if (c == t) { mi = a; nj = b; }
+          if (c == t) return a * 16 + b;
           ++c;
         }
+    return 0;
+  }
+  __device__ __forceinline__ static void tile(int t, int& mi, int& nj) {
+    const int v = code(t);
+    mi = v >> 4;
+    nj = v & 15;
   }
 };
 
@@ -148,9 +152,8 @@ struct NsSmem {
   static constexpr int MP = 16 * MT;
   static constexpr int NW = NT / 32;
   static constexpr int LB = 32 * MT;  // stage bytes per lane and block
-  // rounds in flight; MT <= 2 fits two CTAs per SM, so every cluster of a
-  // batch of up to ~76 members is resident at once
-  static constexpr int S = MT == 1 ? 8 : (MT == 2 ? 5 : (MT == 3 ? 4 : 2));
+  // rounds in flight per warp (MT <= 2 runs 16 warps per CTA)
+  static constexpr int S = MT == 1 ? 4 : (MT == 2 ? 3 : (MT == 3 ? 4 : 2));
   static constexpr int kStage = 0;
   static constexpr int kWarpPart = kStage + S * NW * 32 * LB;
   static constexpr int kCta = kWarpPart + NW * GramTiles<MT>::N * 128 * 4;
@@ -176,8 +179,232 @@ struct Wide {
   }
 };
 
-template <typename TY, int MT, int NT>
-__global__ void __launch_bounds__(NT, (MT <= 2 ? 2 : 1)) k_skinny_ns(KArgs a, SkArgs s) {
+enum PassKind { PASS_FIRST = 0, PASS_MID = 1, PASS_LAST = 2, PASS_ONLY = 3 };
+
+// Per-thread state shared by the passes of one member.
+template <int MT>
+struct PassCtx {
+  int lane, warp, g, t4, m, n, c0, NB;
+  bool pairs;              // M' / P pairs are adjacent and aligned (fast path)
+  bool rv[MT][2];          // row 16 mi + g + 8 h is inside the matrix
+  int64_t roff[MT][2];     // element offset of (row, column 2 t4) when `pairs`
+  const float* Mp;
+  __nv_bfloat16* P;
+  float* dbg;
+  uint8_t* ws;             // this CTA's fragment blocks
+  Wide wd;
+  float inv, decay, coef, inv_alpha;
+};
+
+// One pass over this warp's 16-column blocks (blk = warp + r * NW):
+//   FIRST: fragments from M' * inv, next Gram, store fragments
+//   MID:   Y <- Q Y, next Gram, store fragments
+//   LAST:  Y <- Q Y, P' = P decay - coef Y
+//   ONLY:  fragments from M' * inv, P' = P decay - coef Y   (k = 0)
+// Operands of the next S rounds stream into this lane's planes of a shared
+// ring with cp.async; a lane only reads back what it copied, so the passes
+// need no block barrier.  Plane offsets (bytes, lane 0): M' pair k at
+// k * 256, fragment tile mi at mi * 512, P pair k at MT * 512 + k * 128.
+template <int KIND, typename TY, int MT, int NT, bool HALF>
+__device__ __forceinline__ void run_pass(const PassCtx<MT>& c, uint8_t* stage_warp,
+                                         const uint32_t (&qf)[MT][MT][4], float (&gacc)[GramTiles<MT>::N][4]) {
+  using L = NsSmem<MT, NT>;
+  using GT = GramTiles<MT>;
+  constexpr int NW = L::NW, S = L::S, LB = L::LB;
+  constexpr bool kFromM = KIND == PASS_FIRST || KIND == PASS_ONLY;
+  constexpr bool kWriteP = KIND == PASS_LAST || KIND == PASS_ONLY;
+  constexpr bool kUpdate = KIND == PASS_MID || KIND == PASS_LAST;
+  constexpr int kBlk = (MT - 1) * 512 + (HALF ? 256 : 512);
+  constexpr uint32_t kSlot = NW * 32 * LB;  // bytes of one round of the ring
+  auto full_tile = [](int mi) { return !(HALF && mi == MT - 1); };
+  auto toff = [](int mi) { return mi * 512; };
+  const int lane = c.lane;
+  const bool stream_p = c.pairs && KIND == PASS_LAST;
+  const int rounds = (c.NB + NW - 1) / NW;
+  const uint32_t ring0 = static_cast<uint32_t>(__cvta_generic_to_shared(stage_warp));
+
+  auto issue = [&](int r, uint32_t dst) {
+    const int blk = r * NW + c.warp;
+    if (r < rounds && blk < c.NB) {
+      const int jb = c.c0 + blk * 16;
+      const bool fullblk = jb + 16 <= c.n;
+      if (kFromM) {
+        if (c.pairs) {
+#pragma unroll
+          for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (!full_tile(mi) && (q & 1)) continue;
+              const int dj = (q & 2) ? 8 : 0;
+              const bool ok = c.rv[mi][q & 1] && (fullblk || jb + 2 * c.t4 + dj + 1 < c.n);
+              cp_async8(dst + (mi * 4 + q) * 256 + lane * 8,
+                        ok ? (const void*)(c.Mp + c.roff[mi][q & 1] + jb + dj) : (const void*)c.Mp,
+                        ok ? 8 : 0);
+            }
+        }
+      } else {
+        const uint8_t* wsb = c.ws + (int64_t)blk * kBlk;
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          if (full_tile(mi))
+            cp_async16(dst + mi * 512 + lane * 16, wsb + toff(mi) + lane * 16, 16);
+          else
+            cp_async8(dst + mi * 512 + lane * 8, wsb + toff(mi) + lane * 8, 8);
+        }
+      }
+      if (KIND == PASS_LAST && stream_p) {
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (!full_tile(mi) && (q & 1)) continue;
+            const int dj = (q & 2) ? 8 : 0;
+            const bool ok = c.rv[mi][q & 1] && (fullblk || jb + 2 * c.t4 + dj + 1 < c.n);
+            cp_async4(dst + MT * 512 + (mi * 4 + q) * 128 + lane * 4,
+                      ok ? (const void*)(c.P + c.roff[mi][q & 1] + jb + dj) : (const void*)c.P,
+                      ok ? 4 : 0);
+          }
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
+
+  int slot = 0;
+  for (int r = 0; r < rounds; ++r) {
+    cp_async_wait<S - 1>();
+    const int blk = r * NW + c.warp;
+    const uint32_t dst = ring0 + slot * kSlot;
+    const uint8_t* st = stage_warp + slot * kSlot;
+    if (blk < c.NB) {
+      const int jb = c.c0 + blk * 16;
+      const bool fullblk = jb + 16 <= c.n;
+      uint8_t* wsb = c.ws + (int64_t)blk * kBlk;
+      uint32_t y[MT][4];
+      if (kFromM) {
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float v0 = 0.f, v1 = 0.f;
+            if (!full_tile(mi) && (q & 1)) {
+              y[mi][q] = 0u;
+              continue;
+            }
+            if (c.pairs) {
+              const float2 f = *reinterpret_cast<const float2*>(st + (mi * 4 + q) * 256 + lane * 8);
+              v0 = f.x; v1 = f.y;
+            } else {
+              const int i = mi * 16 + c.g + ((q & 1) ? 8 : 0);
+              const int j = jb + 2 * c.t4 + ((q & 2) ? 8 : 0);
+              if (i < c.m) {
+                if (j < c.n) v0 = c.Mp[c.wd.off(i, j)];
+                if (j + 1 < c.n) v1 = c.Mp[c.wd.off(i, j + 1)];
+              }
+            }
+            y[mi][q] = Mma<TY>::pack(v0 * c.inv, v1 * c.inv);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          if (full_tile(mi)) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + mi * 512 + lane * 16);
+            y[mi][0] = v.x; y[mi][1] = v.y; y[mi][2] = v.z; y[mi][3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(st + mi * 512 + lane * 8);
+            y[mi][0] = v.x; y[mi][1] = 0u; y[mi][2] = v.y; y[mi][3] = 0u;
+          }
+        }
+      }
+      if (kUpdate) {
+        // Y <- Q Y: B operand rows are iterate rows, so transpose 8x8 blocks
+        uint32_t bt[MT][4];
+#pragma unroll
+        for (int kk = 0; kk < MT; ++kk)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            bt[kk][q] = (!full_tile(kk) && (q & 1)) ? 0u : movtrans(y[kk][q]);
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < MT; ++kk) {
+            Mma<TY>::run(d0, qf[mi][kk], bt[kk][0], bt[kk][1]);  // columns 0..7
+            Mma<TY>::run(d1, qf[mi][kk], bt[kk][2], bt[kk][3]);  // columns 8..15
+          }
+          y[mi][0] = Mma<TY>::pack(d0[0], d0[1]);
+          y[mi][1] = Mma<TY>::pack(d0[2], d0[3]);
+          y[mi][2] = Mma<TY>::pack(d1[0], d1[1]);
+          y[mi][3] = Mma<TY>::pack(d1[2], d1[3]);
+        }
+      }
+      if (!kWriteP) {
+        // next Gram: Y Y^T over this block, upper tiles, B operand = rows of Y
+#pragma unroll
+        for (int q = 0; q < GT::N; ++q) {
+          const int mi = GT::code(q) >> 4, nj = GT::code(q) & 15;
+          const uint32_t* src = y[nj >> 1];
+          Mma<TY>::run(gacc[q], y[mi], (nj & 1) ? src[1] : src[0], (nj & 1) ? src[3] : src[2]);
+        }
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          if (full_tile(mi))
+            *reinterpret_cast<uint4*>(wsb + toff(mi) + lane * 16) =
+                make_uint4(y[mi][0], y[mi][1], y[mi][2], y[mi][3]);
+          else
+            *reinterpret_cast<uint2*>(wsb + toff(mi) + lane * 8) = make_uint2(y[mi][0], y[mi][2]);
+        }
+      } else {
+        // P' = P (1 - lr wd) - lr s Y / alpha on the valid elements
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (!full_tile(mi) && (q & 1)) continue;
+            const int dj = (q & 2) ? 8 : 0;
+            if (!c.rv[mi][q & 1]) continue;
+            const float2 yv = Mma<TY>::unpack(y[mi][q]);
+            if (c.pairs) {
+              if (!fullblk && jb + 2 * c.t4 + dj >= c.n) continue;
+              __nv_bfloat16* pp = c.P + c.roff[mi][q & 1] + jb + dj;
+              uint32_t praw = stream_p ? *reinterpret_cast<const uint32_t*>(
+                                             st + MT * 512 + (mi * 4 + q) * 128 + lane * 4)
+                                       : *reinterpret_cast<const uint32_t*>(pp);
+              const float2 pf = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&praw));
+              *reinterpret_cast<__nv_bfloat162*>(pp) = __floats2bfloat162_rn(
+                  fmaf(-c.coef, yv.x, pf.x * c.decay), fmaf(-c.coef, yv.y, pf.y * c.decay));
+              if (c.dbg)
+                *reinterpret_cast<float2*>(c.dbg + c.roff[mi][q & 1] + jb + dj) =
+                    make_float2(yv.x * c.inv_alpha, yv.y * c.inv_alpha);
+            } else {
+              const int i = mi * 16 + c.g + ((q & 1) ? 8 : 0);
+              const int j = jb + 2 * c.t4 + dj;
+              if (j >= c.n) continue;
+              const int64_t o0 = c.wd.off(i, j);
+              c.P[o0] = __float2bfloat16_rn(fmaf(-c.coef, yv.x, __bfloat162float(c.P[o0]) * c.decay));
+              if (c.dbg) c.dbg[o0] = yv.x * c.inv_alpha;
+              if (j + 1 < c.n) {
+                const int64_t o1 = c.wd.off(i, j + 1);
+                c.P[o1] = __float2bfloat16_rn(fmaf(-c.coef, yv.y, __bfloat162float(c.P[o1]) * c.decay));
+                if (c.dbg) c.dbg[o1] = yv.y * c.inv_alpha;
+              }
+            }
+          }
+        }
+      }
+    }
+    // the slot of round r was consumed above (registers): refill it with r + S
+    issue(r + S, dst);
+    slot = slot + 1 == S ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
+template <typename TY, int MT, int NT, bool HALF>
+__global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   using L = NsSmem<MT, NT>;
   using GT = GramTiles<MT>;
   constexpr int MP = L::MP, NW = L::NW;
@@ -189,20 +416,31 @@ __global__ void __launch_bounds__(NT, (MT <= 2 ? 2 : 1)) k_skinny_ns(KArgs a, Sk
   float* misc = reinterpret_cast<float*>(smem + L::kMisc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t4 = lane & 3;
   const uint32_t rank = cluster_rank();
   const int b = blockIdx.x / kCL;
-  const int m = a.m, n = a.n;
-  const int c0 = (int)rank * s.W;
+  const int m = a.m;
   const MemberPtrs mp = a.mem[b];
-  const float* Mp = mp.M;
-  __nv_bfloat16* P = static_cast<__nv_bfloat16*>(mp.P);
-  const Wide wd{a.cols, a.T};
+
+  PassCtx<MT> c;
+  c.lane = lane; c.warp = warp; c.g = lane >> 2; c.t4 = lane & 3;
+  c.m = m; c.n = a.n; c.c0 = (int)rank * s.W; c.NB = s.NB;
+  c.Mp = mp.M;
+  c.P = static_cast<__nv_bfloat16*>(mp.P);
+  c.wd = Wide{a.cols, a.T};
   // pairs (i, j), (i, j+1) are adjacent in memory (fast path) when the wide
   // iterate is the parameter itself, its rows are even and bases are aligned
-  const bool pairs = !a.T && (a.cols % 2 == 0) &&
-                     ((reinterpret_cast<uintptr_t>(Mp) | reinterpret_cast<uintptr_t>(P)) & 7) == 0;
-  uint8_t* ws = s.ws + ((int64_t)b * kCL + rank) * s.NB * s.blk;
+  c.pairs = !a.T && (a.cols % 2 == 0) &&
+            ((reinterpret_cast<uintptr_t>(c.Mp) | reinterpret_cast<uintptr_t>(c.P)) & 7) == 0;
+  c.ws = s.ws + ((int64_t)b * kCL + rank) * s.NB * s.blk;
+  c.dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+#pragma unroll
+  for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = mi * 16 + c.g + 8 * h;
+      c.rv[mi][h] = i < m;
+      c.roff[mi][h] = (int64_t)i * a.cols + 2 * c.t4;
+    }
 
   // Q = 0 outside the m x m block; zero once
   for (int e = tid; e < MP * (MP + 8); e += NT) Qs[e] = from_f32<TY>(0.f);
@@ -210,235 +448,31 @@ __global__ void __launch_bounds__(NT, (MT <= 2 ? 2 : 1)) k_skinny_ns(KArgs a, Sk
   if (tid == 0) {
     const float* pp = a.part + (int64_t)b * a.n_chunks;
     float s2 = 0.f;
-    for (int c = 0; c < a.n_chunks; ++c) s2 += pp[c];
+    for (int k = 0; k < a.n_chunks; ++k) s2 += pp[k];
     misc[0] = a.alpha / (sqrtf(s2) + a.eps);
   }
   __syncthreads();
-  const float inv = misc[0];
+  c.inv = misc[0];
 
   const int ns = a.sc->ns_steps;
   const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
   const float inv_a2 = 1.f / (a.alpha * a.alpha);
   const float lr = a.sc->lr, wdk = a.sc->wd;
-  const float decay = 1.f - lr * wdk;
-  const float inv_alpha = 1.f / a.alpha;
-  const float coef = lr * a.scale * inv_alpha;
-  float* dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+  c.decay = 1.f - lr * wdk;
+  c.inv_alpha = 1.f / a.alpha;
+  c.coef = lr * a.scale * c.inv_alpha;
+  uint8_t* stage_warp = smem + L::kStage + warp * 32 * L::LB;
 
-  // rows of m16 tile mi that hold data; a tile with <= 8 stores only a0, a2
-  auto tile_off = [&](int mi) {
-    int o = 0;
-    for (int q = 0; q < mi; ++q) o += (m - 16 * q > 8) ? 512 : 256;
-    return o;
-  };
-
-  // pass p = 0: fragments from M' / norm;  0 < p: Y <- Q Y;  p = k: write P
-  for (int p = 0; p <= ns; ++p) {
-    const bool first = p == 0, last = p == ns;
-    uint32_t qf[MT][MT][4];
-    if (!first) {
-      const uint32_t qb = smem_u32(Qs);
-#pragma unroll
-      for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-        for (int kk = 0; kk < MT; ++kk)
-          ldsm_x4(qb + 2u * ((mi * 16 + (lane & 15)) * (MP + 8) + kk * 16 + (lane >> 4) * 8),
-                  qf[mi][kk]);
-    }
-    float gacc[GT::N][4];
+  uint32_t qf[MT][MT][4];
+  float gacc[GT::N][4];
+  auto zero_gacc = [&]() {
 #pragma unroll
     for (int q = 0; q < GT::N; ++q) gacc[q][0] = gacc[q][1] = gacc[q][2] = gacc[q][3] = 0.f;
-
-    // Round r: warp w handles block r * NW + w.  Each lane streams its own
-    // operands of the next S rounds into a shared-memory ring with cp.async
-    // (fragments, or M' pairs in the first pass, plus P pairs in the last),
-    // and reads back only what it copied, so no block barrier is needed.
-    constexpr int S = L::S, LB = L::LB;
-    const int rounds = (s.NB + NW - 1) / NW;
-    const bool stream_pairs = pairs;                // aligned pair layout: M' via cp.async
-    const bool stream_p = pairs && last && !first;  // P pairs via cp.async (own stage area)
-    // Stage of one warp and round: 32 * LB bytes as "planes", each plane
-    // holding one 4/8/16-byte item for all 32 lanes contiguously, so fills and
-    // reads are bank-conflict free.  Plane offsets (bytes, for lane 0):
-    //   first pass : M' pair k       at k * 256          (k < 4 MT)
-    //   later      : fragment tile mi at mi * 512         (16 or 8 bytes / lane)
-    //   last pass  : P pair k        at MT * 512 + k * 128
-    const uint32_t stage0 = smem_u32(smem + L::kStage) + (uint32_t)(warp * 32 * LB);
-    auto slot = [&](int r) { return stage0 + (uint32_t)((r % S) * NW * 32 * LB); };
-    auto issue = [&](int r) {
-      const int blk = r * NW + warp;
-      if (r < rounds && blk < s.NB) {
-        const uint32_t dst = slot(r);
-        const int jb = c0 + blk * 16;
-        if (first) {
-          if (stream_pairs) {
-#pragma unroll
-            for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int i = mi * 16 + g + ((q & 1) ? 8 : 0);
-                const int j = jb + 2 * t4 + ((q & 2) ? 8 : 0);
-                const bool ok = i < m && j + 1 < n;
-                cp_async8(dst + (mi * 4 + q) * 256 + lane * 8,
-                          ok ? (const void*)(Mp + wd.off(i, j)) : (const void*)Mp, ok ? 8 : 0);
-              }
-          }
-        } else {
-          const uint8_t* wsb = ws + (int64_t)blk * s.blk;
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi) {
-            const int o = tile_off(mi);
-            if (m - 16 * mi > 8)
-              cp_async16(dst + mi * 512 + lane * 16, wsb + o + lane * 16, 16);
-            else
-              cp_async8(dst + mi * 512 + lane * 8, wsb + o + lane * 8, 8);
-          }
-        }
-        if (stream_p) {
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int i = mi * 16 + g + ((q & 1) ? 8 : 0);
-              const int j = jb + 2 * t4 + ((q & 2) ? 8 : 0);
-              const bool ok = i < m && j + 1 < n;
-              cp_async4(dst + MT * 512 + (mi * 4 + q) * 128 + lane * 4,
-                        ok ? (const void*)(P + wd.off(i, j)) : (const void*)P, ok ? 4 : 0);
-            }
-        }
-      }
-      cp_async_commit();
-    };
-#pragma unroll
-    for (int r = 0; r < S; ++r) issue(r);
-
-    for (int r = 0; r < rounds; ++r) {
-      cp_async_wait<S - 1>();
-      const int blk = r * NW + warp;
-      if (blk < s.NB) {
-        const int jb = c0 + blk * 16;
-        uint8_t* wsb = ws + (int64_t)blk * s.blk;
-        const uint8_t* st = smem + L::kStage + (r % S) * NW * 32 * LB + warp * 32 * LB;
-        uint32_t y[MT][4];
-        uint32_t pv[MT][4];  // last pass: P pairs (bf16x2)
-        if (first) {
-          // fragment registers from M' (fp32) scaled by alpha / ||M'||
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int i = mi * 16 + g + ((q & 1) ? 8 : 0);
-              const int j = jb + 2 * t4 + ((q & 2) ? 8 : 0);
-              float v0 = 0.f, v1 = 0.f;
-              if (stream_pairs) {
-                const float2 f = *reinterpret_cast<const float2*>(st + (mi * 4 + q) * 256 + lane * 8);
-                v0 = f.x; v1 = f.y;
-              } else if (i < m) {
-                if (j < n) v0 = Mp[wd.off(i, j)];
-                if (j + 1 < n) v1 = Mp[wd.off(i, j + 1)];
-              }
-              y[mi][q] = Mma<TY>::pack(v0 * inv, v1 * inv);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi) {
-            if (m - 16 * mi > 8) {
-              const uint4 v = *reinterpret_cast<const uint4*>(st + mi * 512 + lane * 16);
-              y[mi][0] = v.x; y[mi][1] = v.y; y[mi][2] = v.z; y[mi][3] = v.w;
-            } else {
-              const uint2 v = *reinterpret_cast<const uint2*>(st + mi * 512 + lane * 8);
-              y[mi][0] = v.x; y[mi][1] = 0u; y[mi][2] = v.y; y[mi][3] = 0u;
-            }
-          }
-          // Y <- Q Y: B operand rows are iterate rows, so transpose 8x8 blocks
-          uint32_t bt[MT][4];
-#pragma unroll
-          for (int kk = 0; kk < MT; ++kk)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) bt[kk][q] = movtrans(y[kk][q]);
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi) {
-            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < MT; ++kk) {
-              Mma<TY>::run(d0, qf[mi][kk], bt[kk][0], bt[kk][1]);  // columns 0..7
-              Mma<TY>::run(d1, qf[mi][kk], bt[kk][2], bt[kk][3]);  // columns 8..15
-            }
-            y[mi][0] = Mma<TY>::pack(d0[0], d0[1]);
-            y[mi][1] = Mma<TY>::pack(d0[2], d0[3]);
-            y[mi][2] = Mma<TY>::pack(d1[0], d1[1]);
-            y[mi][3] = Mma<TY>::pack(d1[2], d1[3]);
-          }
-        }
-        if (stream_p) {
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              pv[mi][q] = *reinterpret_cast<const uint32_t*>(st + MT * 512 + (mi * 4 + q) * 128 +
-                                                            lane * 4);
-        }
-        if (!last) {
-          // next Gram: Y Y^T over this block, upper tiles, B operand = rows of Y
-#pragma unroll
-          for (int q = 0; q < GT::N; ++q) {
-            int mi = 0, nj = 0;
-            GT::tile(q, mi, nj);
-            const uint32_t* src = y[nj >> 1];
-            const uint32_t b0 = (nj & 1) ? src[1] : src[0];
-            const uint32_t b1 = (nj & 1) ? src[3] : src[2];
-            Mma<TY>::run(gacc[q], y[mi], b0, b1);
-          }
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi) {
-            const int o = tile_off(mi);
-            if (m - 16 * mi > 8)
-              *reinterpret_cast<uint4*>(wsb + o + lane * 16) =
-                  make_uint4(y[mi][0], y[mi][1], y[mi][2], y[mi][3]);
-            else
-              *reinterpret_cast<uint2*>(wsb + o + lane * 8) = make_uint2(y[mi][0], y[mi][2]);
-          }
-        } else {
-          // P' = P (1 - lr wd) - lr s Y / alpha on the valid elements
-#pragma unroll
-          for (int mi = 0; mi < MT; ++mi) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int i = mi * 16 + g + ((q & 1) ? 8 : 0);
-              const int j = jb + 2 * t4 + ((q & 2) ? 8 : 0);
-              if (i >= m || j >= n) continue;
-              const float2 yv = Mma<TY>::unpack(y[mi][q]);
-              if (pairs && j + 1 < n) {
-                uint32_t praw = stream_p ? pv[mi][q]
-                                         : *reinterpret_cast<const uint32_t*>(P + wd.off(i, j));
-                const float2 pf = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&praw));
-                *reinterpret_cast<__nv_bfloat162*>(P + wd.off(i, j)) = __floats2bfloat162_rn(
-                    fmaf(-coef, yv.x, pf.x * decay), fmaf(-coef, yv.y, pf.y * decay));
-                if (dbg)
-                  *reinterpret_cast<float2*>(dbg + wd.off(i, j)) =
-                      make_float2(yv.x * inv_alpha, yv.y * inv_alpha);
-              } else {
-                const int64_t o0 = wd.off(i, j);
-                P[o0] = __float2bfloat16_rn(fmaf(-coef, yv.x, __bfloat162float(P[o0]) * decay));
-                if (dbg) dbg[o0] = yv.x * inv_alpha;
-                if (j + 1 < n) {
-                  const int64_t o1 = wd.off(i, j + 1);
-                  P[o1] = __float2bfloat16_rn(fmaf(-coef, yv.y, __bfloat162float(P[o1]) * decay));
-                  if (dbg) dbg[o1] = yv.y * inv_alpha;
-                }
-              }
-            }
-          }
-        }
-      }
-      // the slot of round r was consumed above (registers): refill it
-      issue(r + S);
-    }
-    cp_async_wait<0>();
-    if (last) break;
-
-    // ---- reduce the Gram partials: warps (fixed order), then CTAs (rank order)
+  };
+  // sum the Gram partials (warps in fixed order, then CTAs in rank order),
+  // form Q = a I + b A + c A A in fp32 and load its fragments
+  auto reduce_and_poly = [&](int p) {
+    const int g = c.g, t4 = c.t4;
 #pragma unroll
     for (int q = 0; q < GT::N; ++q) {
       float* dst = wpart + (warp * GT::N + q) * 128;
@@ -453,9 +487,8 @@ __global__ void __launch_bounds__(NT, (MT <= 2 ? 2 : 1)) k_skinny_ns(KArgs a, Sk
       const int q = e >> 7, w = e & 127;
       float acc = 0.f;
       for (int k = 0; k < NW; ++k) acc += wpart[(k * GT::N + q) * 128 + w];
-      int mi = 0, nj = 0;
-      GT::tile(q, mi, nj);
-      cp[(mi * 16 + (w >> 3)) * MP + nj * 8 + (w & 7)] = acc;
+      const int code = GT::code(q);
+      cp[((code >> 4) * 16 + (w >> 3)) * MP + (code & 15) * 8 + (w & 7)] = acc;
     }
     cluster_sync();
     for (int e = tid; e < m * m; e += NT) {
@@ -469,7 +502,6 @@ __global__ void __launch_bounds__(NT, (MT <= 2 ? 2 : 1)) k_skinny_ns(KArgs a, Sk
       Af[j * MP + i] = acc;
     }
     __syncthreads();
-    // Q = a I + b A + c A A (fp32), cast to the operand type
     for (int e = tid; e < m * m; e += NT) {
       const int i = e / m, j = e - (e / m) * m;
       if (i > j) continue;
@@ -482,14 +514,35 @@ __global__ void __launch_bounds__(NT, (MT <= 2 ? 2 : 1)) k_skinny_ns(KArgs a, Sk
       Qs[j * (MP + 8) + i] = qh;
     }
     __syncthreads();
+    const uint32_t qb = smem_u32(Qs);
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+      for (int kk = 0; kk < MT; ++kk)
+        ldsm_x4(qb + 2u * ((mi * 16 + (lane & 15)) * (MP + 8) + kk * 16 + (lane >> 4) * 8),
+                qf[mi][kk]);
+  };
+
+  zero_gacc();
+  if (ns == 0) {
+    run_pass<PASS_ONLY, TY, MT, NT, HALF>(c, stage_warp, qf, gacc);
+  } else {
+    run_pass<PASS_FIRST, TY, MT, NT, HALF>(c, stage_warp, qf, gacc);
+    for (int p = 1; p < ns; ++p) {
+      reduce_and_poly(p - 1);
+      zero_gacc();
+      run_pass<PASS_MID, TY, MT, NT, HALF>(c, stage_warp, qf, gacc);
+    }
+    reduce_and_poly(ns - 1);
+    run_pass<PASS_LAST, TY, MT, NT, HALF>(c, stage_warp, qf, gacc);
   }
   // the peer may still read this CTA's Gram partial
   cluster_sync();
 }
 
-template <typename TY, int MT, int NT>
+template <typename TY, int MT, int NT, bool HALF>
 cudaError_t launch_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
-  auto fn = k_skinny_ns<TY, MT, NT>;
+  auto fn = k_skinny_ns<TY, MT, NT, HALF>;
   constexpr int smem = NsSmem<MT, NT>::kTotal;
   if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   SkArgs s;
@@ -512,14 +565,23 @@ cudaError_t launch_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool
   return cudaLaunchKernelEx(&lc, fn, a, s);
 }
 
+template <typename TY, bool HALF>
+cudaError_t launch_th(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
+  switch (cfg.mtiles) {
+    case 1: return launch_t<TY, 1, 512, HALF>(a, cfg, st, prep);
+    case 2: return launch_t<TY, 2, 512, HALF>(a, cfg, st, prep);
+    case 3: return launch_t<TY, 3, 256, HALF>(a, cfg, st, prep);
+    default: return launch_t<TY, 4, 256, HALF>(a, cfg, st, prep);
+  }
+}
+
+// HALF: the last m16 tile holds at most 8 rows (stored as half a tile)
+bool half_last_tile(int m, int mtiles) { return m - 16 * (mtiles - 1) <= 8; }
+
 template <typename TY>
 cudaError_t launch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
-  switch (cfg.mtiles) {
-    case 1: return launch_t<TY, 1, 256>(a, cfg, st, prep);
-    case 2: return launch_t<TY, 2, 256>(a, cfg, st, prep);
-    case 3: return launch_t<TY, 3, 256>(a, cfg, st, prep);
-    default: return launch_t<TY, 4, 256>(a, cfg, st, prep);
-  }
+  return half_last_tile(a.m, cfg.mtiles) ? launch_th<TY, true>(a, cfg, st, prep)
+                                         : launch_th<TY, false>(a, cfg, st, prep);
 }
 
 cudaError_t dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
@@ -528,13 +590,14 @@ cudaError_t dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool
                              : launch_ty<__nv_bfloat16>(a, cfg, st, prep);
 }
 
-template <typename TY, int MT>
+template <typename TY, int MT, bool HALF>
 int clusters_of() {
-  auto fn = k_skinny_ns<TY, MT, 256>;
+  constexpr int NT = MT <= 2 ? 512 : 256;
+  auto fn = k_skinny_ns<TY, MT, NT, HALF>;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(kCL * 1024);
-  lc.blockDim = dim3(256);
-  lc.dynamicSmemBytes = NsSmem<MT, 256>::kTotal;
+  lc.blockDim = dim3(NT);
+  lc.dynamicSmemBytes = NsSmem<MT, NT>::kTotal;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = kCL;
@@ -546,6 +609,16 @@ int clusters_of() {
   return cudaOccupancyMaxActiveClusters(&n, fn, &lc) == cudaSuccess ? n : -1;
 }
 
+template <typename TY, bool HALF>
+int clusters_mt(int mtiles) {
+  switch (mtiles) {
+    case 1: return clusters_of<TY, 1, HALF>();
+    case 2: return clusters_of<TY, 2, HALF>();
+    case 3: return clusters_of<TY, 3, HALF>();
+    default: return clusters_of<TY, 4, HALF>();
+  }
+}
+
 }  // namespace
 
 bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg) {
@@ -553,7 +626,7 @@ bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg) {
   if (m < 1 || m > max_m || m > 64) return false;
   cfg->mtiles = (m + 15) / 16;
   cfg->cluster = kCL;
-  cfg->threads = 256;
+  cfg->threads = cfg->mtiles <= 2 ? 512 : 256;
   const int w = (n + kCL - 1) / kCL;
   cfg->width = (w + 15) / 16 * 16;
   int blk = 0;
@@ -572,20 +645,11 @@ cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s) 
   return dispatch(a, cfg, s, false);
 }
 
-int skinny_max_active_clusters(int ns_type, int mtiles) {
-  if (ns_type == NS_F16)
-    switch (mtiles) {
-      case 1: return clusters_of<__half, 1>();
-      case 2: return clusters_of<__half, 2>();
-      case 3: return clusters_of<__half, 3>();
-      default: return clusters_of<__half, 4>();
-    }
-  switch (mtiles) {
-    case 1: return clusters_of<__nv_bfloat16, 1>();
-    case 2: return clusters_of<__nv_bfloat16, 2>();
-    case 3: return clusters_of<__nv_bfloat16, 3>();
-    default: return clusters_of<__nv_bfloat16, 4>();
-  }
+int skinny_max_active_clusters(int ns_type, int m) {
+  const int mt = (m + 15) / 16;
+  const bool half = half_last_tile(m, mt);
+  if (ns_type == NS_F16) return half ? clusters_mt<__half, true>(mt) : clusters_mt<__half, false>(mt);
+  return half ? clusters_mt<__nv_bfloat16, true>(mt) : clusters_mt<__nv_bfloat16, false>(mt);
 }
 
 }  // namespace muon

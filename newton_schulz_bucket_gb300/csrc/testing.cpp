@@ -58,7 +58,8 @@ extern "C" int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m)
   SkinnyCfg cfg;
   if (!skinny_config((int32_t)m, 1024, 64, &cfg)) return -1;
   KArgs k{};
+  k.m = (int32_t)m;
   k.ns_type = ns_dtype == MUON_NS_BF16 ? NS_BF16 : NS_F16;
   if (prepare_skinny(k, cfg) != cudaSuccess) return -1;
-  return skinny_max_active_clusters(k.ns_type, cfg.mtiles);
+  return skinny_max_active_clusters(k.ns_type, (int)m);
 }
