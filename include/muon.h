@@ -214,6 +214,32 @@ MUON_API muon_status_t muon_plan_group_elapsed_ms(muon_plan_t plan, int32_t grou
  * (the word is then cleared). */
 MUON_API muon_status_t muon_plan_check_error(muon_plan_t plan);
 
+/* The skinny-path step (min(rows, cols) <= 64) for callers that cannot
+ * allocate device memory -- for example code inside a framework whose caching
+ * allocator forbids outside cudaMalloc calls, latency-critical loops that must
+ * not enter the driver's allocator, or embedded deployments that fix every
+ * device buffer at start-up.  The pages have no counterpart to this call; it
+ * exists for those callers.  It applies the update at the top of this file to
+ * the `batch` matrices of one [batch, rows, cols] parameter in BF16 mode with
+ * fp16 Newton-Schulz operands, and gives the same results as muon_step on a
+ * plan made of that one parameter (same kernels, same reduction orders).
+ * params (bf16), grads (bf16) and momenta (fp32) are the caller's device
+ * buffers, updated in place as in muon_step.  All scratch lives in one static
+ * device array of 8 MiB inside the library: every GPU that loads the library
+ * keeps it until the process exits, it is shared by every call (calls whose
+ * work overlaps on a GPU race -- issue them on one stream), and a request
+ * needing more (about 8 members of [24, 10240]) fails with
+ * MUON_ERR_INVALID_ARG and a message giving both sizes.  It calls no
+ * allocator.  The first call on each device looks up the array's device
+ * address and sets kernel attributes (host work): make that first call before
+ * any stream capture.  Errors: INVALID_ARG (NULL pointer, bad size, scalar or
+ * scale_mode, too much scratch), UNSUPPORTED (min(rows, cols) > 64), CUDA. */
+MUON_API muon_status_t muon_step_skinny_static(void* params, const void* grads, float* momenta,
+                                               int32_t batch, int64_t rows, int64_t cols,
+                                               float beta, float lr, float wd, int32_t ns_steps,
+                                               float a, float b, float c, float eps,
+                                               int32_t scale_mode, void* stream);
+
 MUON_API const char* muon_status_string(muon_status_t status);
 MUON_API const char* muon_last_error(void);
 /* Library version, e.g. "0.1.0". */

@@ -58,7 +58,8 @@ EXPORTED_TESTING = ["muon_testing_tc_gemm", "muon_testing_skinny_max_clusters"]
 EXPORTED = ["muon_default_options", "muon_plan_describe", "muon_plan_create", "muon_step",
             "muon_step_host", "muon_plan_destroy", "muon_plan_num_groups",
             "muon_plan_group_info", "muon_plan_workspace_bytes", "muon_debug_copy_update",
-            "muon_plan_check_error", "muon_plan_group_elapsed_ms", "muon_status_string",
+            "muon_plan_check_error", "muon_plan_group_elapsed_ms", "muon_step_skinny_static",
+            "muon_status_string",
             "muon_last_error", "muon_version"]
 
 _lib = None
@@ -99,6 +100,9 @@ def load() -> C.CDLL:
     L.muon_debug_copy_update.argtypes = [vp, i32, i64, vp]
     L.muon_plan_check_error.argtypes = [vp]
     L.muon_plan_group_elapsed_ms.argtypes = [vp, i32, C.POINTER(C.c_float)]
+    L.muon_step_skinny_static.argtypes = [vp, vp, vp, i32, i64, i64, f32, f32, f32, i32, f32,
+                                          f32, f32, f32, i32, vp]
+    L.muon_step_skinny_static.restype = C.c_int
     L.muon_testing_tc_gemm.argtypes = [i32, i32, i32, i64, i64, vp, vp, vp, vp, f32, f32, f32,
                                        f32, vp]
     L.muon_testing_tc_gemm.restype = C.c_int

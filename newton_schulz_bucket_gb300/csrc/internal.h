@@ -71,6 +71,9 @@ struct SkinnyCfg {
   int64_t ws_bytes;  // fragment workspace bytes per member
 };
 
+// Sets the thread-local message muon_last_error() returns.
+void set_last_error(const char* msg);
+
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t launch_momentum_partial(const KArgs& a, cudaStream_t s);
 cudaError_t launch_norm_finalize(const KArgs& a, cudaStream_t s);

@@ -1,0 +1,154 @@
+// muon_step_skinny_static: the skinny-path step for callers that cannot
+// allocate device memory.
+//
+// Some callers cannot call cudaMalloc at step time or at all: code running
+// inside a framework's pooled or capped allocator that forbids foreign
+// allocations, real-time loops that must not block on the driver's allocator,
+// and embedded hosts that fix all device memory up front.  For them this entry
+// point runs the same momentum and Newton-Schulz kernels as the SKINNY path
+// of muon_step, but keeps every byte of scratch (the scalar/pointer table, the
+// momentum kernel's partial sums and the fragment-ordered iterate) in one
+// file-scope device array of kStaticScratchBytes.  The array is part of the
+// library image: every GPU that loads the library holds it until the process
+// exits.  Every call uses the same array, so two calls whose kernels overlap
+// on a GPU race (serialise them on one stream).  No byte of the array needs to
+// start at zero: each call writes every location it later reads.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/muon.h"
+#include "internal.h"
+
+namespace muon {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch per device, looked up once with that
+// device current (the array's host-side name is not a device address).
+unsigned char* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_setup_mu;
+
+// Errors are reported through muon_last_error(), like every other entry point.
+muon_status_t static_fail(muon_status_t st, const char* msg) {
+  char buf[320];
+  std::snprintf(buf, sizeof buf, "muon_step_skinny_static: %s", msg);
+  set_last_error(buf);
+  return st;
+}
+
+// One thread fills the step scalars and the member pointer table from the
+// kernel's own arguments (so the call needs neither an allocation nor a host
+// staging buffer).
+__global__ void k_static_setup(StepScalars sc, void* P, const void* G, float* M, int batch,
+                               int64_t per, StepScalars* sc_out, MemberPtrs* mem_out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  *sc_out = sc;
+  for (int b = 0; b < batch; ++b) {
+    mem_out[b].P = static_cast<__nv_bfloat16*>(P) + b * per;
+    mem_out[b].G = static_cast<const __nv_bfloat16*>(G) + b * per;
+    mem_out[b].M = M + b * per;
+  }
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads, float* momenta,
+                                                 int32_t batch, int64_t rows, int64_t cols,
+                                                 float beta, float lr, float wd, int32_t ns_steps,
+                                                 float a, float b, float c, float eps,
+                                                 int32_t scale_mode, void* stream) {
+  if (!params || !grads || !momenta)
+    return static_fail(MUON_ERR_INVALID_ARG, "params, grads and momenta must be non-NULL");
+  if (batch < 1 || rows < 1 || cols < 1 || rows > (1 << 30) || cols > (1 << 30))
+    return static_fail(MUON_ERR_INVALID_ARG, "batch, rows and cols must be >= 1");
+  if (ns_steps < 0 || ns_steps > 1000)
+    return static_fail(MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 1000]");
+  const float sv[7] = {beta, lr, wd, a, b, c, eps};
+  for (float v : sv)
+    if (!std::isfinite(v)) return static_fail(MUON_ERR_INVALID_ARG, "non-finite scalar");
+  if (eps < 0.f) return static_fail(MUON_ERR_INVALID_ARG, "eps must be >= 0");
+  if (scale_mode < MUON_SCALE_SQRT_ASPECT || scale_mode > MUON_SCALE_NONE)
+    return static_fail(MUON_ERR_INVALID_ARG, "scale_mode is not a muon_scale_t");
+  SkinnyCfg cfg;
+  if (!skinny_config((int32_t)rows, (int32_t)cols, 64, &cfg))
+    return static_fail(MUON_ERR_UNSUPPORTED, "min(rows, cols) must be <= 64 (skinny path)");
+
+  const int64_t m = rows < cols ? rows : cols, n = rows < cols ? cols : rows;
+  const int64_t n_chunks = (rows * cols + kMomentumChunk - 1) / kMomentumChunk;
+  // scratch layout: scalars | member table | partial sums | fragment iterate
+  const size_t off_mem = align256(sizeof(StepScalars));
+  const size_t off_part = align256(off_mem + (size_t)batch * sizeof(MemberPtrs));
+  const size_t off_ws = align256(off_part + (size_t)batch * n_chunks * sizeof(float));
+  const size_t total = off_ws + (size_t)batch * cfg.ws_bytes;
+  if (total > kStaticScratchBytes) {
+    char msg[200];
+    std::snprintf(msg, sizeof msg,
+                  "needs %zu bytes of scratch for batch %d of [%lld, %lld]; the static array "
+                  "holds %zu",
+                  total, batch, (long long)rows, (long long)cols, kStaticScratchBytes);
+    return static_fail(MUON_ERR_INVALID_ARG, msg);
+  }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return static_fail(MUON_ERR_CUDA, "cudaGetDevice failed");
+  KArgs k{};
+  k.B = batch;
+  k.rows = (int32_t)rows;
+  k.cols = (int32_t)cols;
+  k.m = (int32_t)m;
+  k.n = (int32_t)n;
+  k.T = rows > cols;
+  k.mode_f32 = 0;
+  k.ns_type = NS_F16;
+  k.n_chunks = (int32_t)n_chunks;
+  k.eps = eps;
+  k.scale = scale_mode == MUON_SCALE_SQRT_ASPECT
+                ? (float)std::sqrt(std::max(1.0, (double)rows / (double)cols))
+                : (scale_mode == MUON_SCALE_RMS_0_2 ? (float)(0.2 * std::sqrt((double)n)) : 1.f);
+  k.alpha = (float)std::ldexp(1.0, (int)std::round(0.5 * std::log2((double)n)));
+  {
+    // once per device, with that device current: the array's device address
+    // and the kernel attributes (host work only; do it before stream capture)
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_scratch_addr[dev]) {
+      void* ptr = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+      if (e != cudaSuccess || !ptr)
+        return static_fail(MUON_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+      g_scratch_addr[dev] = static_cast<unsigned char*>(ptr);
+    }
+    if (prepare_skinny(k, cfg) != cudaSuccess)
+      return static_fail(MUON_ERR_CUDA, "setting the skinny kernel's attributes failed");
+  }
+  unsigned char* base = g_scratch_addr[dev];
+  StepScalars* sc = reinterpret_cast<StepScalars*>(base);
+  MemberPtrs* mem = reinterpret_cast<MemberPtrs*>(base + off_mem);
+  k.sc = sc;
+  k.mem = mem;
+  k.part = reinterpret_cast<float*>(base + off_part);
+  k.y0 = base + off_ws;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const StepScalars hs{beta, lr, wd, a, b, c, ns_steps, 0};
+  k_static_setup<<<1, 32, 0, s>>>(hs, params, grads, momenta, batch, rows * cols, sc, mem);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_momentum_partial(k, s);
+  if (e == cudaSuccess) e = launch_skinny(k, cfg, s);
+  if (e != cudaSuccess) return static_fail(MUON_ERR_CUDA, cudaGetErrorString(e));
+  return MUON_OK;
+}

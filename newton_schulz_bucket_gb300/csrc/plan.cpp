@@ -235,6 +235,9 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 }  // namespace muon
 
 using namespace muon;
