@@ -383,10 +383,13 @@ def main():
     dom = max(range(len(groups)), key=lambda g: per_group[g]["ms"] or 0)
     dg = per_group[dom]
     if dg["path"] == "skinny":
+        gram_space = min(groups[dom]["rows"], groups[dom]["cols"]) <= 32 and w.ns_steps <= 64
+        kfile = "k_skinny_gs.cu" if gram_space else "k_skinny.cu"
         roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dg.get("roofline_frac"),
-                "kernel": "skinny group (k_momentum_partial + k_skinny_ns)",
-                "traffic": ncu_traffic("k_skinny.cu", w.name),
+                "kernel": ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"
+                           if gram_space else "k_momentum_partial + k_skinny_ns"),
+                "traffic": ncu_traffic(kfile, w.name),
                 "peak_source": peaks["source"] + " hbm_gbs (burst copy)"}
     else:
         roof = {"bound": "tensor", "achieved": dg.get("TFLOP_s"), "peak": peaks["bf16_tflops_sustained"],

@@ -204,7 +204,11 @@ class MuonPlan:
         """Number of this library's kernel launches in one step."""
         n = 0
         for g in self.groups():
-            n += 2 if g["path"] == "skinny" else 4 + 3 * int(ns_steps)
+            if g["path"] == "skinny":
+                # one fused kernel in Gram space (m <= 32, up to 64 steps), else momentum + iteration
+                n += 1 if min(g["rows"], g["cols"]) <= 32 and ns_steps <= 64 else 2
+            else:
+                n += 4 + 3 * int(ns_steps)
         return n
 
     def check_error(self) -> None:

@@ -83,6 +83,38 @@ __device__ __forceinline__ uint4 ld_cs(const void* p) {   // read once, then ove
 __device__ __forceinline__ void st_cs(void* p, const uint4& v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
+__device__ __forceinline__ void st_u4(void* p, const uint4& v) {  // re-read soon: keep in L2
+  *reinterpret_cast<uint4*>(p) = v;
+}
+// L2 eviction priorities.  A policy from createpolicy rides on each access;
+// evict_last lines outlive evict_normal / evict_first ones under pressure.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_hint(const void* p, uint64_t pol) {  // read-only data
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_hint(void* p, const uint4& v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void u4_to_f4x2(const uint4& lo, const uint4& hi, float* f) {
   f[0] = __uint_as_float(lo.x); f[1] = __uint_as_float(lo.y);
   f[2] = __uint_as_float(lo.z); f[3] = __uint_as_float(lo.w);

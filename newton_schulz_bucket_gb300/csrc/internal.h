@@ -58,6 +58,7 @@ struct KArgs {
   float* invn;             // [B] alpha / (||M'||_F + eps)
   float* dbg;              // nullable: [B][rows][cols] fp32 copy of O
   int* err;                // device error word
+  int32_t l2_keep_m;       // momentum kernel stores M' evict-last (it is read back soon, twice)
 };
 
 // Skinny path configuration of a group (a function of (rows, cols) only).
@@ -68,8 +69,13 @@ struct SkinnyCfg {
   int32_t mtiles;    // ceil(m / 16)
   int32_t smem;      // unused (shared memory is fixed per instantiation)
   int32_t blk;       // bytes of one 16-column block in the fragment workspace
-  int64_t ws_bytes;  // fragment workspace bytes per member
+  int64_t ws_bytes;  // fragment workspace bytes per member (direct kernel)
+  int32_t gram_space;  // m <= 32: the Gram-space kernel serves ns_steps <= kGramSpaceMaxSteps
 };
+
+// Step counts the Gram-space kernel takes: along an exact null direction of
+// X_0 its m x m product Pi_k grows like a^k (3.4445^64 < 2^115 stays in fp32).
+constexpr int32_t kGramSpaceMaxSteps = 64;
 
 // Sets the thread-local message muon_last_error() returns.
 void set_last_error(const char* msg);
@@ -88,11 +94,16 @@ cudaError_t launch_simt_gram(const KArgs& a, const void* y, cudaStream_t s);
 cudaError_t launch_simt_poly(const KArgs& a, cudaStream_t s);
 cudaError_t launch_simt_update(const KArgs& a, const void* ysrc, void* ydst, cudaStream_t s);
 
-// Skinny path: momentum kernel, then Newton-Schulz + write per member in one
-// cluster, iterate in a fragment-ordered workspace (a.y0).
+// Skinny path, the whole step of a group: for m <= 32 and k <=
+// kGramSpaceMaxSteps one kernel (momentum, then Newton-Schulz in Gram space,
+// then the write, one cluster per member, no workspace); otherwise the
+// momentum kernel, then the direct iteration (iterate in a fragment-ordered
+// workspace a.y0).
 bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg);
 cudaError_t prepare_skinny(const KArgs& a, const SkinnyCfg& cfg);  // function attributes
-cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s);
+cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, int32_t ns_steps, cudaStream_t s);
+cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare);
+int gs_max_active_clusters(int ns_type, int m);
 // Clusters of the skinny kernel for min dim m that fit on the device at once
 // (after prepare_skinny for that m).
 int skinny_max_active_clusters(int ns_type, int m);

@@ -13,19 +13,10 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <typename TP>
-__device__ __forceinline__ void load8(const TP* p, float* f);
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float* f) {
-  bf16x8_to_f32(ldg_nc(p), f);
-}
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float* f) {
-  u4_to_f4x2(ldg_nc(p), ldg_nc(p + 4), f);
-}
-
 // One CTA = one fixed chunk of one member: M' = beta M + G (stored), and the
-// chunk's sum of squares of M' (fixed-order tree) into part[b][chunk].
+// chunk's sum of squares of M' (fixed-order tree) into part[b][chunk].  G and
+// M are read once (evict-first in L2).  M' is stored evict-last when the next
+// kernel reads it back twice (skinny path), so it is still in L2 then.
 template <typename TG>
 __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
   __shared__ float red[33];
@@ -39,6 +30,15 @@ __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
   const float beta = a.sc->beta;
   float acc = 0.f;
   const bool vec = aligned16(G) && aligned16(M);
+  const uint64_t pin = l2_evict_first();
+  const uint64_t pout = a.l2_keep_m ? l2_evict_last() : l2_evict_normal();
+  auto load8g = [&](const TG* p, float* f) {
+    if constexpr (sizeof(TG) == 2) {
+      bf16x8_to_f32(ld_hint(p, pin), f);
+    } else {
+      u4_to_f4x2(ld_hint(p, pin), ld_hint(p + 4, pin), f);
+    }
+  };
   int64_t i0 = start;
   if (vec) {
     constexpr int U = 4;  // 4 x 8 elements in flight per thread
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
       float g[U][8], m[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        load8<TG>(G + i + u * stride, g[u]);
-        u4_to_f4x2(ld_cs(M + i + u * stride), ld_cs(M + i + u * stride + 4), m[u]);
+        load8g(G + i + u * stride, g[u]);
+        u4_to_f4x2(ld_hint(M + i + u * stride, pin), ld_hint(M + i + u * stride + 4, pin), m[u]);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -58,21 +58,21 @@ __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
           m[u][e] = fmaf(beta, m[u][e], g[u][e]);
           acc = fmaf(m[u][e], m[u][e], acc);
         }
-        st_cs(M + i + u * stride, f4_to_u4(m[u]));
-        st_cs(M + i + u * stride + 4, f4_to_u4(m[u] + 4));
+        st_hint(M + i + u * stride, f4_to_u4(m[u]), pout);
+        st_hint(M + i + u * stride + 4, f4_to_u4(m[u] + 4), pout);
       }
     }
     for (; i + 8 <= end; i += stride) {
       float g[8], m[8];
-      load8<TG>(G + i, g);
-      u4_to_f4x2(ld_cs(M + i), ld_cs(M + i + 4), m);
+      load8g(G + i, g);
+      u4_to_f4x2(ld_hint(M + i, pin), ld_hint(M + i + 4, pin), m);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         m[e] = fmaf(beta, m[e], g[e]);
         acc = fmaf(m[e], m[e], acc);
       }
-      st_cs(M + i, f4_to_u4(m));
-      st_cs(M + i + 4, f4_to_u4(m + 4));
+      st_hint(M + i, f4_to_u4(m), pout);
+      st_hint(M + i + 4, f4_to_u4(m + 4), pout);
     }
     i0 = start + ((end - start) / 8) * 8;  // scalar tail below
   }

@@ -1,149 +1,34 @@
-// Skinny path: Newton-Schulz for small m = min(rows, cols) <= 64.
+// Skinny path, direct iteration: Newton-Schulz for m = min(rows, cols) <= 64,
+// one pass over the m x n iterate per step.  It serves 32 < m <= 64 and step
+// counts beyond the Gram-space kernel's range (k_skinny_gs.cu); the host
+// functions at the end choose between the two.
 //
 // «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: for
 // shapes such as [24, 10240] the per-parameter iteration is dominated by host
 // dispatch, small allocations and synchronisation; batching every member of a
-// shape into one launch removes that (Fig. 7).  On this GPU the batched work
-// is bound by memory traffic and by the latency of the k dependent steps, so
-// the path is built around two kernels:
-//
-//  1. the streaming momentum kernel (k_elementwise.cu) writes M' = beta M + G
-//     and fixed-chunk partial sums of squares (HBM bound, fully coalesced);
-//  2. k_skinny_ns below: one cluster of kCL CTAs per member.  CTA r owns
-//     columns [r W, (r+1) W) of the wide m x n iterate.  The iterate is kept in
-//     an L2-resident workspace in the exact register order of mma.sync
-//     fragments, so each pass is: load fragments -> Y <- Q Y (mma.sync, with
-//     movmatrix transposes for the B operand) -> accumulate the next Gram
-//     Y Y^T from the same registers -> store fragments.  No shared-memory
-//     round trip of the iterate, one pass over it per Newton-Schulz step.
-//     Operands of each pass stream through a per-thread cp.async ring.
-//     Per step the per-warp Gram partials are summed in a fixed warp order,
-//     then over the cluster's CTAs in rank order (distributed shared memory),
-//     and every CTA forms Q = a I + b A + c A A in fp32.
+// shape into one launch removes that (Fig. 7).  After the streaming momentum
+// kernel (k_elementwise.cu), k_skinny_ns runs one cluster of kCL CTAs per
+// member.  CTA r owns columns [r W, (r+1) W) of the wide m x n iterate.  The
+// iterate is kept in an L2-resident workspace in the exact register order of
+// mma.sync fragments, so each pass is: load fragments -> Y <- Q Y (mma.sync,
+// with movmatrix transposes for the B operand) -> accumulate the next Gram
+// Y Y^T from the same registers -> store fragments.  Operands of each pass
+// stream through a per-thread cp.async ring.  Per step the per-warp Gram
+// partials are summed in a fixed warp order, then over the cluster's CTAs in
+// rank order (distributed shared memory), and every CTA forms
+// Q = a I + b A + c A A in fp32.
 //
 // Writing aX + (bA + cAA)X as (aI + bA + cAA)X keeps one product per step
 // («关于分布式Muon的想法整合及讨论» §2, §6: Gram matrix, then matrix products;
 // A changes with X every round).  All reduction orders depend only on
 // (rows, cols), so a member gives the same bits in any batch.
-#include "common.cuh"
+#include "warp_mma.cuh"
 
 namespace muon {
 
 namespace {
 
 constexpr int kCL = 2;  // CTAs per member (cluster size), fixed for every shape
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ uint32_t movtrans(uint32_t a) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-  return d;
-}
-
-// Asynchronous global -> shared copies (per thread, no barrier needed when a
-// thread reads back only what it copied).  src_bytes = 0 zero-fills.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-template <typename TY> struct Mma;
-template <> struct Mma<__half> {
-  static __device__ __forceinline__ void run(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-  static __device__ __forceinline__ uint32_t pack(float x, float y) {
-    __half2 h = __floats2half2_rn(x, y);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  static __device__ __forceinline__ float2 unpack(uint32_t u) {
-    return __half22float2(*reinterpret_cast<__half2*>(&u));
-  }
-};
-template <> struct Mma<__nv_bfloat16> {
-  static __device__ __forceinline__ void run(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-  static __device__ __forceinline__ uint32_t pack(float x, float y) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  static __device__ __forceinline__ float2 unpack(uint32_t u) {
-    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
-  }
-};
-
-// Gram tiles (m16 x n8) touching the upper triangle, in a fixed order.
-template <int MT>
-struct GramTiles {
-  __host__ __device__ static constexpr int count() {
-    int c = 0;
-    for (int mi = 0; mi < MT; ++mi)
-      for (int nj = 0; nj < 2 * MT; ++nj)
-        if (nj * 8 + 7 >= mi * 16) ++c;
-    return c;
-  }
-  static constexpr int N = count();
-  __host__ __device__ static constexpr int code(int t) {  // mi * 16 + nj of the t-th tile
-    int c = 0;
-    for (int a = 0; a < MT; ++a)
-      for (int b = 0; b < 2 * MT; ++b)
-        if (b * 8 + 7 >= a * 16) {
-          if (c == t) return a * 16 + b;
-          ++c;
-        }
-    return 0;
-  }
-  __device__ __forceinline__ static void tile(int t, int& mi, int& nj) {
-    const int v = code(t);
-    mi = v >> 4;
-    nj = v & 15;
-  }
-};
 
 // Shared memory (bytes): the cp.async stage ring, per-warp Gram partials, the
 // CTA partial (double buffered, read by the peer), A (fp32), Q (operand type).
@@ -634,24 +519,30 @@ bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg) {
   cfg->cluster = kCL;
   cfg->threads = cfg->mtiles <= 2 ? 512 : 256;
   const int w = (n + kCL - 1) / kCL;
-  cfg->width = (w + 15) / 16 * 16;
+  cfg->width = (w + 31) / 32 * 32;  // whole 32-column superblocks (Gram-space output pass)
   int blk = 0;
   for (int q = 0; q < cfg->mtiles; ++q) blk += (m - 16 * q > 8) ? 512 : 256;
   cfg->blk = blk;
-  cfg->ws_bytes = (int64_t)kCL * (cfg->width / 16) * blk;  // per member
+  cfg->ws_bytes = (int64_t)kCL * (cfg->width / 16) * blk;  // per member (direct kernel)
   cfg->smem = 0;
+  cfg->gram_space = m <= 32;
   return true;
 }
 
 cudaError_t prepare_skinny(const KArgs& a, const SkinnyCfg& cfg) {
-  return dispatch(a, cfg, nullptr, true);
+  cudaError_t e = dispatch(a, cfg, nullptr, true);
+  if (e == cudaSuccess && cfg.gram_space) e = gs_dispatch(a, cfg, nullptr, true);
+  return e;
 }
 
-cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s) {
-  return dispatch(a, cfg, s, false);
+cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, int32_t ns_steps, cudaStream_t s) {
+  if (cfg.gram_space && ns_steps <= kGramSpaceMaxSteps) return gs_dispatch(a, cfg, s, false);
+  const cudaError_t e = launch_momentum_partial(a, s);
+  return e == cudaSuccess ? dispatch(a, cfg, s, false) : e;
 }
 
 int skinny_max_active_clusters(int ns_type, int m) {
+  if (m <= 32) return gs_max_active_clusters(ns_type, m);
   const int mt = (m + 15) / 16;
   const bool half = half_last_tile(m, mt);
   if (ns_type == NS_F16) return half ? clusters_mt<__half, true>(mt) : clusters_mt<__half, false>(mt);

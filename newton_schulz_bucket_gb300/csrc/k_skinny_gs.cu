@@ -1,0 +1,665 @@
+// Skinny path for m = min(rows, cols) <= 32: the whole Muon step of a member
+// in one kernel, with Newton-Schulz evaluated in Gram space.
+//
+// «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: for
+// shapes such as [24, 10240] the per-parameter iteration is dominated by host
+// dispatch, small allocations and synchronisation, and batching every member
+// of a shape into one launch removes that (Fig. 7).  On this GPU the batched
+// work is bound by bytes moved (HBM, and L2, whose read bandwidth is close to
+// HBM's), so the kernel streams the member's data twice however many steps
+// are taken:
+//
+//   1. momentum pass: M' = beta M + G is formed and stored, and from the same
+//      registers the sum of squares ||M'||_F^2 and the Gram matrix M' M'^T
+//      (tf32 tensor-core products, fp32 accumulation: the norm is not known
+//      yet, and tf32 keeps fp32's range with an 11-bit significand);
+//   2. in m x m space, fp32: A_0 = M' M'^T / (||M'||_F + eps)^2, then per step
+//      Q = a I + b A + c A^2, Pi <- Q Pi, A <- Q A Q;
+//   3. output pass: Y_0 = alpha M' / (||M'||_F + eps) in the operand type,
+//      O = Pi_k Y_0 / alpha with Pi_k split into an operand-type high part and
+//      a residual low part, and P' = P (1 - lr wd) - lr s O.
+//
+// Each quintic step is X' = Q X with Q = a I + b A + c A^2 and A = X X^T
+// («关于分布式Muon的想法整合及讨论» §1, §2, §6).  Q is a polynomial in A, so it
+// is symmetric and commutes with A, hence A' = X' X'^T = Q A Q and
+// X_k = Pi_k X_0 with Pi_k = Q_{k-1} ... Q_0: in exact arithmetic this is the
+// iteration itself; in floating point the data is rounded to the operand
+// type once instead of once per step.  All reduction orders depend only on
+// (rows, cols), so a member gives the same bits in any batch.
+//
+// Layout: one cluster of kCL CTAs per member; CTA r owns the wide iterate's
+// columns [r W, (r + 1) W).  The momentum pass walks 16-column blocks (block
+// blk by warp blk % NW): lane (g, t4) holds rows 16 mi + g (+ 8) and the four
+// consecutive columns 4 t4 .. 4 t4 + 3, which stand in the tf32 A-fragment
+// slots (t4, t4 + 4) of the block's two k8 steps.  The output pass walks
+// 32-column superblocks and loads Y_0 straight into B fragments (see
+// gs_out_pass).  The Gram sums over all columns and Pi X acts on each column
+// alone, so these fixed permutations of a block's columns change nothing, and
+// they turn every access into a 16-byte (fp32) or 8/16-byte (bf16) vector.
+// Operands stream through a per-lane cp.async ring.
+#include "warp_mma.cuh"
+
+namespace muon {
+
+namespace {
+
+constexpr int kCL = 2;  // CTAs per member (cluster size)
+
+template <int MT, int NT, bool HALF>
+struct GsLayout {
+  static constexpr int MP = 16 * MT;                    // padded m
+  static constexpr int LD = MP + 4;                     // fp32 m x m row pitch: 16-byte rows, no bank conflicts
+  static constexpr int NW = NT / 32;
+  static constexpr int R = 2 * MT - (HALF ? 1 : 0);     // rows g + 8 h a lane holds (momentum pass, output rows)
+  static constexpr int KR = 4 * MT - (HALF ? 2 : 0);    // rows 2 t4 + {0, 1, 8, 9} a lane holds (output pass)
+  static constexpr int NJ = HALF ? 2 * MT - 1 : 2 * MT; // 8-row groups of the Gram's columns
+  using GT = GramTiles<MT, NJ>;
+  // Both passes are bound by the bytes a CTA keeps in flight, so each ring
+  // takes as many rounds as shared memory holds next to the fixed part.
+  static constexpr int kFixed = MP * MP * 4 + 64 + MP * 4;
+  static constexpr int kCap = 227 * 1024 - kFixed;
+  // momentum pass ring: 16 B of M and 8 B of G per row and lane; rounds consumed two at a time
+  static constexpr int LB1 = 24 * R;
+  static constexpr int S1 = 6 * NW * 32 * LB1 <= kCap ? 6 : 4;
+  static constexpr int kRing1 = S1 * NW * 32 * LB1;
+  // output pass ring: 16 B of M' per k-row and 16 B of P per output row and lane; one round at a time
+  static constexpr int LBO = 16 * (KR + R);
+  static constexpr int SO = 4 * NW * 32 * LBO <= kCap ? 4 : (3 * NW * 32 * LBO <= kCap ? 3 : 2);
+  static constexpr int kRingO = SO * NW * 32 * LBO;
+  // between the passes the ring holds the per-warp Gram partials and sums of
+  // squares, then the m x m work arrays: A, Q, T, Pi (two), the
+  // upper-triangle index table and Pi's operand-type high / low parts
+  static constexpr int kWarpPart = NW * GT::N * 128 * 4 + NW * 4 * 4;
+  static constexpr int kMat = MP * LD * 4;
+  static constexpr int kTab = ((MP * (MP + 1) / 2) * 4 + 15) / 16 * 16;
+  static constexpr int kPiT = MP * (MP + 8) * 2;
+  static constexpr int kMM = 5 * kMat + kTab + 2 * kPiT;
+  static constexpr int kU0 = kRing1 > kRingO ? kRing1 : kRingO;
+  static constexpr int kU = kU0 > kWarpPart + kMM ? kU0 : kWarpPart + kMM;
+  static constexpr int kCta = kU;                       // this CTA's Gram partial (peer reads it)
+  static constexpr int kMisc = kCta + MP * MP * 4;      // [0] sum of squares (peer reads it), [1] norm
+  static constexpr int kTotal = kMisc + 64 + MP * 4;    // misc words, then Pi's row scales
+  static_assert(kTotal == kU + kFixed, "layout");
+  static_assert(kTotal <= 227 * 1024, "Gram-space kernel shared memory exceeds the per-CTA limit");
+};
+
+// Wide-iterate element (i, j) in the parameter's memory.
+struct Wide {
+  int cols, T;
+  __device__ __forceinline__ int64_t off(int i, int j) const {
+    return T ? (int64_t)j * cols + i : (int64_t)i * cols + j;
+  }
+};
+
+// Per-thread state of one member's two data passes.
+struct GsCtx {
+  int lane, warp, g, t4, m, n, c0, NB;  // NB: 16-column blocks of this CTA (even)
+  bool vec;            // rows <= cols, cols % 8 == 0, M', G and P 16-byte aligned
+  float* Mp;
+  const __nv_bfloat16* G;
+  __nv_bfloat16* P;
+  float* dbg;
+  int cols;
+  Wide wd;
+  float beta, inv, decay, coef, inv_alpha;
+};
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Momentum pass over this warp's 16-column blocks: M' = beta M + G stored,
+// ss += M'^2 per lane, and gacc += M' M'^T on the upper Gram tiles (tf32).
+// All three streams keep the default L2 policy: measured, evict-first reads
+// or evict-last stores here only slowed the pass.
+template <int MT, int NT, bool HALF>
+__device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
+                                                 float (&gacc)[GsLayout<MT, NT, HALF>::GT::N][4], float& ss) {
+  using L = GsLayout<MT, NT, HALF>;
+  using GT = typename L::GT;
+  constexpr int NW = L::NW, S = L::S1, LB = L::LB1, R = L::R;
+  constexpr uint32_t kSlot = NW * 32 * LB;
+  const int lane = c.lane;
+  uint8_t* ring_warp = ring + c.warp * 32 * LB;
+  const uint32_t ring0 = smem_u32(ring_warp);
+  const int rounds = (c.NB + NW - 1) / NW;
+  auto row_of = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
+  const uint64_t pol = l2_evict_normal();
+
+  auto issue = [&](int r, uint32_t dst) {
+    const int blk = r * NW + c.warp;
+    if (c.vec && r < rounds && blk < c.NB) {
+      const int j = c.c0 + blk * 16 + 4 * c.t4;  // n % 8 == 0: the lane's 4 columns share fate
+      const bool colok = j < c.n;
+#pragma unroll
+      for (int s = 0; s < R; ++s) {
+        const int i = row_of(s);
+        const bool ok = colok && i < c.m;
+        const int64_t o = (int64_t)i * c.cols + j;
+        cp_async16_hint(dst + s * 512 + lane * 16, ok ? (const void*)(c.Mp + o) : (const void*)c.Mp,
+                        ok ? 16 : 0, pol);
+        cp_async8_hint(dst + R * 512 + s * 256 + lane * 8, ok ? (const void*)(c.G + o) : (const void*)c.G,
+                       ok ? 8 : 0, pol);
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
+
+  auto process = [&](int r, const uint8_t* st) {
+    const int blk = r * NW + c.warp;
+    if (r >= rounds || blk >= c.NB) return;
+    const int j0 = c.c0 + blk * 16 + 4 * c.t4;
+    // tv[mi][step][h][e]: row 16 mi + g + 8 h, tf32 slot k = t4 + 4 e of k8 step `step`
+    // <- column j0 + 2 step + e
+    uint32_t tv[MT][2][2][2];
+#pragma unroll
+    for (int s = 0; s < R; ++s) {
+      const int i = row_of(s);
+      float v[4];
+      if (c.vec) {
+        const float4 mv = *reinterpret_cast<const float4*>(st + s * 512 + lane * 16);
+        const uint2 gr = *reinterpret_cast<const uint2*>(st + R * 512 + s * 256 + lane * 8);
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.y));
+        v[0] = fmaf(c.beta, mv.x, g01.x);
+        v[1] = fmaf(c.beta, mv.y, g01.y);
+        v[2] = fmaf(c.beta, mv.z, g23.x);
+        v[3] = fmaf(c.beta, mv.w, g23.y);
+        if (i < c.m && j0 < c.n)
+          st_hint(c.Mp + (int64_t)i * c.cols + j0,
+                  make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                             __float_as_uint(v[3])),
+                  pol);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[q] = 0.f;
+          if (i < c.m && j0 + q < c.n) {
+            const int64_t o = c.wd.off(i, j0 + q);
+            v[q] = fmaf(c.beta, c.Mp[o], __bfloat162float(c.G[o]));
+            c.Mp[o] = v[q];
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ss = fmaf(v[q], v[q], ss);
+      tv[s >> 1][0][s & 1][0] = to_tf32(v[0]);
+      tv[s >> 1][0][s & 1][1] = to_tf32(v[1]);
+      tv[s >> 1][1][s & 1][0] = to_tf32(v[2]);
+      tv[s >> 1][1][s & 1][1] = to_tf32(v[3]);
+    }
+    if (HALF) tv[MT - 1][0][1][0] = tv[MT - 1][0][1][1] = tv[MT - 1][1][1][0] = tv[MT - 1][1][1][1] = 0u;
+#pragma unroll
+    for (int q = 0; q < GT::N; ++q) {
+      const int mi = GT::code(q) >> 4, nj = GT::code(q) & 15;
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        mma_tf32(gacc[q], tv[mi][k][0][0], tv[mi][k][1][0], tv[mi][k][0][1], tv[mi][k][1][1],
+                 tv[nj >> 1][k][nj & 1][0], tv[nj >> 1][k][nj & 1][1]);
+    }
+  };
+
+  int slot = 0;
+  for (int r = 0; r < rounds; r += 2) {
+    cp_async_wait<S - 2>();
+    const int slot2 = slot + 1 == S ? 0 : slot + 1;
+    process(r, ring_warp + slot * kSlot);
+    process(r + 1, ring_warp + slot2 * kSlot);
+    // rounds r, r + 1 now live in registers: refill their slots
+    issue(r + S, ring0 + slot * kSlot);
+    issue(r + 1 + S, ring0 + slot2 * kSlot);
+    slot = slot2 + 1 == S ? 0 : slot2 + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// Output pass over this warp's 32-column superblocks: O = (Pi_hi + Pi_lo) Y_0
+// and P' = P (1 - lr wd) - lr s O.  Y_0 is loaded straight into B fragments:
+// lane (g, t4) holds rows 16 kk + 2 t4 + {0, 1, 8, 9} of columns
+// J + 4 g .. J + 4 g + 3, column J + 4 g + q standing at n = g of n-tile q.
+// Accumulator n of n-tile q is then column J + 4 n + q, so a lane's outputs
+// of a row are the eight consecutive columns J + 8 t4 .. J + 8 t4 + 7.
+template <typename TY, int MT, int NT, bool HALF>
+__device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
+                                            const uint32_t (&ph)[MT][MT][4], const uint32_t (&pl)[MT][MT][4],
+                                            const float (&rs)[GsLayout<MT, NT, HALF>::R]) {
+  using L = GsLayout<MT, NT, HALF>;
+  constexpr int NW = L::NW, S = L::SO, LB = L::LBO, R = L::R, KR = L::KR;
+  constexpr uint32_t kSlot = NW * 32 * LB;
+  const int lane = c.lane;
+  uint8_t* ring_warp = ring + c.warp * 32 * LB;
+  const uint32_t ring0 = smem_u32(ring_warp);
+  const int nsb = c.NB / 2;  // superblocks of this CTA
+  const int rounds = (nsb + NW - 1) / NW;
+  auto krow = [&](int kr) { return (kr >> 2) * 16 + 2 * c.t4 + (kr & 1) + ((kr & 2) ? 8 : 0); };
+  auto orow = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
+  const uint64_t last_use = l2_evict_first();
+
+  auto issue = [&](int r, uint32_t dst) {
+    const int sb = r * NW + c.warp;
+    if (c.vec && r < rounds && sb < nsb) {
+      const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
+#pragma unroll
+      for (int kr = 0; kr < KR; ++kr) {
+        const int i = krow(kr);
+        const bool ok = i < c.m && jm < c.n;
+        cp_async16_hint(dst + kr * 512 + lane * 16,
+                        ok ? (const void*)(c.Mp + (int64_t)i * c.cols + jm) : (const void*)c.Mp, ok ? 16 : 0,
+                        last_use);
+      }
+#pragma unroll
+      for (int s = 0; s < R; ++s) {
+        const int i = orow(s);
+        const bool ok = i < c.m && jp < c.n;  // n % 8 == 0: the lane's 8 columns share fate
+        cp_async16_hint(dst + (KR + s) * 512 + lane * 16,
+                        ok ? (const void*)(c.P + (int64_t)i * c.cols + jp) : (const void*)c.P, ok ? 16 : 0,
+                        last_use);
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
+
+  auto process = [&](int r, const uint8_t* st) {
+    const int sb = r * NW + c.warp;
+    if (r >= rounds || sb >= nsb) return;
+    const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
+    // B fragments: b[kk][q] = rows (2 t4, 2 t4 + 1) and (2 t4 + 8, 2 t4 + 9) of column jm + q
+    uint32_t b[MT][4][2];
+#pragma unroll
+    for (int kk = 0; kk < MT; ++kk) {
+      const bool half = HALF && kk == MT - 1;
+      float v[4][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (half && e >= 2) {
+          v[e][0] = v[e][1] = v[e][2] = v[e][3] = 0.f;
+          continue;
+        }
+        if (c.vec) {
+          const float4 t = *reinterpret_cast<const float4*>(st + (4 * kk + e) * 512 + lane * 16);
+          v[e][0] = t.x; v[e][1] = t.y; v[e][2] = t.z; v[e][3] = t.w;
+        } else {
+          const int i = krow(4 * kk + e);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[e][q] = (i < c.m && jm + q < c.n) ? c.Mp[c.wd.off(i, jm + q)] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        b[kk][q][0] = Mma<TY>::pack(v[0][q] * c.inv, v[1][q] * c.inv);
+        b[kk][q][1] = half ? 0u : Mma<TY>::pack(v[2][q] * c.inv, v[3][q] * c.inv);
+      }
+    }
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi) {
+      float d[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < MT; ++kk) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (HALF && kk == MT - 1) {  // rows 8..15 of this k-tile are padding
+            Mma<TY>::run8(d[q], ph[mi][kk], b[kk][q][0]);
+            Mma<TY>::run8(d[q], pl[mi][kk], b[kk][q][0]);
+          } else {
+            Mma<TY>::run(d[q], ph[mi][kk], b[kk][q][0], b[kk][q][1]);
+            Mma<TY>::run(d[q], pl[mi][kk], b[kk][q][0], b[kk][q][1]);
+          }
+        }
+      }
+      // rows 16 mi + g (h = 0) and 16 mi + g + 8 (h = 1), columns jp .. jp + 7
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (HALF && mi == MT - 1 && h == 1) continue;
+        const int s = 2 * mi + h;
+        const int i = orow(s);
+        if (i >= c.m || jp >= c.n) continue;
+        const float o[8] = {d[0][2 * h], d[1][2 * h], d[2][2 * h], d[3][2 * h],
+                            d[0][2 * h + 1], d[1][2 * h + 1], d[2][2 * h + 1], d[3][2 * h + 1]};
+        const float coef = c.coef * rs[s], oscale = c.inv_alpha * rs[s];  // row scale of Pi undone
+        if (c.vec) {
+          const uint4 praw = *reinterpret_cast<const uint4*>(st + (KR + s) * 512 + lane * 16);
+          float pf[8];
+          bf16x8_to_f32(praw, pf);
+          float w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = fmaf(-coef, o[e], pf[e] * c.decay);
+          const int64_t off = (int64_t)i * c.cols + jp;
+          *reinterpret_cast<uint4*>(c.P + off) = f32_to_bf16x8(w);
+          if (c.dbg) {
+            float* dp = c.dbg + off;
+            *reinterpret_cast<float4*>(dp) =
+                make_float4(o[0] * oscale, o[1] * oscale, o[2] * oscale, o[3] * oscale);
+            *reinterpret_cast<float4*>(dp + 4) =
+                make_float4(o[4] * oscale, o[5] * oscale, o[6] * oscale, o[7] * oscale);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (jp + e >= c.n) continue;
+            const int64_t off = c.wd.off(i, jp + e);
+            c.P[off] = __float2bfloat16_rn(fmaf(-coef, o[e], __bfloat162float(c.P[off]) * c.decay));
+            if (c.dbg) c.dbg[off] = o[e] * oscale;
+          }
+        }
+      }
+    }
+  };
+
+  for (int r = 0; r < rounds; ++r) {
+    cp_async_wait<S - 1>();
+    uint8_t* st = ring_warp + (r % S) * kSlot;
+    process(r, st);
+    // round r now lives in registers / is written: refill its slot
+    issue(r + S, ring0 + (r % S) * kSlot);
+  }
+  cp_async_wait<0>();
+}
+
+// (X Y)[i][j] for symmetric fp32 MP x MP matrices with zero padding beyond m
+// and row pitch LD (a multiple of 4): rows i of X and j of Y, k in order.
+template <int MP, int LD>
+__device__ __forceinline__ float dot_sym(const float* X, const float* Y, int i, int j) {
+  const float4* x = reinterpret_cast<const float4*>(X + i * LD);
+  const float4* y = reinterpret_cast<const float4*>(Y + j * LD);
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < MP / 4; ++k) {
+    const float4 u = x[k], v = y[k];
+    acc = fmaf(u.x, v.x, acc);
+    acc = fmaf(u.y, v.y, acc);
+    acc = fmaf(u.z, v.z, acc);
+    acc = fmaf(u.w, v.w, acc);
+  }
+  return acc;
+}
+
+template <typename TY, int MT, int NT, bool HALF>
+__global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
+  using L = GsLayout<MT, NT, HALF>;
+  using GT = typename L::GT;
+  constexpr int MP = L::MP, LD = L::LD, NW = L::NW;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* cpart = reinterpret_cast<float*>(smem + L::kCta);
+  float* misc = reinterpret_cast<float*>(smem + L::kMisc);
+  float* rsc = misc + 16;  // per-row power-of-two scale of Pi
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_rank();
+  const int b = blockIdx.x / kCL;
+  const int m = a.m;
+  const MemberPtrs mp = a.mem[b];
+
+  GsCtx c;
+  c.lane = lane; c.warp = warp; c.g = lane >> 2; c.t4 = lane & 3;
+  c.m = m; c.n = a.n; c.c0 = (int)rank * W; c.NB = NB;
+  c.Mp = mp.M;
+  c.G = static_cast<const __nv_bfloat16*>(mp.G);
+  c.P = static_cast<__nv_bfloat16*>(mp.P);
+  c.cols = a.cols;
+  c.wd = Wide{a.cols, a.T};
+  c.vec = !a.T && (a.cols % 8 == 0) && aligned16(c.Mp) && aligned16(c.G) && aligned16(c.P);
+  c.dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+  const int ns = a.sc->ns_steps;
+  c.beta = a.sc->beta;
+  const float lr = a.sc->lr;
+  c.decay = 1.f - lr * a.sc->wd;
+  c.inv_alpha = 1.f / a.alpha;
+  c.coef = lr * a.scale * c.inv_alpha;
+
+  // m x m work arrays (aliasing the ring between the two passes)
+  float* wpart = reinterpret_cast<float*>(smem);
+  float* wss = wpart + NW * GT::N * 128;
+  float* Am = reinterpret_cast<float*>(smem + L::kWarpPart);
+  float* Qm = Am + MP * LD;
+  float* Tm = Qm + MP * LD;
+  float* Pi0 = Tm + MP * LD;
+  float* Pi1 = Pi0 + MP * LD;
+  uint32_t* tab = reinterpret_cast<uint32_t*>(Pi1 + MP * LD);
+  TY* Ph = reinterpret_cast<TY*>(smem + L::kWarpPart + 5 * L::kMat + L::kTab);
+  TY* Pl = Ph + MP * (MP + 8);
+  float* Pi = Pi0;
+  const int nup = m * (m + 1) / 2;
+
+  // 1. momentum, sum of squares and Gram matrix
+  float gacc[GT::N][4];
+#pragma unroll
+  for (int q = 0; q < GT::N; ++q) gacc[q][0] = gacc[q][1] = gacc[q][2] = gacc[q][3] = 0.f;
+  float ss = 0.f;
+  gs_momentum_pass<MT, NT, HALF>(c, smem, gacc, ss);
+  // Hint: move this CTA's slice of P into L2 while the m x m work runs.
+  if (c.vec && warp == NW - 1 && c.c0 < c.n) {
+    const int ncol = min(W, c.n - c.c0);
+    const uint32_t bytes = (uint32_t)(ncol * 2) & ~15u;
+    if (bytes)
+      for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * a.cols + c.c0, bytes);
+  }
+  __syncthreads();  // every warp's ring is drained before it is reused
+  for (int e = tid; e < 5 * MP * LD; e += NT) Am[e] = 0.f;  // m x m arrays, padding included
+  // per-warp partials, then warps summed in a fixed order into this CTA's partial
+  ss = warp_sum(ss);
+  if (lane == 0) wss[warp] = ss;
+#pragma unroll
+  for (int q = 0; q < GT::N; ++q) {
+    float* dst = wpart + (warp * GT::N + q) * 128;
+    dst[c.g * 8 + 2 * c.t4] = gacc[q][0];
+    dst[c.g * 8 + 2 * c.t4 + 1] = gacc[q][1];
+    dst[(c.g + 8) * 8 + 2 * c.t4] = gacc[q][2];
+    dst[(c.g + 8) * 8 + 2 * c.t4 + 1] = gacc[q][3];
+  }
+  __syncthreads();
+  for (int e = tid; e < GT::N * 128; e += NT) {
+    const int q = e >> 7, w = e & 127;
+    float acc = 0.f;
+    for (int k = 0; k < NW; ++k) acc += wpart[(k * GT::N + q) * 128 + w];
+    const int code = GT::code(q);
+    cpart[((code >> 4) * 16 + (w >> 3)) * MP + (code & 15) * 8 + (w & 7)] = acc;
+  }
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int k = 0; k < NW; ++k) acc += wss[k];
+    misc[0] = acc;
+  }
+  cluster_sync();
+  // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: CTAs summed in rank order
+  float ssum = 0.f;
+#pragma unroll
+  for (int r = 0; r < kCL; ++r) ssum += ld_dsmem_f32(&misc[0], (uint32_t)r);
+  const float inv_raw = 1.f / (sqrtf(ssum) + a.eps);
+  c.inv = a.alpha * inv_raw;
+  const float inv2 = inv_raw * inv_raw;
+  for (int e = tid; e < nup; e += NT) {
+    // e -> (i, j), i <= j, row-major over the upper triangle
+    int i = 0, rem = e;
+    while (rem >= m - i) { rem -= m - i; ++i; }
+    const int j = i + rem;
+    tab[e] = (uint32_t)(i << 16 | j);
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
+    acc *= inv2;
+    Am[i * LD + j] = acc;
+    Am[j * LD + i] = acc;
+  }
+  cluster_arrive();  // done reading the peer's partials
+  __syncthreads();
+
+  // 2. the k steps in m x m space
+  if (ns > 0) {
+    const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
+    for (int s = 0; s < ns; ++s) {
+      // Q = a I + b A + c A^2
+      for (int e = tid; e < nup; e += NT) {
+        const int i = tab[e] >> 16, j = tab[e] & 0xffff;
+        float q = fmaf(cc, dot_sym<MP, LD>(Am, Am, i, j), cb * Am[i * LD + j]);
+        if (i == j) q += ca;
+        Qm[i * LD + j] = q;
+        Qm[j * LD + i] = q;
+      }
+      __syncthreads();
+      // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
+      float* Pn = Pi == Pi0 ? Pi1 : Pi0;
+      const bool more = s + 1 < ns;
+      for (int e = tid; e < nup; e += NT) {
+        const int i = tab[e] >> 16, j = tab[e] & 0xffff;
+        const float pv = s == 0 ? Qm[i * LD + j] : dot_sym<MP, LD>(Qm, Pi, i, j);
+        Pn[i * LD + j] = pv;
+        Pn[j * LD + i] = pv;
+        if (more) {
+          const float t = dot_sym<MP, LD>(Qm, Qm, i, j);
+          Tm[i * LD + j] = t;
+          Tm[j * LD + i] = t;
+        }
+      }
+      Pi = Pn;
+      __syncthreads();
+      if (more) {
+        // A <- Q^2 A (written over Q, then the two swap roles)
+        for (int e = tid; e < nup; e += NT) {
+          const int i = tab[e] >> 16, j = tab[e] & 0xffff;
+          const float v = dot_sym<MP, LD>(Tm, Am, i, j);
+          Qm[i * LD + j] = v;
+          Qm[j * LD + i] = v;
+        }
+        float* t = Am; Am = Qm; Qm = t;
+        __syncthreads();
+      }
+    }
+    // Along an exact null direction of X_0 (a zero row, say) Pi grows like
+    // a^k while O does not: scale each row i of Pi by 2^-e_i into the operand
+    // type's range, and O's row i by 2^e_i in the epilogue.
+    for (int i = tid; i < MP; i += NT) {
+      float mx = 0.f;
+      for (int k = 0; k < m && i < m; ++k) mx = fmaxf(mx, fabsf(Pi[i * LD + k]));
+      const int ex = mx >= 32768.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
+      rsc[i] = exp2f((float)ex);
+    }
+    __syncthreads();
+    // Pi in the operand type: high part and residual, zero outside m x m
+    for (int e = tid; e < MP * MP; e += NT) {
+      const int i = e / MP, j = e - (e / MP) * MP;
+      float v = 0.f;
+      if (i < m && j < m) v = Pi[i * LD + j] / rsc[i];
+      const TY hi = from_f32<TY>(v);
+      Ph[i * (MP + 8) + j] = hi;
+      Pl[i * (MP + 8) + j] = from_f32<TY>(v - to_f32(hi));
+    }
+  } else {
+    // no step: O = X_0 (Pi = I, exact in the operand type)
+    for (int i = tid; i < MP; i += NT) rsc[i] = 1.f;
+    for (int e = tid; e < MP * MP; e += NT) {
+      const int i = e / MP, j = e - (e / MP) * MP;
+      Ph[i * (MP + 8) + j] = from_f32<TY>(i == j && i < m ? 1.f : 0.f);
+      Pl[i * (MP + 8) + j] = from_f32<TY>(0.f);
+    }
+  }
+  __syncthreads();
+  uint32_t ph[MT][MT][4], pl[MT][MT][4];
+  {
+    const uint32_t hb = smem_u32(Ph), lb = smem_u32(Pl);
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+      for (int kk = 0; kk < MT; ++kk) {
+        const uint32_t o = 2u * ((mi * 16 + (lane & 15)) * (MP + 8) + kk * 16 + (lane >> 4) * 8);
+        ldsm_x4(hb + o, ph[mi][kk]);
+        ldsm_x4(lb + o, pl[mi][kk]);
+      }
+  }
+  float rs[L::R];
+#pragma unroll
+  for (int s = 0; s < L::R; ++s) rs[s] = rsc[(s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0)];
+  __syncthreads();  // the ring's bytes are reused by the output pass
+
+  // 3. O = Pi_k Y_0 and the parameter write
+  gs_out_pass<TY, MT, NT, HALF>(c, smem, ph, pl, rs);
+  cluster_wait();  // the peer may still read this CTA's partials
+}
+
+template <typename TY, int MT, bool HALF>
+cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
+  constexpr int NT = 512;
+  auto fn = k_skinny_gs<TY, MT, NT, HALF>;
+  constexpr int smem = GsLayout<MT, NT, HALF>::kTotal;
+  if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(a.B * kCL);
+  lc.blockDim = dim3(NT);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, fn, a, (int)cfg.width, (int)(cfg.width / 16));
+}
+
+template <typename TY, int MT, bool HALF>
+int gs_clusters_of() {
+  constexpr int NT = 512;
+  auto fn = k_skinny_gs<TY, MT, NT, HALF>;
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(kCL * 1024);
+  lc.blockDim = dim3(NT);
+  lc.dynamicSmemBytes = GsLayout<MT, NT, HALF>::kTotal;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, fn, &lc) == cudaSuccess ? n : -1;
+}
+
+template <typename TY>
+cudaError_t gs_launch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
+  const bool half = a.m - 16 * (cfg.mtiles - 1) <= 8;
+  if (cfg.mtiles == 1)
+    return half ? launch_gs_t<TY, 1, true>(a, cfg, st, prep) : launch_gs_t<TY, 1, false>(a, cfg, st, prep);
+  return half ? launch_gs_t<TY, 2, true>(a, cfg, st, prep) : launch_gs_t<TY, 2, false>(a, cfg, st, prep);
+}
+
+template <typename TY>
+int gs_clusters_ty(int m) {
+  const int mt = (m + 15) / 16;
+  const bool half = m - 16 * (mt - 1) <= 8;
+  if (mt == 1) return half ? gs_clusters_of<TY, 1, true>() : gs_clusters_of<TY, 1, false>();
+  return half ? gs_clusters_of<TY, 2, true>() : gs_clusters_of<TY, 2, false>();
+}
+
+}  // namespace
+
+cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare) {
+  if (a.mode_f32 || cfg.mtiles > 2) return cudaErrorInvalidValue;
+  return a.ns_type == NS_F16 ? gs_launch_ty<__half>(a, cfg, s, prepare)
+                             : gs_launch_ty<__nv_bfloat16>(a, cfg, s, prepare);
+}
+
+int gs_max_active_clusters(int ns_type, int m) {
+  if (m < 1 || m > 32) return -1;
+  return ns_type == NS_F16 ? gs_clusters_ty<__half>(m) : gs_clusters_ty<__nv_bfloat16>(m);
+}
+
+}  // namespace muon

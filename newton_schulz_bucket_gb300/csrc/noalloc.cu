@@ -121,6 +121,7 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
                 ? (float)std::sqrt(std::max(1.0, (double)rows / (double)cols))
                 : (scale_mode == MUON_SCALE_RMS_0_2 ? (float)(0.2 * std::sqrt((double)n)) : 1.f);
   k.alpha = (float)std::ldexp(1.0, (int)std::round(0.5 * std::log2((double)n)));
+  k.l2_keep_m = 1;
   {
     // once per device, with that device current: the array's device address
     // and the kernel attributes (host work only; do it before stream capture)
@@ -147,8 +148,7 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
   const StepScalars hs{beta, lr, wd, a, b, c, ns_steps, 0};
   k_static_setup<<<1, 32, 0, s>>>(hs, params, grads, momenta, batch, rows * cols, sc, mem);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_momentum_partial(k, s);
-  if (e == cudaSuccess) e = launch_skinny(k, cfg, s);
+  if (e == cudaSuccess) e = launch_skinny(k, cfg, ns_steps, s);
   if (e != cudaSuccess) return static_fail(MUON_ERR_CUDA, cudaGetErrorString(e));
   return MUON_OK;
 }

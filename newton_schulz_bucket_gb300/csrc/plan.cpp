@@ -293,6 +293,7 @@ KArgs make_args(const muon_plan_s* p, const GroupPlan& g) {
   a.dbg = (p->d.opt.flags & MUON_FLAG_KEEP_UPDATE) ? reinterpret_cast<float*>(base + g.off_dbg)
                                                    : nullptr;
   a.err = reinterpret_cast<int*>(p->ws + p->d.off_err);
+  a.l2_keep_m = g.path == PATH_SKINNY;
   return a;
 }
 
@@ -301,8 +302,8 @@ cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int3
                                   cudaStream_t s) {
   const KArgs a = make_args(p, g);
   cudaError_t e;
+  if (g.path == PATH_SKINNY) return launch_skinny(a, g.sk, k, s);
   if ((e = launch_momentum_partial(a, s))) return e;
-  if (g.path == PATH_SKINNY) return launch_skinny(a, g.sk, s);
   if ((e = launch_norm_finalize(a, s))) return e;
   if ((e = launch_normalize_cast(a, a.y0, s))) return e;
   if (g.path == PATH_TENSOR) {

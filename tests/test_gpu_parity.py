@@ -38,6 +38,10 @@ SKINNY_SHAPES = [
     [[48, 2048], [40, 96]],
     [[5, 16], [16, 16]],
     [[2, 33, 70]],               # 3-D, odd
+    [[32, 4096]],                # m = 32: two full m16 tiles
+    [[8, 4096], [16, 4096]],     # one m16 tile (half / full)
+    [[25, 1000]],                # m = 25, ragged 32-column superblock
+    [[24, 1004]],                # cols % 8 != 0: scalar access path
 ]
 
 
@@ -94,6 +98,31 @@ def test_zero_gradient_and_momentum():
     want = want.to(torch.bfloat16).double().numpy()
     assert np.array_equal(run.p1(0), want) or np.max(np.abs(run.p1(0) - want)) <= \
         np.max(np.abs(want)) * 2 ** -8
+    run.close()
+
+
+@pytest.mark.parametrize("k", [10, 64])
+def test_gram_space_zero_rows(k):
+    """Zero rows of M' are exact null directions of X_0, along which the
+    Gram-space product Pi_k = Q_{k-1} ... Q_0 grows like a^k: O keeps them
+    exactly zero and the other rows match the oracle."""
+    w = W.custom([[24, 4096]], seed=21, ns_steps=k)
+    P, G, M = W.make_tensors(w, "cuda")
+    for r in (3, 20):
+        G[0][r] = 0
+        M[0][r] = 0
+    run = GpuRun(w, tensors=(P, G, M))
+    check_all(run)
+    O = run.O(0)
+    assert np.all(np.isfinite(O)) and np.all(O[[3, 20]] == 0)
+    run.close()
+
+
+def test_many_steps_direct_iteration():
+    """Step counts beyond the Gram-space range run the direct iteration."""
+    w = W.custom([[24, 2048], [2, 16, 512]], seed=22, ns_steps=70)
+    run = GpuRun(w)
+    check_all(run)
     run.close()
 
 
