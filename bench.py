@@ -11,9 +11,11 @@ momentum), 5 quintic Newton-Schulz steps -- the fused batch the pages profile
 P, P' traffic for workloads of memory-bound skinny groups; TFLOP/s of
 4 m^2 n + 2 m^3 per matrix per NS step otherwise) with inputs resident in HBM.
 Timing: CUDA events on the launching stream, W untimed warm-up steps, K timed
-steps, barrier + synchronize on both sides, max over ranks.  The inputs rotate
-over several seeded copies whose total exceeds the 129 MB L2, so no step
-starts with its inputs in L2.  `e2e` times the same step through
+steps, barrier + synchronize on both sides, max over ranks.  As in a training
+loop, every step updates the same buffers; before each step an untimed write
+of twice the L2 size flushes it (as the forward and backward passes would),
+and each step is timed alone by its own event pair (an untimed read of as
+much again drains the flush's write-backs before the step starts).  `e2e` times the same step through
 muon_step_host (host buffers in pinned memory, host->device and device->host
 copies inside the timed region).  `--impl reference` times the CPU oracle on
 the host cores instead.
@@ -318,40 +320,52 @@ def main():
     dev = torch.device("cuda", local)
     byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
     in_bytes = sum(math.prod(s) for s in w.shapes) * (8 if w.mode == "bf16" else 12)
-    n_sets = max(1, min(4, math.ceil(2 * L2_BYTES / in_bytes) + 1))
-    sets = [W.make_tensors(W.Workload(**{**w.__dict__, "seed": w.seed + 100 * j}), dev)
-            for j in range(n_sets)]
+    tensors = W.make_tensors(w, dev)
     plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, group_timing=True)
     groups = plan.groups()
     stream = torch.cuda.Stream(dev)
     coeffs = w.coeffs
-    # pointer arrays marshalled once per input set, as a C caller would hold them
-    bound = [plan.bind(*st) for st in sets]
+    # pointer arrays marshalled once, as a C caller would hold them
+    bound = plan.bind(*tensors)
     sp = stream.cuda_stream
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    drain_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
-    def step(j):
-        plan.step_bound(bound[j % n_sets], w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=sp)
+    def flush(j):
+        # untimed: write twice the L2 size (evicts the previous step's lines),
+        # then read as much again so the write-backs of that flush happen here
+        # and not inside the next timed step
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(float(j))
+            torch.sum(drain_buf, dim=0, out=sink)
+
+    def step():
+        plan.step_bound(bound, w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=sp)
 
     for j in range(args.warmup):
-        step(j)
+        flush(j)
+        step()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     gtimes = [[] for _ in groups]
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
-        ev0.record(stream)
         for j in range(args.steps):
-            step(j)
-        ev1.record(stream)
+            flush(j)
+            evs[j][0].record(stream)
+            step()
+            evs[j][1].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
-        ms_total = ev0.elapsed_time(ev1)
+        ms_total = sum(e0.elapsed_time(e1) for e0, e1 in evs)
         # per-group kernel times from events recorded inside the step graph
-        for j in range(min(args.steps, 2 * n_sets)):
-            step(j)
+        for j in range(min(args.steps, 6)):
+            flush(j)
+            step()
             for g in range(len(groups)):
                 gtimes[g].append(plan.group_elapsed_ms(g))
     torch.cuda.synchronize()
@@ -422,8 +436,9 @@ def main():
                 "config": {"workload": w.name, "shapes": describe_shapes(w.shapes),
                            "ns_steps": w.ns_steps, "coeffs": list(w.coeffs),
                            "ns_operands": "fp16 (fp32 accumulate)",
-                           "l2": f"inputs rotate over {n_sets} seeded copies "
-                                 f"({n_sets * in_bytes / 1e6:.0f} MB > L2)",
+                           "l2": f"same buffers every step ({in_bytes / 1e6:.0f} MB of P, G, M); "
+                                 f"L2 flushed before each step by an untimed {2 * L2_BYTES / 1e6:.0f} MB "
+                                 "write, then drained by an untimed read of as much; each step timed alone",
                            "parallelism": f"replicas x{world}"},
                 "matrices_per_s": sum(g["batch"] for g in groups) * world / sec,
                 "tflops": flops * world / sec / 1e12, "gbs": byts * world / sec / 1e9,

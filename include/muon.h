@@ -169,7 +169,9 @@ MUON_API muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_pa
  * (a, b, c): quintic coefficients.  Never allocates.  The first call with a
  * given ns_steps captures and instantiates a CUDA graph (host work only);
  * later calls copy the scalars and pointers into the plan's device table
- * (one async H2D copy from pinned memory) and replay the graph on `stream`.
+ * (one async H2D copy from pinned memory, skipped when they equal those of
+ * the previous call) and replay the graph on `stream`.  Successive calls on
+ * different streams must be ordered by the caller (the table is shared).
  * Errors (nothing is launched): INVALID_ARG for a null plan/array/pointer,
  * ns_steps < 0 or > 1000, or non-finite scalars; CUDA on a launch failure. */
 MUON_API muon_status_t muon_step(muon_plan_t plan, void* const* params,

@@ -55,30 +55,34 @@ struct GsLayout {
   static constexpr int NJ = HALF ? 2 * MT - 1 : 2 * MT; // 8-row groups of the Gram's columns
   using GT = GramTiles<MT, NJ>;
   // Both passes are bound by the bytes a CTA keeps in flight, so each ring
-  // takes as many rounds as shared memory holds next to the fixed part.
-  static constexpr int kFixed = MP * MP * 4 + 64 + MP * 4;
+  // takes as many rounds as shared memory holds next to the fixed part
+  // (this CTA's Gram partial, misc words, Pi's row scales, the upper-triangle
+  // index table).
+  static constexpr int kTab = ((MP * (MP + 1) / 2) * 4 + 15) / 16 * 16;
+  static constexpr int kFixed = MP * MP * 4 + 64 + MP * 4 + kTab;
   static constexpr int kCap = 227 * 1024 - kFixed;
-  // momentum pass ring: 16 B of M and 8 B of G per row and lane; rounds consumed two at a time
-  static constexpr int LB1 = 24 * R;
-  static constexpr int S1 = 6 * NW * 32 * LB1 <= kCap ? 6 : 4;
+  // momentum pass ring: 32 B of M and 16 B of G per row and lane; one round at a time
+  static constexpr int LB1 = 48 * R;
+  static constexpr int S1 = 4 * NW * 32 * LB1 <= kCap ? 4 : (3 * NW * 32 * LB1 <= kCap ? 3 : 2);
   static constexpr int kRing1 = S1 * NW * 32 * LB1;
   // output pass ring: 16 B of M' per k-row and 16 B of P per output row and lane; one round at a time
   static constexpr int LBO = 16 * (KR + R);
   static constexpr int SO = 4 * NW * 32 * LBO <= kCap ? 4 : (3 * NW * 32 * LBO <= kCap ? 3 : 2);
   static constexpr int kRingO = SO * NW * 32 * LBO;
   // between the passes the ring holds the per-warp Gram partials and sums of
-  // squares, then the m x m work arrays: A, Q, T, Pi (two), the
-  // upper-triangle index table and Pi's operand-type high / low parts
+  // squares, then the m x m work arrays: A, Q, T, Pi (two) and Pi's
+  // operand-type high / low parts
   static constexpr int kWarpPart = NW * GT::N * 128 * 4 + NW * 4 * 4;
   static constexpr int kMat = MP * LD * 4;
-  static constexpr int kTab = ((MP * (MP + 1) / 2) * 4 + 15) / 16 * 16;
   static constexpr int kPiT = MP * (MP + 8) * 2;
-  static constexpr int kMM = 5 * kMat + kTab + 2 * kPiT;
+  static constexpr int kMM = 5 * kMat + 2 * kPiT;
   static constexpr int kU0 = kRing1 > kRingO ? kRing1 : kRingO;
   static constexpr int kU = kU0 > kWarpPart + kMM ? kU0 : kWarpPart + kMM;
   static constexpr int kCta = kU;                       // this CTA's Gram partial (peer reads it)
-  static constexpr int kMisc = kCta + MP * MP * 4;      // [0] sum of squares (peer reads it), [1] norm
-  static constexpr int kTotal = kMisc + 64 + MP * 4;    // misc words, then Pi's row scales
+  static constexpr int kMisc = kCta + MP * MP * 4;      // [0] sum of squares (peer reads it)
+  static constexpr int kRsc = kMisc + 64;               // Pi's row scales
+  static constexpr int kTabOff = kRsc + MP * 4;         // (i << 16 | j) of the upper triangle, row-major
+  static constexpr int kTotal = kTabOff + kTab;
   static_assert(kTotal == kU + kFixed, "layout");
   static_assert(kTotal <= 227 * 1024, "Gram-space kernel shared memory exceeds the per-CTA limit");
 };
@@ -118,10 +122,13 @@ __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Momentum pass over this warp's 16-column blocks: M' = beta M + G stored,
-// ss += M'^2 per lane, and gacc += M' M'^T on the upper Gram tiles (tf32).
-// All three streams keep the default L2 policy: measured, evict-first reads
-// or evict-last stores here only slowed the pass.
+// Momentum pass over this warp's 32-column superblocks: M' = beta M + G
+// stored, ss += M'^2 per lane, and gacc += M' M'^T on the upper Gram tiles
+// (tf32).  Lane (g, t4) holds rows 16 mi + g (+ 8) and columns
+// J + 8 t4 .. J + 8 t4 + 7; column J + 8 t4 + 2 st + e stands in the tf32
+// A-fragment slot k = t4 + 4 e of k8 step st.  All three streams keep the
+// default L2 policy: measured, evict-first reads or evict-last stores here
+// only slowed the pass.
 template <int MT, int NT, bool HALF>
 __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
                                                  float (&gacc)[GsLayout<MT, NT, HALF>::GT::N][4], float& ss) {
@@ -132,24 +139,30 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   const int lane = c.lane;
   uint8_t* ring_warp = ring + c.warp * 32 * LB;
   const uint32_t ring0 = smem_u32(ring_warp);
-  const int rounds = (c.NB + NW - 1) / NW;
+  const int nsb = c.NB / 2;  // superblocks of this CTA
+  const int rounds = (nsb + NW - 1) / NW;
   auto row_of = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
   const uint64_t pol = l2_evict_normal();
+  const float2 beta2 = make_float2(c.beta, c.beta);
+  float2 ss2 = make_float2(0.f, 0.f);
 
+  // ring planes (512 B each, lane-contiguous 16 B): M row s low / high half at
+  // 2 s / 2 s + 1, G row s at 2 R + s
   auto issue = [&](int r, uint32_t dst) {
-    const int blk = r * NW + c.warp;
-    if (c.vec && r < rounds && blk < c.NB) {
-      const int j = c.c0 + blk * 16 + 4 * c.t4;  // n % 8 == 0: the lane's 4 columns share fate
+    const int sb = r * NW + c.warp;
+    if (c.vec && r < rounds && sb < nsb) {
+      const int j = c.c0 + sb * 32 + 8 * c.t4;  // n % 8 == 0: the lane's 8 columns share fate
       const bool colok = j < c.n;
 #pragma unroll
       for (int s = 0; s < R; ++s) {
         const int i = row_of(s);
         const bool ok = colok && i < c.m;
         const int64_t o = (int64_t)i * c.cols + j;
-        cp_async16_hint(dst + s * 512 + lane * 16, ok ? (const void*)(c.Mp + o) : (const void*)c.Mp,
+        const float* mp = ok ? c.Mp + o : c.Mp;
+        cp_async16_hint(dst + (2 * s) * 512 + lane * 16, mp, ok ? 16 : 0, pol);
+        cp_async16_hint(dst + (2 * s + 1) * 512 + lane * 16, ok ? mp + 4 : c.Mp, ok ? 16 : 0, pol);
+        cp_async16_hint(dst + (2 * R + s) * 512 + lane * 16, ok ? (const void*)(c.G + o) : (const void*)c.G,
                         ok ? 16 : 0, pol);
-        cp_async8_hint(dst + R * 512 + s * 256 + lane * 8, ok ? (const void*)(c.G + o) : (const void*)c.G,
-                       ok ? 8 : 0, pol);
       }
     }
     cp_async_commit();
@@ -159,33 +172,36 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
 
   auto process = [&](int r, const uint8_t* st) {
-    const int blk = r * NW + c.warp;
-    if (r >= rounds || blk >= c.NB) return;
-    const int j0 = c.c0 + blk * 16 + 4 * c.t4;
-    // tv[mi][step][h][e]: row 16 mi + g + 8 h, tf32 slot k = t4 + 4 e of k8 step `step`
-    // <- column j0 + 2 step + e
-    uint32_t tv[MT][2][2][2];
+    const int sb = r * NW + c.warp;
+    if (r >= rounds || sb >= nsb) return;
+    const int j0 = c.c0 + sb * 32 + 8 * c.t4;
+    // tv[mi][st][h][e]: row 16 mi + g + 8 h, tf32 slot k = t4 + 4 e of k8 step st
+    uint32_t tv[MT][4][2][2];
 #pragma unroll
     for (int s = 0; s < R; ++s) {
       const int i = row_of(s);
-      float v[4];
+      float v[8];
       if (c.vec) {
-        const float4 mv = *reinterpret_cast<const float4*>(st + s * 512 + lane * 16);
-        const uint2 gr = *reinterpret_cast<const uint2*>(st + R * 512 + s * 256 + lane * 8);
-        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.x));
-        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.y));
-        v[0] = fmaf(c.beta, mv.x, g01.x);
-        v[1] = fmaf(c.beta, mv.y, g01.y);
-        v[2] = fmaf(c.beta, mv.z, g23.x);
-        v[3] = fmaf(c.beta, mv.w, g23.y);
-        if (i < c.m && j0 < c.n)
-          st_hint(c.Mp + (int64_t)i * c.cols + j0,
-                  make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                             __float_as_uint(v[3])),
-                  pol);
+        const float4 m0 = *reinterpret_cast<const float4*>(st + (2 * s) * 512 + lane * 16);
+        const float4 m1 = *reinterpret_cast<const float4*>(st + (2 * s + 1) * 512 + lane * 16);
+        float gf[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + (2 * R + s) * 512 + lane * 16), gf);
+        const float2 r0 = __ffma2_rn(beta2, make_float2(m0.x, m0.y), make_float2(gf[0], gf[1]));
+        const float2 r1 = __ffma2_rn(beta2, make_float2(m0.z, m0.w), make_float2(gf[2], gf[3]));
+        const float2 r2 = __ffma2_rn(beta2, make_float2(m1.x, m1.y), make_float2(gf[4], gf[5]));
+        const float2 r3 = __ffma2_rn(beta2, make_float2(m1.z, m1.w), make_float2(gf[6], gf[7]));
+        v[0] = r0.x; v[1] = r0.y; v[2] = r1.x; v[3] = r1.y;
+        v[4] = r2.x; v[5] = r2.y; v[6] = r3.x; v[7] = r3.y;
+        if (i < c.m && j0 < c.n) {
+          float* dp = c.Mp + (int64_t)i * c.cols + j0;
+          st_hint(dp, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                 __float_as_uint(v[3])), pol);
+          st_hint(dp + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]),
+                                     __float_as_uint(v[7])), pol);
+        }
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
           v[q] = 0.f;
           if (i < c.m && j0 + q < c.n) {
             const int64_t o = c.wd.off(i, j0 + q);
@@ -195,35 +211,36 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) ss = fmaf(v[q], v[q], ss);
-      tv[s >> 1][0][s & 1][0] = to_tf32(v[0]);
-      tv[s >> 1][0][s & 1][1] = to_tf32(v[1]);
-      tv[s >> 1][1][s & 1][0] = to_tf32(v[2]);
-      tv[s >> 1][1][s & 1][1] = to_tf32(v[3]);
+      for (int q = 0; q < 4; ++q) ss2 = __ffma2_rn(make_float2(v[2 * q], v[2 * q + 1]),
+                                                  make_float2(v[2 * q], v[2 * q + 1]), ss2);
+#pragma unroll
+      for (int st4 = 0; st4 < 4; ++st4) {
+        tv[s >> 1][st4][s & 1][0] = to_tf32(v[2 * st4]);
+        tv[s >> 1][st4][s & 1][1] = to_tf32(v[2 * st4 + 1]);
+      }
     }
-    if (HALF) tv[MT - 1][0][1][0] = tv[MT - 1][0][1][1] = tv[MT - 1][1][1][0] = tv[MT - 1][1][1][1] = 0u;
+    if (HALF) {
+#pragma unroll
+      for (int st4 = 0; st4 < 4; ++st4) tv[MT - 1][st4][1][0] = tv[MT - 1][st4][1][1] = 0u;
+    }
 #pragma unroll
     for (int q = 0; q < GT::N; ++q) {
       const int mi = GT::code(q) >> 4, nj = GT::code(q) & 15;
 #pragma unroll
-      for (int k = 0; k < 2; ++k)
+      for (int k = 0; k < 4; ++k)
         mma_tf32(gacc[q], tv[mi][k][0][0], tv[mi][k][1][0], tv[mi][k][0][1], tv[mi][k][1][1],
                  tv[nj >> 1][k][nj & 1][0], tv[nj >> 1][k][nj & 1][1]);
     }
   };
 
-  int slot = 0;
-  for (int r = 0; r < rounds; r += 2) {
-    cp_async_wait<S - 2>();
-    const int slot2 = slot + 1 == S ? 0 : slot + 1;
-    process(r, ring_warp + slot * kSlot);
-    process(r + 1, ring_warp + slot2 * kSlot);
-    // rounds r, r + 1 now live in registers: refill their slots
-    issue(r + S, ring0 + slot * kSlot);
-    issue(r + 1 + S, ring0 + slot2 * kSlot);
-    slot = slot2 + 1 == S ? 0 : slot2 + 1;
+  for (int r = 0; r < rounds; ++r) {
+    cp_async_wait<S - 1>();
+    process(r, ring_warp + (r % S) * kSlot);
+    // round r now lives in registers: refill its slot
+    issue(r + S, ring0 + (r % S) * kSlot);
   }
   cp_async_wait<0>();
+  ss += ss2.x + ss2.y;
 }
 
 // Output pass over this warp's 32-column superblocks: O = (Pi_hi + Pi_lo) Y_0
@@ -247,6 +264,7 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   auto krow = [&](int kr) { return (kr >> 2) * 16 + 2 * c.t4 + (kr & 1) + ((kr & 2) ? 8 : 0); };
   auto orow = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
   const uint64_t last_use = l2_evict_first();
+  const float2 inv2 = make_float2(c.inv, c.inv), decay2 = make_float2(c.decay, c.decay);
 
   auto issue = [&](int r, uint32_t dst) {
     const int sb = r * NW + c.warp;
@@ -302,8 +320,14 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        b[kk][q][0] = Mma<TY>::pack(v[0][q] * c.inv, v[1][q] * c.inv);
-        b[kk][q][1] = half ? 0u : Mma<TY>::pack(v[2][q] * c.inv, v[3][q] * c.inv);
+        const float2 lo = __fmul2_rn(make_float2(v[0][q], v[1][q]), inv2);
+        b[kk][q][0] = Mma<TY>::pack(lo.x, lo.y);
+        if (half) {
+          b[kk][q][1] = 0u;
+        } else {
+          const float2 hi = __fmul2_rn(make_float2(v[2][q], v[3][q]), inv2);
+          b[kk][q][1] = Mma<TY>::pack(hi.x, hi.y);
+        }
       }
     }
 #pragma unroll
@@ -338,9 +362,15 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
           const uint4 praw = *reinterpret_cast<const uint4*>(st + (KR + s) * 512 + lane * 16);
           float pf[8];
           bf16x8_to_f32(praw, pf);
+          const float2 nc2 = make_float2(-coef, -coef);
           float w[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) w[e] = fmaf(-coef, o[e], pf[e] * c.decay);
+          for (int e = 0; e < 8; e += 2) {
+            const float2 wv = __ffma2_rn(nc2, make_float2(o[e], o[e + 1]),
+                                         __fmul2_rn(make_float2(pf[e], pf[e + 1]), decay2));
+            w[e] = wv.x;
+            w[e + 1] = wv.y;
+          }
           const int64_t off = (int64_t)i * c.cols + jp;
           *reinterpret_cast<uint4*>(c.P + off) = f32_to_bf16x8(w);
           if (c.dbg) {
@@ -373,22 +403,45 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   cp_async_wait<0>();
 }
 
-// (X Y)[i][j] for symmetric fp32 MP x MP matrices with zero padding beyond m
-// and row pitch LD (a multiple of 4): rows i of X and j of Y, k in order.
+// One m16 x n8 tile of C = X Y for fp32 MP x MP matrices in shared memory
+// (row pitch LD), on the tensor cores with the 3xTF32 split: x = x_hi + x_lo
+// with both parts tf32, and x y ~ x_hi y_hi + x_hi y_lo + x_lo y_hi (the
+// dropped x_lo y_lo is ~2^-22 relative).  d[0..3] = C at rows
+// 16 mi + g (+ 8), columns 8 nj + 2 t4 (+ 1).
 template <int MP, int LD>
-__device__ __forceinline__ float dot_sym(const float* X, const float* Y, int i, int j) {
-  const float4* x = reinterpret_cast<const float4*>(X + i * LD);
-  const float4* y = reinterpret_cast<const float4*>(Y + j * LD);
-  float acc = 0.f;
+__device__ __forceinline__ void mm_tile(const float* X, const float* Y, int tile, int g, int t4,
+                                        float (&d)[4]) {
+  const int mi = tile / (MP / 8), nj = tile % (MP / 8);
+  auto split = [](float x, uint32_t& hi, uint32_t& lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+  };
+  // one accumulator per k8 step: independent chains of three products,
+  // summed in a fixed order at the end (the stage is latency-bound)
+  float acc[MP / 8][4];
 #pragma unroll
-  for (int k = 0; k < MP / 4; ++k) {
-    const float4 u = x[k], v = y[k];
-    acc = fmaf(u.x, v.x, acc);
-    acc = fmaf(u.y, v.y, acc);
-    acc = fmaf(u.z, v.z, acc);
-    acc = fmaf(u.w, v.w, acc);
+  for (int kk = 0; kk < MP / 8; ++kk) {
+    const float* x0 = X + (mi * 16 + g) * LD + kk * 8 + t4;
+    const float* y0 = Y + (kk * 8 + t4) * LD + nj * 8 + g;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    split(x0[0], ah[0], al[0]);
+    split(x0[8 * LD], ah[1], al[1]);
+    split(x0[4], ah[2], al[2]);
+    split(x0[8 * LD + 4], ah[3], al[3]);
+    split(y0[0], bh[0], bl[0]);
+    split(y0[4 * LD], bh[1], bl[1]);
+    acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
+    mma_tf32(acc[kk], al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    mma_tf32(acc[kk], ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+    mma_tf32(acc[kk], ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
   }
-  return acc;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float v = acc[0][q];
+#pragma unroll
+    for (int kk = 1; kk < MP / 8; ++kk) v += acc[kk][q];
+    d[q] = v;
+  }
 }
 
 template <typename TY, int MT, int NT, bool HALF>
@@ -399,7 +452,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   extern __shared__ __align__(128) uint8_t smem[];
   float* cpart = reinterpret_cast<float*>(smem + L::kCta);
   float* misc = reinterpret_cast<float*>(smem + L::kMisc);
-  float* rsc = misc + 16;  // per-row power-of-two scale of Pi
+  float* rsc = reinterpret_cast<float*>(smem + L::kRsc);         // per-row power-of-two scale of Pi
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + L::kTabOff);  // upper triangle (i << 16 | j)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank();
@@ -432,11 +486,16 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   float* Tm = Qm + MP * LD;
   float* Pi0 = Tm + MP * LD;
   float* Pi1 = Pi0 + MP * LD;
-  uint32_t* tab = reinterpret_cast<uint32_t*>(Pi1 + MP * LD);
-  TY* Ph = reinterpret_cast<TY*>(smem + L::kWarpPart + 5 * L::kMat + L::kTab);
+  TY* Ph = reinterpret_cast<TY*>(smem + L::kWarpPart + 5 * L::kMat);
   TY* Pl = Ph + MP * (MP + 8);
   float* Pi = Pi0;
   const int nup = m * (m + 1) / 2;
+  for (int e = tid; e < nup; e += NT) {
+    // e -> (i, j), i <= j, row-major over the upper triangle
+    int i = 0, rem = e;
+    while (rem >= m - i) { rem -= m - i; ++i; }
+    tab[e] = (uint32_t)(i << 16 | (i + rem));
+  }
 
   // 1. momentum, sum of squares and Gram matrix
   float gacc[GT::N][4];
@@ -486,11 +545,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   c.inv = a.alpha * inv_raw;
   const float inv2 = inv_raw * inv_raw;
   for (int e = tid; e < nup; e += NT) {
-    // e -> (i, j), i <= j, row-major over the upper triangle
-    int i = 0, rem = e;
-    while (rem >= m - i) { rem -= m - i; ++i; }
-    const int j = i + rem;
-    tab[e] = (uint32_t)(i << 16 | j);
+    const int i = tab[e] >> 16, j = tab[e] & 0xffff;
     float acc = 0.f;
 #pragma unroll
     for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
@@ -501,42 +556,69 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   cluster_arrive();  // done reading the peer's partials
   __syncthreads();
 
-  // 2. the k steps in m x m space
+  // 2. the k steps in m x m space, one m16 x n8 tile per warp (3xTF32)
   if (ns > 0) {
+    constexpr int TPP = (MP / 16) * (MP / 8);  // tiles of one product
+    static_assert(2 * TPP <= NW, "one tile per warp in the two-product stage");
     const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
+    // element (i, j) of this lane's accumulator slot q in tile `tile`
+    auto at = [&](int tile, int q, int& i, int& j) {
+      i = (tile / (MP / 8)) * 16 + c.g + ((q & 2) ? 8 : 0);
+      j = (tile % (MP / 8)) * 8 + 2 * c.t4 + (q & 1);
+    };
     for (int s = 0; s < ns; ++s) {
-      // Q = a I + b A + c A^2
-      for (int e = tid; e < nup; e += NT) {
-        const int i = tab[e] >> 16, j = tab[e] & 0xffff;
-        float q = fmaf(cc, dot_sym<MP, LD>(Am, Am, i, j), cb * Am[i * LD + j]);
-        if (i == j) q += ca;
-        Qm[i * LD + j] = q;
-        Qm[j * LD + i] = q;
+      const bool more = s + 1 < ns;
+      // Q = a I + b A + c A^2 (zero outside m x m)
+      if (warp < TPP) {
+        float d[4];
+        mm_tile<MP, LD>(Am, Am, warp, c.g, c.t4, d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          int i, j;
+          at(warp, q, i, j);
+          float v = 0.f;
+          if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, Am[i * LD + j], i == j ? ca : 0.f));
+          Qm[i * LD + j] = v;
+        }
       }
       __syncthreads();
       // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
       float* Pn = Pi == Pi0 ? Pi1 : Pi0;
-      const bool more = s + 1 < ns;
-      for (int e = tid; e < nup; e += NT) {
-        const int i = tab[e] >> 16, j = tab[e] & 0xffff;
-        const float pv = s == 0 ? Qm[i * LD + j] : dot_sym<MP, LD>(Qm, Pi, i, j);
-        Pn[i * LD + j] = pv;
-        Pn[j * LD + i] = pv;
+      if (warp < TPP) {
         if (more) {
-          const float t = dot_sym<MP, LD>(Qm, Qm, i, j);
-          Tm[i * LD + j] = t;
-          Tm[j * LD + i] = t;
+          float d[4];
+          mm_tile<MP, LD>(Qm, Qm, warp, c.g, c.t4, d);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            int i, j;
+            at(warp, q, i, j);
+            Tm[i * LD + j] = d[q];
+          }
+        }
+      } else if (warp < 2 * TPP) {
+        const int tile = warp - TPP;
+        float d[4];
+        if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, c.g, c.t4, d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          int i, j;
+          at(tile, q, i, j);
+          Pn[i * LD + j] = s > 0 ? d[q] : Qm[i * LD + j];
         }
       }
       Pi = Pn;
       __syncthreads();
       if (more) {
         // A <- Q^2 A (written over Q, then the two swap roles)
-        for (int e = tid; e < nup; e += NT) {
-          const int i = tab[e] >> 16, j = tab[e] & 0xffff;
-          const float v = dot_sym<MP, LD>(Tm, Am, i, j);
-          Qm[i * LD + j] = v;
-          Qm[j * LD + i] = v;
+        if (warp < TPP) {
+          float d[4];
+          mm_tile<MP, LD>(Tm, Am, warp, c.g, c.t4, d);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            int i, j;
+            at(warp, q, i, j);
+            Qm[i * LD + j] = d[q];
+          }
         }
         float* t = Am; Am = Qm; Qm = t;
         __syncthreads();
@@ -545,11 +627,13 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     // Along an exact null direction of X_0 (a zero row, say) Pi grows like
     // a^k while O does not: scale each row i of Pi by 2^-e_i into the operand
     // type's range, and O's row i by 2^e_i in the epilogue.
-    for (int i = tid; i < MP; i += NT) {
+    for (int i = warp; i < MP; i += NW) {  // one warp per row: lanes over columns
       float mx = 0.f;
-      for (int k = 0; k < m && i < m; ++k) mx = fmaxf(mx, fabsf(Pi[i * LD + k]));
+      for (int k = lane; k < m && i < m; k += 32) mx = fmaxf(mx, fabsf(Pi[i * LD + k]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const int ex = mx >= 32768.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
-      rsc[i] = exp2f((float)ex);
+      if (lane == 0) rsc[i] = exp2f((float)ex);
     }
     __syncthreads();
     // Pi in the operand type: high part and residual, zero outside m x m
