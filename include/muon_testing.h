@@ -31,6 +31,16 @@ MUON_API muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int32_
  * current device can hold at once for the given operand type; -1 on error. */
 MUON_API int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m);
 
+/* Failure detection without a GPU fault: one kernel waits on an mbarrier with
+ * the bounded wait every wait of this library uses, for at most limit_cycles
+ * SM cycles (1 .. 2^33).  arrive != 0: a second thread completes the barrier
+ * and the call returns OK.  arrive == 0: nothing completes it, the wait gives
+ * up, the kernel records the timeout in an error word and ends normally, and
+ * the call returns TIMEOUT; the context stays usable.  INVALID_ARG for a
+ * limit out of range; CUDA or OOM on a runtime failure.  Synchronises
+ * `stream`. */
+MUON_API muon_status_t muon_testing_wait_probe(int32_t arrive, int64_t limit_cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

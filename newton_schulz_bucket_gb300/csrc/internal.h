@@ -108,6 +108,10 @@ int gs_max_active_clusters(int ns_type, int m);
 // (after prepare_skinny for that m).
 int skinny_max_active_clusters(int ns_type, int m);
 
+// Test hook: one bounded mbarrier wait, completed by a second thread
+// (arrive != 0) or by nothing; on giving up it sets bit 16 of *err.
+cudaError_t launch_wait_probe(int* err, long long limit, int arrive, cudaStream_t s);
+
 // TENSOR path: tcgen05 GEMMs fed by TMA.  Tensor maps are encoded once per
 // group at plan creation (they hold the workspace addresses).
 struct TcMaps {

@@ -1,5 +1,5 @@
 // Test hooks (include/muon_testing.h): one tcgen05 product on caller buffers,
-// and the skinny kernel's cluster occupancy.
+// the skinny kernel's cluster occupancy, and a bounded wait that times out.
 #include <cstring>
 
 #include <cuda_runtime.h>
@@ -62,4 +62,19 @@ extern "C" int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m)
   k.ns_type = ns_dtype == MUON_NS_BF16 ? NS_BF16 : NS_F16;
   if (prepare_skinny(k, cfg) != cudaSuccess) return -1;
   return skinny_max_active_clusters(k.ns_type, (int)m);
+}
+
+extern "C" muon_status_t muon_testing_wait_probe(int32_t arrive, int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > (1ll << 33)) return MUON_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = nullptr;
+  if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return MUON_ERR_OOM;
+  cudaError_t e = cudaMemset(err, 0, sizeof(int));
+  if (e == cudaSuccess) e = launch_wait_probe(err, limit_cycles, arrive ? 1 : 0, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  int w = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&w, err, sizeof w, cudaMemcpyDeviceToHost);
+  cudaFree(err);
+  if (e != cudaSuccess) return MUON_ERR_CUDA;
+  return w ? MUON_ERR_TIMEOUT : MUON_OK;
 }
