@@ -70,12 +70,13 @@ struct GsLayout {
   static constexpr int SO = 4 * NW * 32 * LBO <= kCap ? 4 : (3 * NW * 32 * LBO <= kCap ? 3 : 2);
   static constexpr int kRingO = SO * NW * 32 * LBO;
   // between the passes the ring holds the per-warp Gram partials and sums of
-  // squares, then the m x m work arrays: A, Q, T, Pi (two) and Pi's
-  // operand-type high / low parts
+  // squares, then the m x m work arrays: A, Q, T, Pi (two), each stored as
+  // a tf32 high part and a tf32 residual, and Pi's operand-type high / low
+  // parts
   static constexpr int kWarpPart = NW * GT::N * 128 * 4 + NW * 4 * 4;
   static constexpr int kMat = MP * LD * 4;
   static constexpr int kPiT = MP * (MP + 8) * 2;
-  static constexpr int kMM = 5 * kMat + 2 * kPiT;
+  static constexpr int kMM = 10 * kMat + 2 * kPiT;  // A, Q, T, Pi x2, each as tf32 high + low
   static constexpr int kU0 = kRing1 > kRingO ? kRing1 : kRingO;
   static constexpr int kU = kU0 > kWarpPart + kMM ? kU0 : kWarpPart + kMM;
   static constexpr int kCta = kU;                       // this CTA's Gram partial (peer reads it)
@@ -124,7 +125,7 @@ __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uin
 
 // Momentum pass over this warp's 32-column superblocks: M' = beta M + G
 // stored, ss += M'^2 per lane, and gacc += M' M'^T on the upper Gram tiles
-// (tf32).  Lane (g, t4) holds rows 16 mi + g (+ 8) and columns
+// (tf32).  In registers lane (g, t4) holds rows 16 mi + g (+ 8) and columns
 // J + 8 t4 .. J + 8 t4 + 7; column J + 8 t4 + 2 st + e stands in the tf32
 // A-fragment slot k = t4 + 4 e of k8 step st.  All three streams keep the
 // default L2 policy: measured, evict-first reads or evict-last stores here
@@ -146,22 +147,32 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   const float2 beta2 = make_float2(c.beta, c.beta);
   float2 ss2 = make_float2(0.f, 0.f);
 
-  // ring planes (512 B each, lane-contiguous 16 B): M row s low / high half at
-  // 2 s / 2 s + 1, G row s at 2 R + s
+  // A round's slot holds the superblock as row-major tiles, so that every
+  // global access of a warp moves whole lines: M (later M') rows of 128 B
+  // whose 16-byte chunk q sits at q ^ (row & 1) (the fragment reads below are
+  // then free of bank conflicts), and G rows of 64 B.  Lanes copy in and out
+  // by rows (8 lanes per M row, 4 per G row) and read their fragments after a
+  // warp barrier.
+  constexpr int RT = 8 * R;  // rows of the tile (rows >= m are zero-filled)
+  auto mchunk = [](int row, int q) { return row * 128 + ((q ^ (row & 1)) << 4); };
   auto issue = [&](int r, uint32_t dst) {
     const int sb = r * NW + c.warp;
     if (c.vec && r < rounds && sb < nsb) {
-      const int j = c.c0 + sb * 32 + 8 * c.t4;  // n % 8 == 0: the lane's 8 columns share fate
-      const bool colok = j < c.n;
+      const int J = c.c0 + sb * 32;
 #pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int i = row_of(s);
-        const bool ok = colok && i < c.m;
-        const int64_t o = (int64_t)i * c.cols + j;
-        const float* mp = ok ? c.Mp + o : c.Mp;
-        cp_async16_hint(dst + (2 * s) * 512 + lane * 16, mp, ok ? 16 : 0, pol);
-        cp_async16_hint(dst + (2 * s + 1) * 512 + lane * 16, ok ? mp + 4 : c.Mp, ok ? 16 : 0, pol);
-        cp_async16_hint(dst + (2 * R + s) * 512 + lane * 16, ok ? (const void*)(c.G + o) : (const void*)c.G,
+      for (int k = 0; k < RT / 4; ++k) {
+        const int row = 4 * k + (lane >> 3), q = lane & 7;
+        const bool ok = row < c.m && J + 4 * q < c.n;
+        cp_async16_hint(dst + mchunk(row, q),
+                        ok ? (const void*)(c.Mp + (int64_t)row * c.cols + J + 4 * q) : (const void*)c.Mp,
+                        ok ? 16 : 0, pol);
+      }
+#pragma unroll
+      for (int k = 0; k < RT / 8; ++k) {
+        const int row = 8 * k + (lane >> 2), q = lane & 3;
+        const bool ok = row < c.m && J + 8 * q < c.n;
+        cp_async16_hint(dst + RT * 128 + row * 64 + q * 16,
+                        ok ? (const void*)(c.G + (int64_t)row * c.cols + J + 8 * q) : (const void*)c.G,
                         ok ? 16 : 0, pol);
       }
     }
@@ -171,34 +182,32 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
 #pragma unroll
   for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
 
-  auto process = [&](int r, const uint8_t* st) {
+  auto process = [&](int r, uint8_t* st) {
     const int sb = r * NW + c.warp;
     if (r >= rounds || sb >= nsb) return;
-    const int j0 = c.c0 + sb * 32 + 8 * c.t4;
+    const int J = c.c0 + sb * 32;
+    const int j0 = J + 8 * c.t4;
     // tv[mi][st][h][e]: row 16 mi + g + 8 h, tf32 slot k = t4 + 4 e of k8 step st
     uint32_t tv[MT][4][2][2];
+    if (c.vec) __syncwarp();  // every lane's copies of this round have landed
 #pragma unroll
     for (int s = 0; s < R; ++s) {
       const int i = row_of(s);
       float v[8];
       if (c.vec) {
-        const float4 m0 = *reinterpret_cast<const float4*>(st + (2 * s) * 512 + lane * 16);
-        const float4 m1 = *reinterpret_cast<const float4*>(st + (2 * s + 1) * 512 + lane * 16);
+        float4* m0p = reinterpret_cast<float4*>(st + mchunk(i, 2 * c.t4));
+        float4* m1p = reinterpret_cast<float4*>(st + mchunk(i, 2 * c.t4 + 1));
+        const float4 m0 = *m0p, m1 = *m1p;
         float gf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + (2 * R + s) * 512 + lane * 16), gf);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + RT * 128 + i * 64 + c.t4 * 16), gf);
         const float2 r0 = __ffma2_rn(beta2, make_float2(m0.x, m0.y), make_float2(gf[0], gf[1]));
         const float2 r1 = __ffma2_rn(beta2, make_float2(m0.z, m0.w), make_float2(gf[2], gf[3]));
         const float2 r2 = __ffma2_rn(beta2, make_float2(m1.x, m1.y), make_float2(gf[4], gf[5]));
         const float2 r3 = __ffma2_rn(beta2, make_float2(m1.z, m1.w), make_float2(gf[6], gf[7]));
         v[0] = r0.x; v[1] = r0.y; v[2] = r1.x; v[3] = r1.y;
         v[4] = r2.x; v[5] = r2.y; v[6] = r3.x; v[7] = r3.y;
-        if (i < c.m && j0 < c.n) {
-          float* dp = c.Mp + (int64_t)i * c.cols + j0;
-          st_hint(dp, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                                 __float_as_uint(v[3])), pol);
-          st_hint(dp + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]),
-                                     __float_as_uint(v[7])), pol);
-        }
+        *m0p = make_float4(v[0], v[1], v[2], v[3]);  // M' replaces M in the tile
+        *m1p = make_float4(v[4], v[5], v[6], v[7]);
       } else {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -219,6 +228,17 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
         tv[s >> 1][st4][s & 1][1] = to_tf32(v[2 * st4 + 1]);
       }
     }
+    if (c.vec) {
+      // M' out by rows, whole lines (each lane stores the chunks it will refill)
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < RT / 4; ++k) {
+        const int row = 4 * k + (lane >> 3), q = lane & 7;
+        if (row < c.m && J + 4 * q < c.n)
+          st_hint(c.Mp + (int64_t)row * c.cols + J + 4 * q,
+                  *reinterpret_cast<const uint4*>(st + mchunk(row, q)), pol);
+      }
+    }
     if (HALF) {
 #pragma unroll
       for (int st4 = 0; st4 < 4; ++st4) tv[MT - 1][st4][1][0] = tv[MT - 1][st4][1][1] = 0u;
@@ -236,7 +256,7 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   for (int r = 0; r < rounds; ++r) {
     cp_async_wait<S - 1>();
     process(r, ring_warp + (r % S) * kSlot);
-    // round r now lives in registers: refill its slot
+    // round r is consumed (its M' copied out): refill its slot
     issue(r + S, ring0 + (r % S) * kSlot);
   }
   cp_async_wait<0>();
@@ -403,37 +423,49 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   cp_async_wait<0>();
 }
 
-// One m16 x n8 tile of C = X Y for fp32 MP x MP matrices in shared memory
-// (row pitch LD), on the tensor cores with the 3xTF32 split: x = x_hi + x_lo
-// with both parts tf32, and x y ~ x_hi y_hi + x_hi y_lo + x_lo y_hi (the
-// dropped x_lo y_lo is ~2^-22 relative).  d[0..3] = C at rows
-// 16 mi + g (+ 8), columns 8 nj + 2 t4 (+ 1).
+// An m x m fp32 matrix kept as two tf32 parts, x = hi + lo (both exact
+// tf32 values, pitch LD), so that the tensor-core products below read their
+// operands already split.
+struct SplitMat {
+  uint32_t* hi;
+  uint32_t* lo;
+};
+template <int LD>
+__device__ __forceinline__ void put(const SplitMat& X, int i, int j, float v) {
+  const uint32_t h = to_tf32(v);
+  X.hi[i * LD + j] = h;
+  X.lo[i * LD + j] = to_tf32(v - __uint_as_float(h));
+}
+template <int LD>
+__device__ __forceinline__ float get(const SplitMat& X, int i, int j) {
+  return __uint_as_float(X.hi[i * LD + j]) + __uint_as_float(X.lo[i * LD + j]);
+}
+
+// One m16 x n8 tile of C = X Y (MP x MP, zero beyond m), on the tensor cores
+// with the 3xTF32 split: x y ~ x_hi y_hi + x_hi y_lo + x_lo y_hi (the dropped
+// x_lo y_lo is ~2^-22 relative).  k8 steps beyond m (ks of them are live)
+// are skipped.  d[0..3] = C at rows 16 mi + g (+ 8), columns 8 nj + 2 t4
+// (+ 1).
 template <int MP, int LD>
-__device__ __forceinline__ void mm_tile(const float* X, const float* Y, int tile, int g, int t4,
-                                        float (&d)[4]) {
+__device__ __forceinline__ void mm_tile(const SplitMat& X, const SplitMat& Y, int tile, int ks, int g,
+                                        int t4, float (&d)[4]) {
   const int mi = tile / (MP / 8), nj = tile % (MP / 8);
-  auto split = [](float x, uint32_t& hi, uint32_t& lo) {
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
-  };
   // one accumulator per k8 step: independent chains of three products,
   // summed in a fixed order at the end (the stage is latency-bound)
   float acc[MP / 8][4];
 #pragma unroll
   for (int kk = 0; kk < MP / 8; ++kk) {
-    const float* x0 = X + (mi * 16 + g) * LD + kk * 8 + t4;
-    const float* y0 = Y + (kk * 8 + t4) * LD + nj * 8 + g;
-    uint32_t ah[4], al[4], bh[2], bl[2];
-    split(x0[0], ah[0], al[0]);
-    split(x0[8 * LD], ah[1], al[1]);
-    split(x0[4], ah[2], al[2]);
-    split(x0[8 * LD + 4], ah[3], al[3]);
-    split(y0[0], bh[0], bl[0]);
-    split(y0[4 * LD], bh[1], bl[1]);
     acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
-    mma_tf32(acc[kk], al[0], al[1], al[2], al[3], bh[0], bh[1]);
-    mma_tf32(acc[kk], ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-    mma_tf32(acc[kk], ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+    if (kk < ks) {
+      const int xo = (mi * 16 + g) * LD + kk * 8 + t4;
+      const int yo = (kk * 8 + t4) * LD + nj * 8 + g;
+      const uint32_t ah0 = X.hi[xo], ah1 = X.hi[xo + 8 * LD], ah2 = X.hi[xo + 4], ah3 = X.hi[xo + 8 * LD + 4];
+      const uint32_t al0 = X.lo[xo], al1 = X.lo[xo + 8 * LD], al2 = X.lo[xo + 4], al3 = X.lo[xo + 8 * LD + 4];
+      const uint32_t bh0 = Y.hi[yo], bh1 = Y.hi[yo + 4 * LD], bl0 = Y.lo[yo], bl1 = Y.lo[yo + 4 * LD];
+      mma_tf32(acc[kk], al0, al1, al2, al3, bh0, bh1);
+      mma_tf32(acc[kk], ah0, ah1, ah2, ah3, bl0, bl1);
+      mma_tf32(acc[kk], ah0, ah1, ah2, ah3, bh0, bh1);
+    }
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -481,14 +513,12 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   // m x m work arrays (aliasing the ring between the two passes)
   float* wpart = reinterpret_cast<float*>(smem);
   float* wss = wpart + NW * GT::N * 128;
-  float* Am = reinterpret_cast<float*>(smem + L::kWarpPart);
-  float* Qm = Am + MP * LD;
-  float* Tm = Qm + MP * LD;
-  float* Pi0 = Tm + MP * LD;
-  float* Pi1 = Pi0 + MP * LD;
-  TY* Ph = reinterpret_cast<TY*>(smem + L::kWarpPart + 5 * L::kMat);
+  uint32_t* mmbase = reinterpret_cast<uint32_t*>(smem + L::kWarpPart);
+  auto mat = [&](int k) { return SplitMat{mmbase + (2 * k) * MP * LD, mmbase + (2 * k + 1) * MP * LD}; };
+  SplitMat Am = mat(0), Qm = mat(1), Tm = mat(2), Pi0 = mat(3), Pi1 = mat(4);
+  TY* Ph = reinterpret_cast<TY*>(smem + L::kWarpPart + 10 * L::kMat);
   TY* Pl = Ph + MP * (MP + 8);
-  float* Pi = Pi0;
+  SplitMat Pi = Pi0;
   const int nup = m * (m + 1) / 2;
   for (int e = tid; e < nup; e += NT) {
     // e -> (i, j), i <= j, row-major over the upper triangle
@@ -511,7 +541,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
       for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * a.cols + c.c0, bytes);
   }
   __syncthreads();  // every warp's ring is drained before it is reused
-  for (int e = tid; e < 5 * MP * LD; e += NT) Am[e] = 0.f;  // m x m arrays, padding included
+  for (int e = tid; e < 10 * MP * LD; e += NT) mmbase[e] = 0u;  // m x m arrays, padding included
   // per-warp partials, then warps summed in a fixed order into this CTA's partial
   ss = warp_sum(ss);
   if (lane == 0) wss[warp] = ss;
@@ -550,8 +580,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 #pragma unroll
     for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
     acc *= inv2;
-    Am[i * LD + j] = acc;
-    Am[j * LD + i] = acc;
+    put<LD>(Am, i, j, acc);
+    put<LD>(Am, j, i, acc);
   }
   cluster_arrive();  // done reading the peer's partials
   __syncthreads();
@@ -561,6 +591,9 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     constexpr int TPP = (MP / 16) * (MP / 8);  // tiles of one product
     static_assert(2 * TPP <= NW, "one tile per warp in the two-product stage");
     const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
+    const int ks = (m + 7) / 8;  // live k8 steps
+    // a tile wholly beyond m (rows or columns) stays zero and is skipped
+    auto live = [&](int tile) { return (tile / (MP / 8)) * 16 < m && (tile % (MP / 8)) * 8 < m; };
     // element (i, j) of this lane's accumulator slot q in tile `tile`
     auto at = [&](int tile, int q, int& i, int& j) {
       i = (tile / (MP / 8)) * 16 + c.g + ((q & 2) ? 8 : 0);
@@ -569,58 +602,63 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     for (int s = 0; s < ns; ++s) {
       const bool more = s + 1 < ns;
       // Q = a I + b A + c A^2 (zero outside m x m)
-      if (warp < TPP) {
+      if (warp < TPP && live(warp)) {
         float d[4];
-        mm_tile<MP, LD>(Am, Am, warp, c.g, c.t4, d);
+        mm_tile<MP, LD>(Am, Am, warp, ks, c.g, c.t4, d);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           int i, j;
           at(warp, q, i, j);
           float v = 0.f;
-          if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, Am[i * LD + j], i == j ? ca : 0.f));
-          Qm[i * LD + j] = v;
+          if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, get<LD>(Am, i, j), i == j ? ca : 0.f));
+          put<LD>(Qm, i, j, v);
         }
       }
       __syncthreads();
       // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
-      float* Pn = Pi == Pi0 ? Pi1 : Pi0;
+      SplitMat Pn = Pi.hi == Pi0.hi ? Pi1 : Pi0;
       if (warp < TPP) {
-        if (more) {
+        if (more && live(warp)) {
           float d[4];
-          mm_tile<MP, LD>(Qm, Qm, warp, c.g, c.t4, d);
+          mm_tile<MP, LD>(Qm, Qm, warp, ks, c.g, c.t4, d);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int i, j;
             at(warp, q, i, j);
-            Tm[i * LD + j] = d[q];
+            put<LD>(Tm, i, j, d[q]);
           }
         }
-      } else if (warp < 2 * TPP) {
+      } else if (warp < 2 * TPP && live(warp - TPP)) {
         const int tile = warp - TPP;
         float d[4];
-        if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, c.g, c.t4, d);
+        if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, ks, c.g, c.t4, d);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           int i, j;
           at(tile, q, i, j);
-          Pn[i * LD + j] = s > 0 ? d[q] : Qm[i * LD + j];
+          if (s > 0) {
+            put<LD>(Pn, i, j, d[q]);
+          } else {
+            Pn.hi[i * LD + j] = Qm.hi[i * LD + j];
+            Pn.lo[i * LD + j] = Qm.lo[i * LD + j];
+          }
         }
       }
       Pi = Pn;
       __syncthreads();
       if (more) {
         // A <- Q^2 A (written over Q, then the two swap roles)
-        if (warp < TPP) {
+        if (warp < TPP && live(warp)) {
           float d[4];
-          mm_tile<MP, LD>(Tm, Am, warp, c.g, c.t4, d);
+          mm_tile<MP, LD>(Tm, Am, warp, ks, c.g, c.t4, d);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int i, j;
             at(warp, q, i, j);
-            Qm[i * LD + j] = d[q];
+            put<LD>(Qm, i, j, d[q]);
           }
         }
-        float* t = Am; Am = Qm; Qm = t;
+        const SplitMat t = Am; Am = Qm; Qm = t;
         __syncthreads();
       }
     }
@@ -629,7 +667,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     // type's range, and O's row i by 2^e_i in the epilogue.
     for (int i = warp; i < MP; i += NW) {  // one warp per row: lanes over columns
       float mx = 0.f;
-      for (int k = lane; k < m && i < m; k += 32) mx = fmaxf(mx, fabsf(Pi[i * LD + k]));
+      for (int k = lane; k < m && i < m; k += 32) mx = fmaxf(mx, fabsf(get<LD>(Pi, i, k)));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const int ex = mx >= 32768.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
@@ -640,7 +678,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     for (int e = tid; e < MP * MP; e += NT) {
       const int i = e / MP, j = e - (e / MP) * MP;
       float v = 0.f;
-      if (i < m && j < m) v = Pi[i * LD + j] / rsc[i];
+      if (i < m && j < m) v = get<LD>(Pi, i, j) / rsc[i];
       const TY hi = from_f32<TY>(v);
       Ph[i * (MP + 8) + j] = hi;
       Pl[i * (MP + 8) + j] = from_f32<TY>(v - to_f32(hi));
