@@ -150,6 +150,29 @@ MUON_API muon_status_t muon_plan_describe(const muon_shape_t* shapes, int32_t n_
                                           int64_t member_cap, int64_t* n_members,
                                           size_t* workspace_bytes);
 
+/* Host-only ownership planner for data-parallel replicas: assigns every
+ * member matrix (numbered as muon_plan_describe numbers them) to one of
+ * n_ranks ranks so that the estimated Newton-Schulz cost is balanced.
+ * Matrices are the atomic units, a 3-D parameter's experts are assigned one
+ * by one, and the assignment is greedy: members in decreasing cost (then
+ * increasing index), each to the rank with the least cost so far (then the
+ * lowest rank) («MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升»,
+ * HSDP分组去冗余: replicas split the parameters with a greedy algorithm for
+ * balance; «关于分布式Muon的想法整合及讨论» §3: whole matrices per owner,
+ * balanced by compute cost, not size).  A member's cost is its estimated
+ * seconds on this library's path for its group (memory traffic over HBM
+ * bandwidth, Newton-Schulz FLOPs over the tensor rate; nominal rates).  The
+ * result is deterministic: a function of the shapes, options, ns_steps and
+ * n_ranks only.  owner: member_cap >= member count entries, receives ranks in
+ * [0, n_ranks); member_cost (nullable, member_cap entries) and rank_cost
+ * (nullable, n_ranks entries) receive seconds.  No communication and no
+ * device.  Errors: INVALID_ARG (as muon_plan_describe; n_ranks not in
+ * [1, 2^20]; ns_steps not in [0, 1000]; owner NULL or too short). */
+MUON_API muon_status_t muon_plan_assign(const muon_shape_t* shapes, int32_t n_params,
+                                        const muon_plan_options* opts, int32_t ns_steps,
+                                        int32_t n_ranks, int32_t* owner, int64_t member_cap,
+                                        double* member_cost, double* rank_cost);
+
 /* Builds a plan on CUDA device `device`: the bucketing above, per-group path
  * and tile choices (functions of (rows, cols) only, never of the batch size,
  * so a matrix gets bit-identical results in any batch), and every device

@@ -12,7 +12,7 @@ from typing import Dict, List, Sequence
 from . import _capi as _c
 from ._capi import MuonError  # noqa: F401
 
-__all__ = ["MuonPlan", "describe", "load_library", "MuonError", "QUINTIC"]
+__all__ = ["MuonPlan", "describe", "assign_owners", "load_library", "MuonError", "QUINTIC"]
 
 QUINTIC = (3.4445, -4.7750, 2.0315)
 
@@ -81,6 +81,26 @@ def describe(shapes: Sequence[Sequence[int]], **opts) -> Dict:
     return {"groups": [_group_dict(groups[i]) for i in range(ng.value)],
             "members": [(mp[i], me[i]) for i in range(nm.value)],
             "workspace_bytes": ws.value}
+
+
+def assign_owners(shapes: Sequence[Sequence[int]], n_ranks: int, ns_steps: int = 5, **opts) -> Dict:
+    """Host-only greedy, cost-balanced ownership of every member matrix over
+    n_ranks data-parallel replicas (muon_plan_assign).  Returns the members
+    (parameter, expert) in plan order, each member's owner rank and estimated
+    cost (seconds), and each rank's summed cost."""
+    L = _c.load()
+    d = describe(shapes, **opts)
+    nm = len(d["members"])
+    sh = _shapes(shapes)
+    o = _options(**opts)
+    owner = (C.c_int32 * max(nm, 1))()
+    mcost = (C.c_double * max(nm, 1))()
+    rcost = (C.c_double * max(int(n_ranks), 1))()
+    _c.check(L.muon_plan_assign(sh, len(shapes), C.byref(o), int(ns_steps), int(n_ranks), owner, nm,
+                                mcost, rcost), "muon_plan_assign")
+    return {"members": d["members"], "owner": [owner[i] for i in range(nm)],
+            "member_cost": [mcost[i] for i in range(nm)],
+            "rank_cost": [rcost[r] for r in range(int(n_ranks))]}
 
 
 class MuonPlan:

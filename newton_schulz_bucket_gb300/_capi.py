@@ -59,6 +59,7 @@ EXPORTED_TESTING = ["muon_testing_tc_gemm", "muon_testing_skinny_max_clusters",
 EXPORTED = ["muon_default_options", "muon_plan_describe", "muon_plan_create", "muon_step",
             "muon_step_host", "muon_plan_destroy", "muon_plan_num_groups",
             "muon_plan_group_info", "muon_plan_workspace_bytes", "muon_debug_copy_update",
+            "muon_plan_assign",
             "muon_plan_check_error", "muon_plan_group_elapsed_ms", "muon_step_skinny_static",
             "muon_status_string",
             "muon_last_error", "muon_version"]
@@ -93,6 +94,8 @@ def load() -> C.CDLL:
                             f32, f32, f32, vp]
     L.muon_step_host.argtypes = L.muon_step.argtypes
     L.muon_plan_destroy.argtypes = [vp]
+    L.muon_plan_assign.argtypes = [C.POINTER(muon_shape_t), i32, C.POINTER(muon_plan_options), i32, i32,
+                                   C.POINTER(i32), i64, C.POINTER(C.c_double), C.POINTER(C.c_double)]
     L.muon_plan_num_groups.argtypes = [vp]
     L.muon_plan_num_groups.restype = i32
     L.muon_plan_group_info.argtypes = [vp, i32, C.POINTER(muon_group_info_t)]

@@ -13,8 +13,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <map>
 #include <new>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -455,6 +457,66 @@ muon_status_t muon_plan_describe(const muon_shape_t* shapes, int32_t n_params,
     if (member_expert) member_expert[i] = d.member_expert[i];
   }
   if (workspace_bytes) *workspace_bytes = d.ws_bytes;
+  return MUON_OK;
+}
+
+namespace {
+
+// Estimated seconds of one member's step on this library's path for its
+// group: the larger of its compulsory memory traffic over the HBM rate and
+// its Newton-Schulz work over the tensor (or fp32 FMA) rate.  Only ratios
+// matter to the planner, so nominal rates are used.
+double member_seconds(const GroupPlan& g, int32_t ns_steps, bool f32) {
+  constexpr double kHbm = 6.8e12, kTensor = 1.7e15, kFp32 = 6.0e13;
+  const double m = (double)g.m, n = (double)g.n;
+  const double bytes = m * n * (f32 ? 20.0 : 14.0);
+  const double flops = (double)ns_steps * (4 * m * m * n + 2 * m * m * m);
+  const double rate = f32 ? kFp32 : kTensor;
+  return std::max(bytes / kHbm, g.path == PATH_SKINNY ? 0.0 : flops / rate);
+}
+
+}  // namespace
+
+muon_status_t muon_plan_assign(const muon_shape_t* shapes, int32_t n_params,
+                               const muon_plan_options* opts, int32_t ns_steps, int32_t n_ranks,
+                               int32_t* owner, int64_t member_cap, double* member_cost,
+                               double* rank_cost) {
+  if (n_ranks < 1 || n_ranks > (1 << 20))
+    return fail(MUON_ERR_INVALID_ARG, "n_ranks %d out of [1, 2^20]", n_ranks);
+  if (ns_steps < 0 || ns_steps > 1000)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps %d out of [0, 1000]", ns_steps);
+  PlanDesc d;
+  if (muon_status_t st = build_desc(shapes, n_params, opts, &d)) return st;
+  const int64_t nm = (int64_t)d.member_param.size();
+  if (!owner || member_cap < nm)
+    return fail(MUON_ERR_INVALID_ARG, "owner must hold %lld members", (long long)nm);
+  const bool f32 = d.opt.mode == MUON_MODE_FP32;
+  std::vector<double> cost((size_t)nm);
+  for (const GroupPlan& g : d.groups) {
+    const double t = member_seconds(g, ns_steps, f32);
+    for (int64_t i = 0; i < g.batch; ++i) cost[(size_t)(g.first_member + i)] = t;
+  }
+  // longest processing time first: members by cost (descending, then index),
+  // each to the rank with the least load so far (then the lowest rank)
+  std::vector<int64_t> order((size_t)nm);
+  for (int64_t i = 0; i < nm; ++i) order[(size_t)i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int64_t x, int64_t y) { return cost[(size_t)x] > cost[(size_t)y]; });
+  using Slot = std::pair<double, int32_t>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int32_t r = 0; r < n_ranks; ++r) heap.push({0.0, r});
+  std::vector<double> load((size_t)n_ranks, 0.0);
+  for (int64_t i : order) {
+    const Slot s = heap.top();
+    heap.pop();
+    owner[i] = s.second;
+    load[(size_t)s.second] = s.first + cost[(size_t)i];
+    heap.push({load[(size_t)s.second], s.second});
+  }
+  if (member_cost)
+    for (int64_t i = 0; i < nm; ++i) member_cost[i] = cost[(size_t)i];
+  if (rank_cost)
+    for (int32_t r = 0; r < n_ranks; ++r) rank_cost[r] = load[(size_t)r];
   return MUON_OK;
 }
 
