@@ -42,7 +42,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile 
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;
-      atomicOr(err, code);
+      if (err) atomicOr(err, code);
       return false;
     }
   }
