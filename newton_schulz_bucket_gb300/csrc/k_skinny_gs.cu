@@ -99,7 +99,7 @@ struct Wide {
 // Per-thread state of one member's two data passes.
 struct GsCtx {
   int lane, warp, g, t4, m, n, c0, NB;  // NB: 16-column blocks of this CTA (even)
-  bool vec;            // rows <= cols, cols % 8 == 0, M', G and P 16-byte aligned
+  bool vec;            // rows <= cols, cols % 8 == 0, 32 cols < 2^31, M', G and P 16-byte aligned
   float* Mp;
   const __nv_bfloat16* G;
   __nv_bfloat16* P;
@@ -286,24 +286,35 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   const uint64_t last_use = l2_evict_first();
   const float2 inv2 = make_float2(c.inv, c.inv), decay2 = make_float2(c.decay, c.decay);
 
+  // loop-invariant element offsets of this lane's rows (32 cols < 2^31 on the
+  // vector path); rows >= m read as zero
+  int moff[KR], poff[R];
+  uint32_t mok = 0, pok = 0;
+#pragma unroll
+  for (int kr = 0; kr < KR; ++kr) {
+    moff[kr] = krow(kr) * c.cols;
+    if (krow(kr) < c.m) mok |= 1u << kr;
+  }
+#pragma unroll
+  for (int s = 0; s < R; ++s) {
+    poff[s] = orow(s) * c.cols;
+    if (orow(s) < c.m) pok |= 1u << s;
+  }
+
   auto issue = [&](int r, uint32_t dst) {
     const int sb = r * NW + c.warp;
     if (c.vec && r < rounds && sb < nsb) {
       const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
+      const bool cm = jm < c.n, cpp = jp < c.n;  // n % 8 == 0: a lane's columns share fate
 #pragma unroll
       for (int kr = 0; kr < KR; ++kr) {
-        const int i = krow(kr);
-        const bool ok = i < c.m && jm < c.n;
-        cp_async16_hint(dst + kr * 512 + lane * 16,
-                        ok ? (const void*)(c.Mp + (int64_t)i * c.cols + jm) : (const void*)c.Mp, ok ? 16 : 0,
-                        last_use);
+        const bool ok = cm && ((mok >> kr) & 1u);
+        cp_async16_hint(dst + kr * 512 + lane * 16, c.Mp + (ok ? moff[kr] + jm : 0), ok ? 16 : 0, last_use);
       }
 #pragma unroll
       for (int s = 0; s < R; ++s) {
-        const int i = orow(s);
-        const bool ok = i < c.m && jp < c.n;  // n % 8 == 0: the lane's 8 columns share fate
-        cp_async16_hint(dst + (KR + s) * 512 + lane * 16,
-                        ok ? (const void*)(c.P + (int64_t)i * c.cols + jp) : (const void*)c.P, ok ? 16 : 0,
+        const bool ok = cpp && ((pok >> s) & 1u);
+        cp_async16_hint(dst + (KR + s) * 512 + lane * 16, c.P + (ok ? poff[s] + jp : 0), ok ? 16 : 0,
                         last_use);
       }
     }
@@ -391,7 +402,7 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
             w[e] = wv.x;
             w[e + 1] = wv.y;
           }
-          const int64_t off = (int64_t)i * c.cols + jp;
+          const int off = poff[s] + jp;
           *reinterpret_cast<uint4*>(c.P + off) = f32_to_bf16x8(w);
           if (c.dbg) {
             float* dp = c.dbg + off;
@@ -501,7 +512,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   c.P = static_cast<__nv_bfloat16*>(mp.P);
   c.cols = a.cols;
   c.wd = Wide{a.cols, a.T};
-  c.vec = !a.T && (a.cols % 8 == 0) && aligned16(c.Mp) && aligned16(c.G) && aligned16(c.P);
+  c.vec = !a.T && (a.cols % 8 == 0) && 32ll * a.cols < (1ll << 31) && aligned16(c.Mp) &&
+          aligned16(c.G) && aligned16(c.P);
   c.dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
   const int ns = a.sc->ns_steps;
   c.beta = a.sc->beta;
