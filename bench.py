@@ -403,7 +403,7 @@ def main():
     dom = max(range(len(groups)), key=lambda g: per_group[g]["ms"] or 0)
     dg = per_group[dom]
     if dg["path"] == "skinny":
-        gram_space = min(groups[dom]["rows"], groups[dom]["cols"]) <= 32 and w.ns_steps <= 64
+        gram_space = w.ns_steps <= 64
         kfile = "k_skinny_gs.cu" if gram_space else "k_skinny.cu"
         roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dg.get("roofline_frac"),

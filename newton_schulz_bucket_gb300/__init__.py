@@ -225,8 +225,8 @@ class MuonPlan:
         n = 0
         for g in self.groups():
             if g["path"] == "skinny":
-                # one fused kernel in Gram space (m <= 32, up to 64 steps), else momentum + iteration
-                n += 1 if min(g["rows"], g["cols"]) <= 32 and ns_steps <= 64 else 2
+                # one fused kernel in Gram space (up to 64 steps), else momentum + iteration
+                n += 1 if ns_steps <= 64 else 2
             else:
                 n += 4 + 3 * int(ns_steps)
         return n

@@ -70,7 +70,7 @@ struct SkinnyCfg {
   int32_t smem;      // unused (shared memory is fixed per instantiation)
   int32_t blk;       // bytes of one 16-column block in the fragment workspace
   int64_t ws_bytes;  // fragment workspace bytes per member (direct kernel)
-  int32_t gram_space;  // m <= 32: the Gram-space kernel serves ns_steps <= kGramSpaceMaxSteps
+  int32_t gram_space;  // the Gram-space kernel serves ns_steps <= kGramSpaceMaxSteps
 };
 
 // Step counts the Gram-space kernel takes: along an exact null direction of
@@ -94,8 +94,8 @@ cudaError_t launch_simt_gram(const KArgs& a, const void* y, cudaStream_t s);
 cudaError_t launch_simt_poly(const KArgs& a, cudaStream_t s);
 cudaError_t launch_simt_update(const KArgs& a, const void* ysrc, void* ydst, cudaStream_t s);
 
-// Skinny path, the whole step of a group: for m <= 32 and k <=
-// kGramSpaceMaxSteps one kernel (momentum, then Newton-Schulz in Gram space,
+// Skinny path, the whole step of a group: for k <= kGramSpaceMaxSteps one
+// kernel (momentum, then Newton-Schulz in Gram space,
 // then the write, one cluster per member, no workspace); otherwise the
 // momentum kernel, then the direct iteration (iterate in a fragment-ordered
 // workspace a.y0).

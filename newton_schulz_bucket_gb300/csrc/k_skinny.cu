@@ -525,7 +525,7 @@ bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg) {
   cfg->blk = blk;
   cfg->ws_bytes = (int64_t)kCL * (cfg->width / 16) * blk;  // per member (direct kernel)
   cfg->smem = 0;
-  cfg->gram_space = m <= 32;
+  cfg->gram_space = 1;  // every skinny m (<= 64); the step count decides at launch
   return true;
 }
 
@@ -542,11 +542,13 @@ cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, int32_t ns_steps
 }
 
 int skinny_max_active_clusters(int ns_type, int m) {
-  if (m <= 32) return gs_max_active_clusters(ns_type, m);
   const int mt = (m + 15) / 16;
   const bool half = half_last_tile(m, mt);
-  if (ns_type == NS_F16) return half ? clusters_mt<__half, true>(mt) : clusters_mt<__half, false>(mt);
-  return half ? clusters_mt<__nv_bfloat16, true>(mt) : clusters_mt<__nv_bfloat16, false>(mt);
+  const int direct = ns_type == NS_F16 ? (half ? clusters_mt<__half, true>(mt) : clusters_mt<__half, false>(mt))
+                                       : (half ? clusters_mt<__nv_bfloat16, true>(mt)
+                                               : clusters_mt<__nv_bfloat16, false>(mt));
+  const int gs = gs_max_active_clusters(ns_type, m);  // either kernel may serve a step
+  return gs < direct ? gs : direct;
 }
 
 }  // namespace muon

@@ -77,8 +77,11 @@ struct GsLayout {
   static constexpr int kMat = MP * LD * 4;
   static constexpr int kPiT = MP * (MP + 8) * 2;
   static constexpr int kMM = 10 * kMat + 2 * kPiT;  // A, Q, T, Pi x2, each as tf32 high + low
+  // the rings, the per-warp partials and the m x m arrays are live one after
+  // the other and share the same bytes
   static constexpr int kU0 = kRing1 > kRingO ? kRing1 : kRingO;
-  static constexpr int kU = kU0 > kWarpPart + kMM ? kU0 : kWarpPart + kMM;
+  static constexpr int kU1 = kWarpPart > kMM ? kWarpPart : kMM;
+  static constexpr int kU = kU0 > kU1 ? kU0 : kU1;
   static constexpr int kCta = kU;                       // this CTA's Gram partial (peer reads it)
   static constexpr int kMisc = kCta + MP * MP * 4;      // [0] sum of squares (peer reads it)
   static constexpr int kRsc = kMisc + 64;               // Pi's row scales
@@ -263,66 +266,99 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   ss += ss2.x + ss2.y;
 }
 
+// The output pass's ring and its copies.  Between the passes the m x m
+// stage uses the ring's first kBusy slots; the other kEarly slots take the
+// output pass's first rounds before that stage starts, so that its loads
+// overlap the latency-bound m x m work.  Round r lives in slot slot(r).
+template <int MT, int NT, bool HALF>
+struct GsOutRing {
+  using L = GsLayout<MT, NT, HALF>;
+  static constexpr int NW = L::NW, S = L::SO, LB = L::LBO, R = L::R, KR = L::KR;
+  static constexpr uint32_t kSlot = NW * 32 * LB;
+  static constexpr int kLive = L::kWarpPart > L::kMM ? L::kWarpPart : L::kMM;
+  static constexpr int kBusy = (kLive + (int)kSlot - 1) / (int)kSlot;
+  static constexpr int kEarly = S > kBusy ? S - kBusy : 0;
+  static __device__ __forceinline__ int slot(int r) { return (r + kBusy) % S; }
+
+  // loop-invariant element offsets of this lane's rows (32 cols < 2^31 on the
+  // vector path); rows >= m read as zero
+  int moff[KR], poff[R];
+  uint32_t mok, pok;
+  uint32_t ring0;
+  int rounds, nsb;
+
+  __device__ __forceinline__ static int krow(const GsCtx& c, int kr) {
+    return (kr >> 2) * 16 + 2 * c.t4 + (kr & 1) + ((kr & 2) ? 8 : 0);
+  }
+  __device__ __forceinline__ static int orow(const GsCtx& c, int s) {
+    return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0);
+  }
+  __device__ __forceinline__ GsOutRing(const GsCtx& c, uint8_t* ring) {
+    ring0 = smem_u32(ring + c.warp * 32 * LB);
+    nsb = c.NB / 2;  // superblocks of this CTA
+    rounds = (nsb + NW - 1) / NW;
+    mok = pok = 0;
+#pragma unroll
+    for (int kr = 0; kr < KR; ++kr) {
+      moff[kr] = krow(c, kr) * c.cols;
+      if (krow(c, kr) < c.m) mok |= 1u << kr;
+    }
+#pragma unroll
+    for (int s = 0; s < R; ++s) {
+      poff[s] = orow(c, s) * c.cols;
+      if (orow(c, s) < c.m) pok |= 1u << s;
+    }
+  }
+  // round r's M' and P into its slot, as one commit group (empty past the end)
+  __device__ __forceinline__ void issue(const GsCtx& c, int r, uint64_t pol) const {
+    const int sb = r * NW + c.warp;
+    if (c.vec && r < rounds && sb < nsb) {
+      const uint32_t dst = ring0 + slot(r) * kSlot;
+      const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
+      const bool cm = jm < c.n, cpp = jp < c.n;  // n % 8 == 0: a lane's columns share fate
+#pragma unroll
+      for (int kr = 0; kr < KR; ++kr) {
+        const bool ok = cm && ((mok >> kr) & 1u);
+        cp_async16_hint(dst + kr * 512 + c.lane * 16, c.Mp + (ok ? moff[kr] + jm : 0), ok ? 16 : 0, pol);
+      }
+#pragma unroll
+      for (int s = 0; s < R; ++s) {
+        const bool ok = cpp && ((pok >> s) & 1u);
+        cp_async16_hint(dst + (KR + s) * 512 + c.lane * 16, c.P + (ok ? poff[s] + jp : 0), ok ? 16 : 0,
+                        pol);
+      }
+    }
+    cp_async_commit();
+  }
+};
+
 // Output pass over this warp's 32-column superblocks: O = (Pi_hi + Pi_lo) Y_0
 // and P' = P (1 - lr wd) - lr s O.  Y_0 is loaded straight into B fragments:
 // lane (g, t4) holds rows 16 kk + 2 t4 + {0, 1, 8, 9} of columns
 // J + 4 g .. J + 4 g + 3, column J + 4 g + q standing at n = g of n-tile q.
 // Accumulator n of n-tile q is then column J + 4 n + q, so a lane's outputs
 // of a row are the eight consecutive columns J + 8 t4 .. J + 8 t4 + 7.
+// Rounds 0 .. kEarly - 1 were issued before the m x m stage.
 template <typename TY, int MT, int NT, bool HALF>
 __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
                                             const uint32_t (&ph)[MT][MT][4], const uint32_t (&pl)[MT][MT][4],
                                             const float (&rs)[GsLayout<MT, NT, HALF>::R]) {
   using L = GsLayout<MT, NT, HALF>;
-  constexpr int NW = L::NW, S = L::SO, LB = L::LBO, R = L::R, KR = L::KR;
+  using Ring = GsOutRing<MT, NT, HALF>;
+  constexpr int NW = L::NW, S = L::SO, LB = L::LBO, KR = L::KR;
   constexpr uint32_t kSlot = NW * 32 * LB;
   const int lane = c.lane;
   uint8_t* ring_warp = ring + c.warp * 32 * LB;
-  const uint32_t ring0 = smem_u32(ring_warp);
-  const int nsb = c.NB / 2;  // superblocks of this CTA
-  const int rounds = (nsb + NW - 1) / NW;
-  auto krow = [&](int kr) { return (kr >> 2) * 16 + 2 * c.t4 + (kr & 1) + ((kr & 2) ? 8 : 0); };
-  auto orow = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
+  const Ring rg(c, ring);
+  const int nsb = rg.nsb, rounds = rg.rounds;
+  auto krow = [&](int kr) { return Ring::krow(c, kr); };
+  auto orow = [&](int s) { return Ring::orow(c, s); };
   const uint64_t last_use = l2_evict_first();
   const float2 inv2 = make_float2(c.inv, c.inv), decay2 = make_float2(c.decay, c.decay);
-
-  // loop-invariant element offsets of this lane's rows (32 cols < 2^31 on the
-  // vector path); rows >= m read as zero
-  int moff[KR], poff[R];
-  uint32_t mok = 0, pok = 0;
-#pragma unroll
-  for (int kr = 0; kr < KR; ++kr) {
-    moff[kr] = krow(kr) * c.cols;
-    if (krow(kr) < c.m) mok |= 1u << kr;
-  }
-#pragma unroll
-  for (int s = 0; s < R; ++s) {
-    poff[s] = orow(s) * c.cols;
-    if (orow(s) < c.m) pok |= 1u << s;
-  }
-
-  auto issue = [&](int r, uint32_t dst) {
-    const int sb = r * NW + c.warp;
-    if (c.vec && r < rounds && sb < nsb) {
-      const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
-      const bool cm = jm < c.n, cpp = jp < c.n;  // n % 8 == 0: a lane's columns share fate
-#pragma unroll
-      for (int kr = 0; kr < KR; ++kr) {
-        const bool ok = cm && ((mok >> kr) & 1u);
-        cp_async16_hint(dst + kr * 512 + lane * 16, c.Mp + (ok ? moff[kr] + jm : 0), ok ? 16 : 0, last_use);
-      }
-#pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const bool ok = cpp && ((pok >> s) & 1u);
-        cp_async16_hint(dst + (KR + s) * 512 + lane * 16, c.P + (ok ? poff[s] + jp : 0), ok ? 16 : 0,
-                        last_use);
-      }
-    }
-    cp_async_commit();
-  };
+  const int* poff = rg.poff;
 
 #pragma unroll
-  for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
+  for (int r = Ring::kEarly; r < S; ++r) rg.issue(c, r, last_use);
 
   auto process = [&](int r, const uint8_t* st) {
     const int sb = r * NW + c.warp;
@@ -426,12 +462,23 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
 
   for (int r = 0; r < rounds; ++r) {
     cp_async_wait<S - 1>();
-    uint8_t* st = ring_warp + (r % S) * kSlot;
+    uint8_t* st = ring_warp + Ring::slot(r) * kSlot;
     process(r, st);
     // round r now lives in registers / is written: refill its slot
-    issue(r + S, ring0 + (r % S) * kSlot);
+    rg.issue(c, r + S, last_use);
   }
   cp_async_wait<0>();
+}
+
+// The output pass's first rounds, into the slots the m x m stage leaves free.
+template <int MT, int NT, bool HALF>
+__device__ __forceinline__ void gs_out_prefetch(const GsCtx& c, uint8_t* ring) {
+  using Ring = GsOutRing<MT, NT, HALF>;
+  if (Ring::kEarly == 0) return;
+  const Ring rg(c, ring);
+  const uint64_t last_use = l2_evict_first();
+#pragma unroll
+  for (int r = 0; r < Ring::kEarly; ++r) rg.issue(c, r, last_use);
 }
 
 // An m x m fp32 matrix kept as two tf32 parts, x = hi + lo (both exact
@@ -525,10 +572,10 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   // m x m work arrays (aliasing the ring between the two passes)
   float* wpart = reinterpret_cast<float*>(smem);
   float* wss = wpart + NW * GT::N * 128;
-  uint32_t* mmbase = reinterpret_cast<uint32_t*>(smem + L::kWarpPart);
+  uint32_t* mmbase = reinterpret_cast<uint32_t*>(smem);
   auto mat = [&](int k) { return SplitMat{mmbase + (2 * k) * MP * LD, mmbase + (2 * k + 1) * MP * LD}; };
   SplitMat Am = mat(0), Qm = mat(1), Tm = mat(2), Pi0 = mat(3), Pi1 = mat(4);
-  TY* Ph = reinterpret_cast<TY*>(smem + L::kWarpPart + 10 * L::kMat);
+  TY* Ph = reinterpret_cast<TY*>(smem + 10 * L::kMat);
   TY* Pl = Ph + MP * (MP + 8);
   SplitMat Pi = Pi0;
   const int nup = m * (m + 1) / 2;
@@ -553,7 +600,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
       for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * a.cols + c.c0, bytes);
   }
   __syncthreads();  // every warp's ring is drained before it is reused
-  for (int e = tid; e < 10 * MP * LD; e += NT) mmbase[e] = 0u;  // m x m arrays, padding included
+  gs_out_prefetch<MT, NT, HALF>(c, smem);
   // per-warp partials, then warps summed in a fixed order into this CTA's partial
   ss = warp_sum(ss);
   if (lane == 0) wss[warp] = ss;
@@ -578,7 +625,9 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     for (int k = 0; k < NW; ++k) acc += wss[k];
     misc[0] = acc;
   }
-  cluster_sync();
+  cluster_sync();  // (also a CTA barrier: the partials are consumed)
+  for (int e = tid; e < 10 * MP * LD; e += NT) mmbase[e] = 0u;  // m x m arrays, padding included
+  __syncthreads();
   // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: CTAs summed in rank order
   float ssum = 0.f;
 #pragma unroll
@@ -598,10 +647,9 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   cluster_arrive();  // done reading the peer's partials
   __syncthreads();
 
-  // 2. the k steps in m x m space, one m16 x n8 tile per warp (3xTF32)
+  // 2. the k steps in m x m space, m16 x n8 tiles dealt to the warps in turn (3xTF32)
   if (ns > 0) {
     constexpr int TPP = (MP / 16) * (MP / 8);  // tiles of one product
-    static_assert(2 * TPP <= NW, "one tile per warp in the two-product stage");
     const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
     const int ks = (m + 7) / 8;  // live k8 steps
     // a tile wholly beyond m (rows or columns) stays zero and is skipped
@@ -614,13 +662,14 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     for (int s = 0; s < ns; ++s) {
       const bool more = s + 1 < ns;
       // Q = a I + b A + c A^2 (zero outside m x m)
-      if (warp < TPP && live(warp)) {
+      for (int tile = warp; tile < TPP; tile += NW) {
+        if (!live(tile)) continue;
         float d[4];
-        mm_tile<MP, LD>(Am, Am, warp, ks, c.g, c.t4, d);
+        mm_tile<MP, LD>(Am, Am, tile, ks, c.g, c.t4, d);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           int i, j;
-          at(warp, q, i, j);
+          at(tile, q, i, j);
           float v = 0.f;
           if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, get<LD>(Am, i, j), i == j ? ca : 0.f));
           put<LD>(Qm, i, j, v);
@@ -629,19 +678,21 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
       __syncthreads();
       // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
       SplitMat Pn = Pi.hi == Pi0.hi ? Pi1 : Pi0;
-      if (warp < TPP) {
-        if (more && live(warp)) {
+      for (int t = warp; t < 2 * TPP; t += NW) {
+        if (t < TPP) {
+          if (!more || !live(t)) continue;
           float d[4];
-          mm_tile<MP, LD>(Qm, Qm, warp, ks, c.g, c.t4, d);
+          mm_tile<MP, LD>(Qm, Qm, t, ks, c.g, c.t4, d);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int i, j;
-            at(warp, q, i, j);
+            at(t, q, i, j);
             put<LD>(Tm, i, j, d[q]);
           }
+          continue;
         }
-      } else if (warp < 2 * TPP && live(warp - TPP)) {
-        const int tile = warp - TPP;
+        const int tile = t - TPP;
+        if (!live(tile)) continue;
         float d[4];
         if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, ks, c.g, c.t4, d);
 #pragma unroll
@@ -660,13 +711,14 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
       __syncthreads();
       if (more) {
         // A <- Q^2 A (written over Q, then the two swap roles)
-        if (warp < TPP && live(warp)) {
+        for (int tile = warp; tile < TPP; tile += NW) {
+          if (!live(tile)) continue;
           float d[4];
-          mm_tile<MP, LD>(Tm, Am, warp, ks, c.g, c.t4, d);
+          mm_tile<MP, LD>(Tm, Am, tile, ks, c.g, c.t4, d);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int i, j;
-            at(warp, q, i, j);
+            at(tile, q, i, j);
             put<LD>(Qm, i, j, d[q]);
           }
         }
@@ -727,9 +779,14 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   cluster_wait();  // the peer may still read this CTA's partials
 }
 
+// Threads per CTA: 16 warps up to m = 32; beyond, 8 warps, each with the
+// registers for Pi's fragments of all 16-row tiles.
+template <int MT>
+constexpr int gs_threads() { return MT <= 2 ? 512 : 256; }
+
 template <typename TY, int MT, bool HALF>
 cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
-  constexpr int NT = 512;
+  constexpr int NT = gs_threads<MT>();
   auto fn = k_skinny_gs<TY, MT, NT, HALF>;
   constexpr int smem = GsLayout<MT, NT, HALF>::kTotal;
   if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -750,7 +807,7 @@ cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, b
 
 template <typename TY, int MT, bool HALF>
 int gs_clusters_of() {
-  constexpr int NT = 512;
+  constexpr int NT = gs_threads<MT>();
   auto fn = k_skinny_gs<TY, MT, NT, HALF>;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(kCL * 1024);
@@ -767,32 +824,41 @@ int gs_clusters_of() {
   return cudaOccupancyMaxActiveClusters(&n, fn, &lc) == cudaSuccess ? n : -1;
 }
 
+// HALF (a last 16-row tile of at most 8 rows, stored as half a tile) is
+// instantiated up to m = 32; beyond, such a tile is padded to 16 rows.
 template <typename TY>
 cudaError_t gs_launch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
   const bool half = a.m - 16 * (cfg.mtiles - 1) <= 8;
-  if (cfg.mtiles == 1)
-    return half ? launch_gs_t<TY, 1, true>(a, cfg, st, prep) : launch_gs_t<TY, 1, false>(a, cfg, st, prep);
-  return half ? launch_gs_t<TY, 2, true>(a, cfg, st, prep) : launch_gs_t<TY, 2, false>(a, cfg, st, prep);
+  switch (cfg.mtiles) {
+    case 1: return half ? launch_gs_t<TY, 1, true>(a, cfg, st, prep) : launch_gs_t<TY, 1, false>(a, cfg, st, prep);
+    case 2: return half ? launch_gs_t<TY, 2, true>(a, cfg, st, prep) : launch_gs_t<TY, 2, false>(a, cfg, st, prep);
+    case 3: return launch_gs_t<TY, 3, false>(a, cfg, st, prep);
+    default: return launch_gs_t<TY, 4, false>(a, cfg, st, prep);
+  }
 }
 
 template <typename TY>
 int gs_clusters_ty(int m) {
   const int mt = (m + 15) / 16;
   const bool half = m - 16 * (mt - 1) <= 8;
-  if (mt == 1) return half ? gs_clusters_of<TY, 1, true>() : gs_clusters_of<TY, 1, false>();
-  return half ? gs_clusters_of<TY, 2, true>() : gs_clusters_of<TY, 2, false>();
+  switch (mt) {
+    case 1: return half ? gs_clusters_of<TY, 1, true>() : gs_clusters_of<TY, 1, false>();
+    case 2: return half ? gs_clusters_of<TY, 2, true>() : gs_clusters_of<TY, 2, false>();
+    case 3: return gs_clusters_of<TY, 3, false>();
+    default: return gs_clusters_of<TY, 4, false>();
+  }
 }
 
 }  // namespace
 
 cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare) {
-  if (a.mode_f32 || cfg.mtiles > 2) return cudaErrorInvalidValue;
+  if (a.mode_f32 || cfg.mtiles < 1 || cfg.mtiles > 4) return cudaErrorInvalidValue;
   return a.ns_type == NS_F16 ? gs_launch_ty<__half>(a, cfg, s, prepare)
                              : gs_launch_ty<__nv_bfloat16>(a, cfg, s, prepare);
 }
 
 int gs_max_active_clusters(int ns_type, int m) {
-  if (m < 1 || m > 32) return -1;
+  if (m < 1 || m > 64) return -1;
   return ns_type == NS_F16 ? gs_clusters_ty<__half>(m) : gs_clusters_ty<__nv_bfloat16>(m);
 }
 

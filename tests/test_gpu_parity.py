@@ -42,6 +42,9 @@ SKINNY_SHAPES = [
     [[8, 4096], [16, 4096]],     # one m16 tile (half / full)
     [[25, 1000]],                # m = 25, ragged 32-column superblock
     [[24, 1004]],                # cols % 8 != 0: scalar access path
+    [[56, 3000]],                # m = 56: last m16 tile padded, ragged superblock
+    [[2048, 36], [7168, 64]],    # transposed, three and four m16 tiles
+    [[4, 64, 1504]],             # 3-D, m = 64
 ]
 
 
@@ -101,26 +104,27 @@ def test_zero_gradient_and_momentum():
     run.close()
 
 
-@pytest.mark.parametrize("k", [10, 64])
-def test_gram_space_zero_rows(k):
+@pytest.mark.parametrize("k,rows", [(10, 24), (64, 24), (64, 64)])
+def test_gram_space_zero_rows(k, rows):
     """Zero rows of M' are exact null directions of X_0, along which the
     Gram-space product Pi_k = Q_{k-1} ... Q_0 grows like a^k: O keeps them
     exactly zero and the other rows match the oracle."""
-    w = W.custom([[24, 4096]], seed=21, ns_steps=k)
+    w = W.custom([[rows, 4096]], seed=21, ns_steps=k)
     P, G, M = W.make_tensors(w, "cuda")
-    for r in (3, 20):
+    zero = (3, 20, rows - 1)
+    for r in zero:
         G[0][r] = 0
         M[0][r] = 0
     run = GpuRun(w, tensors=(P, G, M))
     check_all(run)
     O = run.O(0)
-    assert np.all(np.isfinite(O)) and np.all(O[[3, 20]] == 0)
+    assert np.all(np.isfinite(O)) and np.all(O[list(zero)] == 0)
     run.close()
 
 
 def test_many_steps_direct_iteration():
     """Step counts beyond the Gram-space range run the direct iteration."""
-    w = W.custom([[24, 2048], [2, 16, 512]], seed=22, ns_steps=70)
+    w = W.custom([[24, 2048], [2, 16, 512], [64, 1024], [40, 512]], seed=22, ns_steps=70)
     run = GpuRun(w)
     check_all(run)
     run.close()
@@ -146,6 +150,20 @@ def test_batch_invariance_bitwise():
             assert np.array_equal(run.m1(j), full.m1(i))
             assert np.array_equal(run.O(j), full.O(i))
         run.close()
+    full.close()
+
+
+def test_batch_invariance_bitwise_m64():
+    """The same for four 16-row tiles (m = 64): a member alone equals the
+    member inside a batch of 9."""
+    w = W.custom([[64, 7168]] * 9, seed=23)
+    full = GpuRun(w)
+    sub = W.custom([w.shapes[6]], seed=0)
+    run = GpuRun(sub, tensors=_member_tensors(w, [6]))
+    assert np.array_equal(run.p1(0), full.p1(6))
+    assert np.array_equal(run.m1(0), full.m1(6))
+    assert np.array_equal(run.O(0), full.O(6))
+    run.close()
     full.close()
 
 
