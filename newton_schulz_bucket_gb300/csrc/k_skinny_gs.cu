@@ -1,4 +1,4 @@
-// Skinny path for m = min(rows, cols) <= 32: the whole Muon step of a member
+// Skinny path for m = min(rows, cols) <= 64: the whole Muon step of a member
 // in one kernel, with Newton-Schulz evaluated in Gram space.
 //
 // «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: for
@@ -14,7 +14,9 @@
 //      (tf32 tensor-core products, fp32 accumulation: the norm is not known
 //      yet, and tf32 keeps fp32's range with an 11-bit significand);
 //   2. in m x m space, fp32: A_0 = M' M'^T / (||M'||_F + eps)^2, then per step
-//      Q = a I + b A + c A^2, Pi <- Q Pi, A <- Q A Q;
+//      Q = a I + b A + c A^2, Pi <- Q Pi, A <- Q A Q (3xTF32 tensor-core
+//      tiles up to m = 32, where the stage is latency-bound; fp32 FFMA
+//      above, where it is throughput-bound);
 //   3. output pass: Y_0 = alpha M' / (||M'||_F + eps) in the operand type,
 //      O = Pi_k Y_0 / alpha with Pi_k split into an operand-type high part and
 //      a residual low part, and P' = P (1 - lr wd) - lr s O.
@@ -28,12 +30,13 @@
 // (rows, cols), so a member gives the same bits in any batch.
 //
 // Layout: one cluster of kCL CTAs per member; CTA r owns the wide iterate's
-// columns [r W, (r + 1) W).  The momentum pass walks 16-column blocks (block
-// blk by warp blk % NW): lane (g, t4) holds rows 16 mi + g (+ 8) and the four
-// consecutive columns 4 t4 .. 4 t4 + 3, which stand in the tf32 A-fragment
-// slots (t4, t4 + 4) of the block's two k8 steps.  The output pass walks
-// 32-column superblocks and loads Y_0 straight into B fragments (see
-// gs_out_pass).  The Gram sums over all columns and Pi X acts on each column
+// columns [r W, (r + 1) W), 16 warps up to m = 32 and 8 beyond (each lane
+// then keeps Pi's fragments for four 16-row tiles, 128 registers).  Both
+// passes walk 32-column superblocks (superblock sb by warp sb % NW).  In the
+// momentum pass lane (g, t4) holds rows 16 mi + g (+ 8) and the eight
+// consecutive columns 8 t4 .. 8 t4 + 7, which stand in tf32 A-fragment slots
+// (see gs_momentum_pass); the output pass loads Y_0 straight into B
+// fragments (see gs_out_pass).  The Gram sums over all columns and Pi X acts on each column
 // alone, so these fixed permutations of a block's columns change nothing, and
 // they turn every access into a 16-byte (fp32) or 8/16-byte (bf16) vector.
 // Operands stream through a per-lane cp.async ring.
@@ -70,13 +73,14 @@ struct GsLayout {
   static constexpr int SO = 4 * NW * 32 * LBO <= kCap ? 4 : (3 * NW * 32 * LBO <= kCap ? 3 : 2);
   static constexpr int kRingO = SO * NW * 32 * LBO;
   // between the passes the ring holds the per-warp Gram partials and sums of
-  // squares, then the m x m work arrays: A, Q, T, Pi (two), each stored as
-  // a tf32 high part and a tf32 residual, and Pi's operand-type high / low
-  // parts
+  // squares, then the m x m work arrays: A, Q, T, Pi (two) -- for m <= 32
+  // each stored as a tf32 high part and a tf32 residual, else in fp32 -- and
+  // Pi's operand-type high / low parts
   static constexpr int kWarpPart = NW * GT::N * 128 * 4 + NW * 4 * 4;
   static constexpr int kMat = MP * LD * 4;
   static constexpr int kPiT = MP * (MP + 8) * 2;
-  static constexpr int kMM = 10 * kMat + 2 * kPiT;  // A, Q, T, Pi x2, each as tf32 high + low
+  static constexpr bool TC = MT <= 2;  // m x m products on the tensor cores (else FFMA)
+  static constexpr int kMM = (TC ? 10 : 5) * kMat + 2 * kPiT;  // A, Q, T, Pi x2, then Pi high / low
   // the rings, the per-warp partials and the m x m arrays are live one after
   // the other and share the same bytes
   static constexpr int kU0 = kRing1 > kRingO ? kRing1 : kRingO;
@@ -266,19 +270,13 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   ss += ss2.x + ss2.y;
 }
 
-// The output pass's ring and its copies.  Between the passes the m x m
-// stage uses the ring's first kBusy slots; the other kEarly slots take the
-// output pass's first rounds before that stage starts, so that its loads
-// overlap the latency-bound m x m work.  Round r lives in slot slot(r).
+// The output pass's ring and its copies: round r lives in slot r % S.
 template <int MT, int NT, bool HALF>
 struct GsOutRing {
   using L = GsLayout<MT, NT, HALF>;
   static constexpr int NW = L::NW, S = L::SO, LB = L::LBO, R = L::R, KR = L::KR;
   static constexpr uint32_t kSlot = NW * 32 * LB;
-  static constexpr int kLive = L::kWarpPart > L::kMM ? L::kWarpPart : L::kMM;
-  static constexpr int kBusy = (kLive + (int)kSlot - 1) / (int)kSlot;
-  static constexpr int kEarly = S > kBusy ? S - kBusy : 0;
-  static __device__ __forceinline__ int slot(int r) { return (r + kBusy) % S; }
+  static __device__ __forceinline__ int slot(int r) { return r % S; }
 
   // loop-invariant element offsets of this lane's rows (32 cols < 2^31 on the
   // vector path); rows >= m read as zero
@@ -338,7 +336,6 @@ struct GsOutRing {
 // J + 4 g .. J + 4 g + 3, column J + 4 g + q standing at n = g of n-tile q.
 // Accumulator n of n-tile q is then column J + 4 n + q, so a lane's outputs
 // of a row are the eight consecutive columns J + 8 t4 .. J + 8 t4 + 7.
-// Rounds 0 .. kEarly - 1 were issued before the m x m stage.
 template <typename TY, int MT, int NT, bool HALF>
 __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
                                             const uint32_t (&ph)[MT][MT][4], const uint32_t (&pl)[MT][MT][4],
@@ -358,7 +355,7 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   const int* poff = rg.poff;
 
 #pragma unroll
-  for (int r = Ring::kEarly; r < S; ++r) rg.issue(c, r, last_use);
+  for (int r = 0; r < S; ++r) rg.issue(c, r, last_use);
 
   auto process = [&](int r, const uint8_t* st) {
     const int sb = r * NW + c.warp;
@@ -470,17 +467,6 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   cp_async_wait<0>();
 }
 
-// The output pass's first rounds, into the slots the m x m stage leaves free.
-template <int MT, int NT, bool HALF>
-__device__ __forceinline__ void gs_out_prefetch(const GsCtx& c, uint8_t* ring) {
-  using Ring = GsOutRing<MT, NT, HALF>;
-  if (Ring::kEarly == 0) return;
-  const Ring rg(c, ring);
-  const uint64_t last_use = l2_evict_first();
-#pragma unroll
-  for (int r = 0; r < Ring::kEarly; ++r) rg.issue(c, r, last_use);
-}
-
 // An m x m fp32 matrix kept as two tf32 parts, x = hi + lo (both exact
 // tf32 values, pitch LD), so that the tensor-core products below read their
 // operands already split.
@@ -534,6 +520,90 @@ __device__ __forceinline__ void mm_tile(const SplitMat& X, const SplitMat& Y, in
   }
 }
 
+// The m x m stage in plain fp32 (FFMA), for m > 32.  Every left operand there (A, Q and
+// Q^2) is symmetric, so C = X Y is formed as C[i][j] = sum_k X[k][i] Y[k][j]:
+// both operands read by rows, k ascending, one fixed order per element.
+// Thread t < 256 owns the RI x CJ block at rows RI (t / BJ) + r, columns
+// CJ (t % BJ) + c.
+template <int MP, int NT>
+struct MmBlk {
+  static constexpr int RI = MP / 16, CJ = RI;
+  static constexpr int BI = MP / RI, BJ = MP / CJ;
+  static_assert(BI * BJ <= NT, "one block per thread");
+};
+
+template <int N>
+__device__ __forceinline__ void lds_run(const float* p, float (&v)[N]) {
+  if constexpr (N == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else if constexpr (N == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = p[e];
+  }
+}
+
+// acc[y] = this thread's block of X^T Y_y over k < m, for NY right operands
+// sharing the left one.
+template <int LD, int RI, int CJ, int NY>
+__device__ __forceinline__ void mm_blk(const float* X, const float* const (&Y)[NY], int m, int i0, int j0,
+                                       float (&acc)[NY][RI][CJ]) {
+#pragma unroll
+  for (int y = 0; y < NY; ++y)
+#pragma unroll
+    for (int r = 0; r < RI; ++r)
+#pragma unroll
+      for (int c = 0; c < CJ; ++c) acc[y][r][c] = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < m; ++k) {
+    float x[RI];
+    lds_run<RI>(X + k * LD + i0, x);
+#pragma unroll
+    for (int y = 0; y < NY; ++y) {
+      float v[CJ];
+      lds_run<CJ>(Y[y] + k * LD + j0, v);
+#pragma unroll
+      for (int r = 0; r < RI; ++r) {
+        if constexpr (CJ % 2 == 0) {
+#pragma unroll
+          for (int c = 0; c < CJ; c += 2) {
+            const float2 t = __ffma2_rn(make_float2(x[r], x[r]), make_float2(v[c], v[c + 1]),
+                                        make_float2(acc[y][r][c], acc[y][r][c + 1]));
+            acc[y][r][c] = t.x;
+            acc[y][r][c + 1] = t.y;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < CJ; ++c) acc[y][r][c] = fmaf(x[r], v[c], acc[y][r][c]);
+        }
+      }
+    }
+  }
+}
+
+// The m x m work arrays A, Q, T, Pi (two): matrix k at base, either split
+// into tf32 high / low parts (tensor-core form, m <= 32) or plain fp32.
+template <int MP, int LD, bool TC>
+struct MmMats {
+  uint32_t* base;
+  static constexpr int kWords = (TC ? 10 : 5) * MP * LD;
+  __device__ __forceinline__ SplitMat split(int k) const {
+    return SplitMat{base + (2 * k) * MP * LD, base + (2 * k + 1) * MP * LD};
+  }
+  __device__ __forceinline__ float* plain(int k) const { return reinterpret_cast<float*>(base) + k * MP * LD; }
+  __device__ __forceinline__ float get(int k, int i, int j) const {
+    if constexpr (TC) return ::muon::get<LD>(split(k), i, j);
+    else return plain(k)[i * LD + j];
+  }
+  __device__ __forceinline__ void put(int k, int i, int j, float v) const {
+    if constexpr (TC) ::muon::put<LD>(split(k), i, j, v);
+    else plain(k)[i * LD + j] = v;
+  }
+};
+
 template <typename TY, int MT, int NT, bool HALF>
 __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   using L = GsLayout<MT, NT, HALF>;
@@ -572,12 +642,11 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   // m x m work arrays (aliasing the ring between the two passes)
   float* wpart = reinterpret_cast<float*>(smem);
   float* wss = wpart + NW * GT::N * 128;
-  uint32_t* mmbase = reinterpret_cast<uint32_t*>(smem);
-  auto mat = [&](int k) { return SplitMat{mmbase + (2 * k) * MP * LD, mmbase + (2 * k + 1) * MP * LD}; };
-  SplitMat Am = mat(0), Qm = mat(1), Tm = mat(2), Pi0 = mat(3), Pi1 = mat(4);
-  TY* Ph = reinterpret_cast<TY*>(smem + 10 * L::kMat);
+  using Mats = MmMats<MP, LD, L::TC>;
+  const Mats mats{reinterpret_cast<uint32_t*>(smem)};
+  TY* Ph = reinterpret_cast<TY*>(smem + Mats::kWords * 4);
   TY* Pl = Ph + MP * (MP + 8);
-  SplitMat Pi = Pi0;
+  int ip = 3;  // matrix index of the final Pi (3 or 4)
   const int nup = m * (m + 1) / 2;
   for (int e = tid; e < nup; e += NT) {
     // e -> (i, j), i <= j, row-major over the upper triangle
@@ -600,7 +669,6 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
       for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * a.cols + c.c0, bytes);
   }
   __syncthreads();  // every warp's ring is drained before it is reused
-  gs_out_prefetch<MT, NT, HALF>(c, smem);
   // per-warp partials, then warps summed in a fixed order into this CTA's partial
   ss = warp_sum(ss);
   if (lane == 0) wss[warp] = ss;
@@ -626,7 +694,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     misc[0] = acc;
   }
   cluster_sync();  // (also a CTA barrier: the partials are consumed)
-  for (int e = tid; e < 10 * MP * LD; e += NT) mmbase[e] = 0u;  // m x m arrays, padding included
+  for (int e = tid; e < Mats::kWords; e += NT) mats.base[e] = 0u;  // m x m arrays, padding included
   __syncthreads();
   // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: CTAs summed in rank order
   float ssum = 0.f;
@@ -641,97 +709,176 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 #pragma unroll
     for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
     acc *= inv2;
-    put<LD>(Am, i, j, acc);
-    put<LD>(Am, j, i, acc);
+    mats.put(0, i, j, acc);
+    mats.put(0, j, i, acc);
   }
   cluster_arrive();  // done reading the peer's partials
   __syncthreads();
 
-  // 2. the k steps in m x m space, m16 x n8 tiles dealt to the warps in turn (3xTF32)
+  // 2. the k steps in m x m space: for m <= 32 m16 x n8 tiles dealt to the
+  // warps on the tensor cores (3xTF32; the stage is latency-bound there),
+  // else fp32 FFMA blocks, one per thread (throughput-bound)
   if (ns > 0) {
-    constexpr int TPP = (MP / 16) * (MP / 8);  // tiles of one product
-    const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
-    const int ks = (m + 7) / 8;  // live k8 steps
-    // a tile wholly beyond m (rows or columns) stays zero and is skipped
-    auto live = [&](int tile) { return (tile / (MP / 8)) * 16 < m && (tile % (MP / 8)) * 8 < m; };
-    // element (i, j) of this lane's accumulator slot q in tile `tile`
-    auto at = [&](int tile, int q, int& i, int& j) {
-      i = (tile / (MP / 8)) * 16 + c.g + ((q & 2) ? 8 : 0);
-      j = (tile % (MP / 8)) * 8 + 2 * c.t4 + (q & 1);
-    };
-    for (int s = 0; s < ns; ++s) {
-      const bool more = s + 1 < ns;
-      // Q = a I + b A + c A^2 (zero outside m x m)
-      for (int tile = warp; tile < TPP; tile += NW) {
-        if (!live(tile)) continue;
-        float d[4];
-        mm_tile<MP, LD>(Am, Am, tile, ks, c.g, c.t4, d);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          int i, j;
-          at(tile, q, i, j);
-          float v = 0.f;
-          if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, get<LD>(Am, i, j), i == j ? ca : 0.f));
-          put<LD>(Qm, i, j, v);
-        }
-      }
-      __syncthreads();
-      // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
-      SplitMat Pn = Pi.hi == Pi0.hi ? Pi1 : Pi0;
-      for (int t = warp; t < 2 * TPP; t += NW) {
-        if (t < TPP) {
-          if (!more || !live(t)) continue;
-          float d[4];
-          mm_tile<MP, LD>(Qm, Qm, t, ks, c.g, c.t4, d);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            int i, j;
-            at(t, q, i, j);
-            put<LD>(Tm, i, j, d[q]);
-          }
-          continue;
-        }
-        const int tile = t - TPP;
-        if (!live(tile)) continue;
-        float d[4];
-        if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, ks, c.g, c.t4, d);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          int i, j;
-          at(tile, q, i, j);
-          if (s > 0) {
-            put<LD>(Pn, i, j, d[q]);
-          } else {
-            Pn.hi[i * LD + j] = Qm.hi[i * LD + j];
-            Pn.lo[i * LD + j] = Qm.lo[i * LD + j];
-          }
-        }
-      }
-      Pi = Pn;
-      __syncthreads();
-      if (more) {
-        // A <- Q^2 A (written over Q, then the two swap roles)
+    if constexpr (L::TC) {
+      constexpr int TPP = (MP / 16) * (MP / 8);  // tiles of one product
+      SplitMat Am = mats.split(0), Qm = mats.split(1), Tm = mats.split(2), Pi0 = mats.split(3);
+      SplitMat Pi1 = mats.split(4), Pi = Pi0;
+      const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
+      const int ks = (m + 7) / 8;  // live k8 steps
+      // a tile wholly beyond m (rows or columns) stays zero and is skipped
+      auto live = [&](int tile) { return (tile / (MP / 8)) * 16 < m && (tile % (MP / 8)) * 8 < m; };
+      // element (i, j) of this lane's accumulator slot q in tile `tile`
+      auto at = [&](int tile, int q, int& i, int& j) {
+        i = (tile / (MP / 8)) * 16 + c.g + ((q & 2) ? 8 : 0);
+        j = (tile % (MP / 8)) * 8 + 2 * c.t4 + (q & 1);
+      };
+      for (int s = 0; s < ns; ++s) {
+        const bool more = s + 1 < ns;
+        // Q = a I + b A + c A^2 (zero outside m x m)
         for (int tile = warp; tile < TPP; tile += NW) {
           if (!live(tile)) continue;
           float d[4];
-          mm_tile<MP, LD>(Tm, Am, tile, ks, c.g, c.t4, d);
+          mm_tile<MP, LD>(Am, Am, tile, ks, c.g, c.t4, d);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             int i, j;
             at(tile, q, i, j);
-            put<LD>(Qm, i, j, d[q]);
+            float v = 0.f;
+            if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, get<LD>(Am, i, j), i == j ? ca : 0.f));
+            put<LD>(Qm, i, j, v);
           }
         }
-        const SplitMat t = Am; Am = Qm; Qm = t;
         __syncthreads();
+        // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
+        SplitMat Pn = Pi.hi == Pi0.hi ? Pi1 : Pi0;
+        for (int t = warp; t < 2 * TPP; t += NW) {
+          if (t < TPP) {
+            if (!more || !live(t)) continue;
+            float d[4];
+            mm_tile<MP, LD>(Qm, Qm, t, ks, c.g, c.t4, d);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              int i, j;
+              at(t, q, i, j);
+              put<LD>(Tm, i, j, d[q]);
+            }
+            continue;
+          }
+          const int tile = t - TPP;
+          if (!live(tile)) continue;
+          float d[4];
+          if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, ks, c.g, c.t4, d);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            int i, j;
+            at(tile, q, i, j);
+            if (s > 0) {
+              put<LD>(Pn, i, j, d[q]);
+            } else {
+              Pn.hi[i * LD + j] = Qm.hi[i * LD + j];
+              Pn.lo[i * LD + j] = Qm.lo[i * LD + j];
+            }
+          }
+        }
+        Pi = Pn;
+        __syncthreads();
+        if (more) {
+          // A <- Q^2 A (written over Q, then the two swap roles)
+          for (int tile = warp; tile < TPP; tile += NW) {
+            if (!live(tile)) continue;
+            float d[4];
+            mm_tile<MP, LD>(Tm, Am, tile, ks, c.g, c.t4, d);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              int i, j;
+              at(tile, q, i, j);
+              put<LD>(Qm, i, j, d[q]);
+            }
+          }
+          const SplitMat t = Am; Am = Qm; Qm = t;
+          __syncthreads();
+        }
       }
+      ip = Pi.hi == Pi0.hi ? 3 : 4;
+    } else {
+      using B = MmBlk<MP, NT>;
+      constexpr int RI = B::RI, CJ = B::CJ;
+      const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
+      const int i0 = RI * (tid / B::BJ), j0 = CJ * (tid % B::BJ);
+      const bool own = tid < B::BI * B::BJ;
+      // this thread's block into C, zero outside m x m
+      auto store = [&](float* C, const float (&v)[RI][CJ]) {
+#pragma unroll
+        for (int r = 0; r < RI; ++r)
+#pragma unroll
+          for (int q = 0; q < CJ; ++q) {
+            const int i = i0 + r, j = j0 + q;
+            C[i * LD + j] = (i < m && j < m) ? v[r][q] : 0.f;
+          }
+      };
+      float *Am = mats.plain(0), *Qm = mats.plain(1), *Tm = mats.plain(2);
+      float *Pi0 = mats.plain(3), *Pi1 = mats.plain(4), *Pi = Pi0;
+      for (int s = 0; s < ns; ++s) {
+        const bool more = s + 1 < ns;
+        // Q = a I + b A + c A^2
+        if (own) {
+          float acc[1][RI][CJ];
+          mm_blk<LD, RI, CJ, 1>(Am, {Am}, m, i0, j0, acc);
+#pragma unroll
+          for (int r = 0; r < RI; ++r)
+#pragma unroll
+            for (int q = 0; q < CJ; ++q) {
+              const int i = i0 + r, j = j0 + q;
+              acc[0][r][q] = fmaf(cc, acc[0][r][q], fmaf(cb, Am[i * LD + j], i == j ? ca : 0.f));
+            }
+          store(Qm, acc[0]);
+        }
+        __syncthreads();
+        // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
+        float* Pn = Pi == Pi0 ? Pi1 : Pi0;
+        if (own) {
+          if (s > 0 && more) {
+            float acc[2][RI][CJ];
+            mm_blk<LD, RI, CJ, 2>(Qm, {Qm, Pi}, m, i0, j0, acc);
+            store(Tm, acc[0]);
+            store(Pn, acc[1]);
+          } else if (s > 0) {
+            float acc[1][RI][CJ];
+            mm_blk<LD, RI, CJ, 1>(Qm, {Pi}, m, i0, j0, acc);
+            store(Pn, acc[0]);
+          } else {
+            if (more) {
+              float acc[1][RI][CJ];
+              mm_blk<LD, RI, CJ, 1>(Qm, {Qm}, m, i0, j0, acc);
+              store(Tm, acc[0]);
+            }
+#pragma unroll
+            for (int r = 0; r < RI; ++r)
+#pragma unroll
+              for (int q = 0; q < CJ; ++q) Pn[(i0 + r) * LD + j0 + q] = Qm[(i0 + r) * LD + j0 + q];
+          }
+        }
+        Pi = Pn;
+        __syncthreads();
+        if (more) {
+          // A <- Q^2 A (written over Q, then the two swap roles)
+          if (own) {
+            float acc[1][RI][CJ];
+            mm_blk<LD, RI, CJ, 1>(Tm, {Am}, m, i0, j0, acc);
+            store(Qm, acc[0]);
+          }
+          float* t = Am; Am = Qm; Qm = t;
+          __syncthreads();
+        }
+      }
+      ip = Pi == Pi0 ? 3 : 4;
     }
     // Along an exact null direction of X_0 (a zero row, say) Pi grows like
     // a^k while O does not: scale each row i of Pi by 2^-e_i into the operand
     // type's range, and O's row i by 2^e_i in the epilogue.
     for (int i = warp; i < MP; i += NW) {  // one warp per row: lanes over columns
       float mx = 0.f;
-      for (int k = lane; k < m && i < m; k += 32) mx = fmaxf(mx, fabsf(get<LD>(Pi, i, k)));
+      for (int k = lane; k < m && i < m; k += 32) mx = fmaxf(mx, fabsf(mats.get(ip, i, k)));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const int ex = mx >= 32768.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
@@ -742,7 +889,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     for (int e = tid; e < MP * MP; e += NT) {
       const int i = e / MP, j = e - (e / MP) * MP;
       float v = 0.f;
-      if (i < m && j < m) v = get<LD>(Pi, i, j) / rsc[i];
+      if (i < m && j < m) v = mats.get(ip, i, j) / rsc[i];
       const TY hi = from_f32<TY>(v);
       Ph[i * (MP + 8) + j] = hi;
       Pl[i * (MP + 8) + j] = from_f32<TY>(v - to_f32(hi));
