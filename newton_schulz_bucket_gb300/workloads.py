@@ -68,7 +68,8 @@ def _log_uniform(g: torch.Generator, lo: float, hi: float, n: int) -> List[float
 def get(name: str, ns_steps: Optional[int] = None) -> Workload:
     """The named workload.  Names: 'c1_fp32_64x128', 'c2_skinny_74x24x10240',
     'c3_moe_64x2048x7168_32x24x10240', 'c4_dense_h4096', 'c5_mixed_1000',
-    plus small parity cases built by ``custom``."""
+    'c5_group_<rows>x<cols>' (one shape group of the mixed bag), plus small
+    parity cases built by ``custom``."""
     beta, lr = 0.95, 0.02
     if name == "c1_fp32_64x128":
         w = Workload(name, [[64, 128]], "fp32", beta, lr, 0.0, 5,
@@ -96,6 +97,17 @@ def get(name: str, ns_steps: Optional[int] = None) -> Workload:
         w = Workload(name, shapes, "bf16", beta, lr, 0.1, 5,
                      p_std=[0.02] * len(shapes), g_std=_log_uniform(g, 1e-5, 1e-2, len(shapes)),
                      seed=5, describe="1000 matrices over 12 shapes, per-matrix std log-uniform [1e-5,1e-2]")
+    elif name.startswith("c5_group_"):
+        # one shape group of the mixed bag alone (its count and value law),
+        # for per-group profiling: e.g. 'c5_group_64x7168'
+        shape = [int(x) for x in name[len("c5_group_"):].split("x")]
+        if shape not in C5_SHAPES:
+            raise KeyError(name)
+        full = get("c5_mixed_1000")
+        idx = [i for i, s in enumerate(full.shapes) if s == shape]
+        w = Workload(name, [shape] * len(idx), "bf16", beta, lr, 0.1, 5,
+                     p_std=[full.p_std[i] for i in idx], g_std=[full.g_std[i] for i in idx], seed=5,
+                     describe=f"the {shape} group of the mixed bag ({len(idx)} matrices)")
     else:
         raise KeyError(name)
     if ns_steps is not None:
