@@ -36,8 +36,10 @@ from .muon_ref import (  # noqa: F401
     momentum,
     muon_step_ref,
     muon_update_ref,
+    nesterov_input,
     newton_schulz,
     ns_polynomial,
     orthogonalize,
     scale_factor,
+    step_coefficients,
 )

@@ -32,6 +32,32 @@ def momentum(M: np.ndarray, G: np.ndarray, beta: float) -> np.ndarray:
     return float(beta) * np.asarray(M, np.float64) + np.asarray(G, np.float64)
 
 
+def nesterov_input(Mp: np.ndarray, G: np.ndarray, beta: float) -> np.ndarray:
+    """U = G + beta * M', the Nesterov look-ahead of the momentum M'.
+
+    The pages name no Nesterov variant; this is the reading taken for the
+    option, the form that goes with undamped momentum M' = beta M + G: the
+    gradient plus beta times the new momentum is orthogonalised instead of
+    M' itself (M' is still the stored momentum).
+    """
+    return np.asarray(G, np.float64) + float(beta) * np.asarray(Mp, np.float64)
+
+
+def step_coefficients(k: int, a: float, b: float, c: float, schedule=None):
+    """The (a_s, b_s, c_s) of steps s = 0 .. k-1.
+
+    With no schedule every step takes (a, b, c).  A schedule is a list of
+    rows (a_s, b_s, c_s); past its last row the last row repeats (reading:
+    the pages list 5-10 steps and give no per-step values).
+    """
+    if schedule is None:
+        return [(float(a), float(b), float(c))] * int(k)
+    rows = [tuple(float(v) for v in r) for r in schedule]
+    if not rows or any(len(r) != 3 for r in rows):
+        raise ValueError("a schedule is a non-empty list of (a, b, c) rows")
+    return [rows[min(s, len(rows) - 1)] for s in range(int(k))]
+
+
 def frobenius_normalize(M: np.ndarray, eps: float) -> np.ndarray:
     """X0 = M / (||M||_F + eps).
 
@@ -51,21 +77,24 @@ def ns_polynomial(sigma, a: float, b: float, c: float):
     return a * s + b * s ** 3 + c * s ** 5
 
 
-def newton_schulz(X: np.ndarray, k: int, a: float, b: float, c: float) -> np.ndarray:
+def newton_schulz(X: np.ndarray, k: int, a: float, b: float, c: float,
+                  schedule=None) -> np.ndarray:
     """k quintic Newton-Schulz steps on a wide matrix X (rows <= cols).
 
     Each step forms the Gram matrix A = X X^T and then X <- aX + (bA + cA A)X
     («关于分布式Muon的想法整合及讨论» §2: the structure is a Gram matrix and a
     series of matrix products; §6: A changes with X every round, so it is
     recomputed each step).  «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能
-    跃升», 三大性能挑战: typically 5-10 iterations.
+    跃升», 三大性能挑战: typically 5-10 iterations.  Step s takes the
+    coefficients step_coefficients(k, a, b, c, schedule)[s].
     """
     X = np.array(X, dtype=np.float64, copy=True)
     if X.ndim != 2:
         raise ValueError("newton_schulz acts on one matrix")
     if X.shape[0] > X.shape[1]:
         raise ValueError("newton_schulz expects rows <= cols; use orthogonalize")
-    for _ in range(int(k)):
+    coeffs = step_coefficients(k, a, b, c, schedule)
+    for a, b, c in coeffs:
         A = X @ X.T
         B = b * A + c * (A @ A)
         X = a * X + B @ X
@@ -73,7 +102,7 @@ def newton_schulz(X: np.ndarray, k: int, a: float, b: float, c: float) -> np.nda
 
 
 def orthogonalize(Mp: np.ndarray, k: int, a: float, b: float, c: float,
-                  eps: float) -> np.ndarray:
+                  eps: float, schedule=None) -> np.ndarray:
     """O = NS_k(M' / (||M'||_F + eps)), iterating on the wide orientation.
 
     When rows > cols the normalised matrix is transposed before the iteration
@@ -85,7 +114,7 @@ def orthogonalize(Mp: np.ndarray, k: int, a: float, b: float, c: float,
     transposed = X.shape[0] > X.shape[1]
     if transposed:
         X = X.T
-    X = newton_schulz(X, k, a, b, c)
+    X = newton_schulz(X, k, a, b, c, schedule)
     return X.T if transposed else X
 
 
@@ -106,12 +135,13 @@ def scale_factor(rows: int, cols: int, mode: str = "sqrt_aspect") -> float:
 
 
 def muon_update_ref(P, G, M, beta, lr, wd, k, a, b, c, eps=1e-7,
-                    scale_mode="sqrt_aspect"):
+                    scale_mode="sqrt_aspect", nesterov=False, schedule=None):
     """One Muon update of one matrix, in float64.
 
     Returns (P', M', O) with
       M' = beta M + G
-      O  = orthogonalize(M', k, a, b, c, eps)
+      U  = G + beta M' with nesterov, else M'
+      O  = orthogonalize(U, k, a, b, c, eps, schedule)
       P' = P (1 - lr wd) - lr s(rows, cols) O
     The decoupled, multiplicative weight decay and the scale are readings (the
     pages describe only momentum -> orthogonalised update direction).
@@ -120,7 +150,8 @@ def muon_update_ref(P, G, M, beta, lr, wd, k, a, b, c, eps=1e-7,
     if P.ndim != 2:
         raise ValueError("muon_update_ref acts on one matrix")
     Mp = momentum(M, G, beta)
-    O = orthogonalize(Mp, k, a, b, c, eps)
+    U = nesterov_input(Mp, G, beta) if nesterov else Mp
+    O = orthogonalize(U, k, a, b, c, eps, schedule)
     s = scale_factor(P.shape[0], P.shape[1], scale_mode)
     Pn = P * (1.0 - float(lr) * float(wd)) - float(lr) * s * O
     return Pn, Mp, O
@@ -160,7 +191,7 @@ def bucket_shapes(shapes: Sequence[Sequence[int]]) -> List[Dict]:
 
 
 def muon_step_ref(params, grads, momenta, beta, lr, wd, k, a, b, c,
-                  eps=1e-7, scale_mode="sqrt_aspect"):
+                  eps=1e-7, scale_mode="sqrt_aspect", nesterov=False, schedule=None):
     """Muon update of a list of 2-D / 3-D parameters, matrix by matrix.
 
     Bucketing changes nothing mathematically (each member is independent), so
@@ -171,11 +202,11 @@ def muon_step_ref(params, grads, momenta, beta, lr, wd, k, a, b, c,
     for P, G, M in zip(params, grads, momenta):
         P = np.asarray(P, np.float64)
         if P.ndim == 2:
-            r = muon_update_ref(P, G, M, beta, lr, wd, k, a, b, c, eps, scale_mode)
+            r = muon_update_ref(P, G, M, beta, lr, wd, k, a, b, c, eps, scale_mode, nesterov, schedule)
             outP.append(r[0]); outM.append(r[1]); outO.append(r[2])
         elif P.ndim == 3:
             rs = [muon_update_ref(P[e], np.asarray(G)[e], np.asarray(M)[e], beta, lr,
-                                  wd, k, a, b, c, eps, scale_mode)
+                                  wd, k, a, b, c, eps, scale_mode, nesterov, schedule)
                   for e in range(P.shape[0])]
             outP.append(np.stack([r[0] for r in rs]))
             outM.append(np.stack([r[1] for r in rs]))

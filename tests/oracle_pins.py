@@ -166,3 +166,57 @@ def pin_scale_and_decay(ref):
 
 
 ALL_PINS.append(pin_scale_and_decay)
+
+
+def p_iter_schedule(s, rows, k):
+    """Scalar iteration with per-step coefficients, the last row repeating,
+    in plain Python floats (Horner form)."""
+    out = []
+    for v in np.ravel(s):
+        v = float(v)
+        for t in range(k):
+            a, b, c = rows[min(t, len(rows) - 1)]
+            v2 = v * v
+            v = v * (a + v2 * (b + c * v2))
+        out.append(v)
+    return np.array(out).reshape(np.shape(s))
+
+
+# A per-step schedule of distinct rows: the quintic above, two milder
+# steps, then the textbook quintic Newton-Schulz map for the polar factor,
+# p(s) = (15 s - 10 s^3 + 3 s^5) / 8 (p(1) = 1, p'(1) = 0), which repeats.
+SCHEDULE = [(A_, B_, C_), (3.0, -3.2, 1.2), (2.0, -1.5, 0.5), (1.875, -1.25, 0.375)]
+
+
+def pin_schedule_diagonal(ref, k=6):
+    """Per-step coefficients act on each singular value as the composed
+    scalar maps p_{k-1}( ... p_0(s)), the last schedule row repeating: the
+    closed form of the diagonal case, step by step."""
+    sig = np.array([1.0, 0.8, 0.5, 0.11, 0.003])
+    X = np.zeros((5, 9)); X[np.arange(5), np.arange(5)] = sig
+    out = ref.newton_schulz(X, k, A_, B_, C_, SCHEDULE)
+    want = np.zeros_like(X); want[np.arange(5), np.arange(5)] = p_iter_schedule(sig, SCHEDULE, k)
+    assert np.max(np.abs(out - want)) <= 1e-12 * np.max(np.abs(want)), "schedule closed form"
+    one = ref.newton_schulz(X, k, A_, B_, C_, [(A_, B_, C_)])
+    assert np.array_equal(one, ref.newton_schulz(X, k, A_, B_, C_)), "one-row schedule = constant"
+
+
+def pin_nesterov(ref):
+    """Nesterov input U = G + beta M' on a 1 x n matrix (one singular value):
+    O = p^k(1) U / ||U|| with eps = 0, while M' stays beta M + G; with
+    beta = 0 the option changes nothing."""
+    rng = np.random.default_rng(7)
+    G = rng.standard_normal((1, 9)); M = rng.standard_normal((1, 9)); P = rng.standard_normal((1, 9))
+    beta = 0.9
+    U = G + beta * (beta * M + G)
+    _, Mp, O = ref.muon_update_ref(P, G, M, beta, 0.02, 0.0, 5, A_, B_, C_, 0.0, "none", True)
+    want = p_iter(np.array([1.0]), 5)[0] * U / math.sqrt(float(np.sum(U * U)))
+    assert np.max(np.abs(O - want)) <= 1e-12, "nesterov direction"
+    assert np.max(np.abs(Mp - (beta * M + G))) <= 1e-15, "nesterov keeps M'"
+    G2 = rng.standard_normal((4, 7)); M2 = rng.standard_normal((4, 7)); P2 = rng.standard_normal((4, 7))
+    r0 = ref.muon_update_ref(P2, G2, M2, 0.0, 0.02, 0.1, 5, A_, B_, C_, 1e-7, "sqrt_aspect", False)
+    r1 = ref.muon_update_ref(P2, G2, M2, 0.0, 0.02, 0.1, 5, A_, B_, C_, 1e-7, "sqrt_aspect", True)
+    assert all(np.array_equal(x, y) for x, y in zip(r0, r1)), "beta = 0"
+
+
+ALL_PINS += [pin_schedule_diagonal, pin_nesterov]

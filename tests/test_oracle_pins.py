@@ -43,7 +43,15 @@ MUTANTS = {
     "additive_decay": ("Pn = P * (1.0 - float(lr) * float(wd))", "Pn = P - float(lr) * float(wd)"),
     "scale_swapped": ("scale_factor(P.shape[0], P.shape[1], scale_mode)",
                       "scale_factor(P.shape[1], P.shape[0], scale_mode)"),
-    "one_step_short": ("for _ in range(int(k)):", "for _ in range(max(int(k) - 1, 0)):"),
+    "one_step_short": ("for a, b, c in coeffs:", "for a, b, c in coeffs[1:]:"),
+    "schedule_reversed": ("return [rows[min(s, len(rows) - 1)] for s in range(int(k))]",
+                          "return [rows[::-1][min(s, len(rows) - 1)] for s in range(int(k))]"),
+    "schedule_first_repeats": ("return [rows[min(s, len(rows) - 1)] for s in range(int(k))]",
+                               "return [rows[s] if s < len(rows) else rows[0] for s in range(int(k))]"),
+    "nesterov_undamped": ("return np.asarray(G, np.float64) + float(beta) * np.asarray(Mp, np.float64)",
+                          "return np.asarray(G, np.float64) + np.asarray(Mp, np.float64)"),
+    "nesterov_on_old_m": ("U = nesterov_input(Mp, G, beta) if nesterov else Mp",
+                          "U = nesterov_input(M, G, beta) if nesterov else Mp"),
 }
 
 
