@@ -404,7 +404,7 @@ def main():
     dg = per_group[dom]
     if dg["path"] == "skinny":
         gram_space = w.ns_steps <= 64
-        kfile = "k_skinny_gs.cu" if gram_space else "k_skinny.cu"
+        kfile = "k_skinny_gs.cuh" if gram_space else "k_skinny.cu"
         roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dg.get("roofline_frac"),
                 "kernel": ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"

@@ -106,6 +106,15 @@ typedef struct {
 #define MUON_FLAG_NO_GRAPH     2u  /* launch kernels one by one instead of a CUDA-graph replay  */
 #define MUON_FLAG_HOST_STAGING 4u  /* allocate device mirrors so muon_step_host can run         */
 #define MUON_FLAG_GROUP_TIMING 8u  /* record CUDA events around each group's kernels            */
+/* Nesterov look-ahead: orthogonalise U = G + beta M' instead of M' (M' is
+ * still the stored momentum).  The pages name no Nesterov form; this is the
+ * one that goes with the undamped momentum M' = beta M + G.  Skinny groups
+ * then also read G in the output pass, and for ns_steps > 64 (direct
+ * iteration) keep U in the workspace (4 bytes per element). */
+#define MUON_FLAG_NESTEROV    16u
+
+/* Rows a per-step coefficient schedule may have (muon_step_schedule). */
+#define MUON_MAX_SCHEDULE_ROWS 64
 
 typedef struct {
   int32_t mode;              /* muon_mode_t, default BF16                          */
@@ -201,6 +210,21 @@ MUON_API muon_status_t muon_step(muon_plan_t plan, void* const* params,
                                  const void* const* grads, float* const* momenta,
                                  float beta, float lr, float wd, int32_t ns_steps,
                                  float a, float b, float c, void* stream);
+
+/* muon_step with per-step coefficients («MindSpore HyperParallel X 盘古,Muon
+ * 优化器实现6倍性能跃升», 三大性能挑战: 5-10 iterations; the pages give no
+ * per-step values): Newton-Schulz step s (0-based) takes row
+ * min(s, n_rows - 1) of coeffs, a HOST array of n_rows x 3 floats
+ * (a_s, b_s, c_s), row-major, read before the call returns; the last row
+ * repeats past the end.  muon_step(..., a, b, c, ...) is the one-row case.
+ * The graph captured for ns_steps serves every schedule (the rows travel in
+ * the step's scalar table).  Errors: as muon_step, plus INVALID_ARG for
+ * coeffs NULL, n_rows not in [1, MUON_MAX_SCHEDULE_ROWS], or a non-finite
+ * coefficient. */
+MUON_API muon_status_t muon_step_schedule(muon_plan_t plan, void* const* params,
+                                          const void* const* grads, float* const* momenta,
+                                          float beta, float lr, float wd, int32_t ns_steps,
+                                          const float* coeffs, int32_t n_rows, void* stream);
 
 /* The same step on HOST buffers (pinned or pageable): copies each parameter,
  * gradient and momentum to the plan's device mirrors, runs muon_step on them,

@@ -41,7 +41,7 @@ def _shapes(shapes: Sequence[Sequence[int]]):
 
 def _options(mode="bf16", scale="sqrt_aspect", eps=1e-7, ns_dtype="fp16", skinny_threshold=0,
              path="auto", keep_update=False, no_graph=False, host_staging=False, max_streams=0,
-             group_timing=False):
+             group_timing=False, nesterov=False):
     L = _c.load()
     o = _c.muon_plan_options()
     _c.check(L.muon_default_options(C.byref(o)), "muon_default_options")
@@ -54,7 +54,8 @@ def _options(mode="bf16", scale="sqrt_aspect", eps=1e-7, ns_dtype="fp16", skinny
     o.flags = ((_c.MUON_FLAG_KEEP_UPDATE if keep_update else 0)
                | (_c.MUON_FLAG_NO_GRAPH if no_graph else 0)
                | (_c.MUON_FLAG_HOST_STAGING if host_staging else 0)
-               | (_c.MUON_FLAG_GROUP_TIMING if group_timing else 0))
+               | (_c.MUON_FLAG_GROUP_TIMING if group_timing else 0)
+               | (_c.MUON_FLAG_NESTEROV if nesterov else 0))
     o.max_streams = int(max_streams)
     return o
 
@@ -161,18 +162,31 @@ class MuonPlan:
             stream = torch.cuda.current_stream(self.device)
         return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
+    def _launch(self, P, G, M, beta, lr, wd, ns_steps, coeffs, stream):
+        """muon_step for one (a, b, c) triple; muon_step_schedule for a list of
+        per-step rows [(a_0, b_0, c_0), ...] (the last row repeats)."""
+        st = C.c_void_p(self._stream(stream))
+        if len(coeffs) and isinstance(coeffs[0], (tuple, list)):
+            rows = [tuple(float(v) for v in r) for r in coeffs]
+            flat = (C.c_float * (3 * max(len(rows), 1)))(*[v for r in rows for v in r])
+            _c.check(self._L.muon_step_schedule(self._h, P, G, M, float(beta), float(lr), float(wd),
+                                                int(ns_steps), flat, len(rows), st),
+                     "muon_step_schedule")
+            return
+        a, b, c = coeffs
+        _c.check(self._L.muon_step(self._h, P, G, M, float(beta), float(lr), float(wd),
+                                   int(ns_steps), float(a), float(b), float(c), st), "muon_step")
+
     def step(self, params, grads, momenta, beta, lr, wd, ns_steps=5, coeffs=QUINTIC,
              stream=None) -> None:
-        """One Muon step on device tensors (params / momenta updated in place)."""
+        """One Muon step on device tensors (params / momenta updated in place).
+        coeffs: (a, b, c), or a per-step schedule [(a_0, b_0, c_0), ...]."""
         import torch
         pd = self._pdtype()
         P = self._ptrs(params, "params", pd, "cuda")
         G = self._ptrs(grads, "grads", pd, "cuda")
         M = self._ptrs(momenta, "momenta", torch.float32, "cuda")
-        a, b, c = coeffs
-        _c.check(self._L.muon_step(self._h, P, G, M, float(beta), float(lr), float(wd),
-                                   int(ns_steps), float(a), float(b), float(c),
-                                   C.c_void_p(self._stream(stream))), "muon_step")
+        self._launch(P, G, M, beta, lr, wd, ns_steps, coeffs, stream)
 
     def bind(self, params, grads, momenta):
         """Validate and marshal the tensors once; the returned handle feeds
@@ -185,10 +199,7 @@ class MuonPlan:
     def step_bound(self, bound, beta, lr, wd, ns_steps=5, coeffs=QUINTIC, stream=None) -> None:
         """muon_step on pointer arrays prepared by bind()."""
         P, G, M = bound
-        a, b, c = coeffs
-        _c.check(self._L.muon_step(self._h, P, G, M, float(beta), float(lr), float(wd),
-                                   int(ns_steps), float(a), float(b), float(c),
-                                   C.c_void_p(self._stream(stream))), "muon_step")
+        self._launch(P, G, M, beta, lr, wd, ns_steps, coeffs, stream)
 
     def step_host(self, params, grads, momenta, beta, lr, wd, ns_steps=5, coeffs=QUINTIC,
                   stream=None) -> None:

@@ -32,6 +32,8 @@ MUON_FLAG_KEEP_UPDATE = 1
 MUON_FLAG_NO_GRAPH = 2
 MUON_FLAG_HOST_STAGING = 4
 MUON_FLAG_GROUP_TIMING = 8
+MUON_FLAG_NESTEROV = 16
+MUON_MAX_SCHEDULE_ROWS = 64
 
 
 class muon_shape_t(C.Structure):
@@ -57,7 +59,7 @@ EXPORTED_TESTING = ["muon_testing_tc_gemm", "muon_testing_skinny_max_clusters",
 
 # every symbol include/muon.h declares, for the export check
 EXPORTED = ["muon_default_options", "muon_plan_describe", "muon_plan_create", "muon_step",
-            "muon_step_host", "muon_plan_destroy", "muon_plan_num_groups",
+            "muon_step_schedule", "muon_step_host", "muon_plan_destroy", "muon_plan_num_groups",
             "muon_plan_group_info", "muon_plan_workspace_bytes", "muon_debug_copy_update",
             "muon_plan_assign",
             "muon_plan_check_error", "muon_plan_group_elapsed_ms", "muon_step_skinny_static",
@@ -93,6 +95,8 @@ def load() -> C.CDLL:
     L.muon_step.argtypes = [vp, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), f32, f32, f32, i32,
                             f32, f32, f32, vp]
     L.muon_step_host.argtypes = L.muon_step.argtypes
+    L.muon_step_schedule.argtypes = [vp, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), f32, f32, f32,
+                                     i32, C.POINTER(f32), i32, vp]
     L.muon_plan_destroy.argtypes = [vp]
     L.muon_plan_assign.argtypes = [C.POINTER(muon_shape_t), i32, C.POINTER(muon_plan_options), i32, i32,
                                    C.POINTER(i32), i64, C.POINTER(C.c_double), C.POINTER(C.c_double)]
@@ -121,7 +125,7 @@ def load() -> C.CDLL:
     L.muon_version.argtypes = []
     L.muon_version.restype = C.c_char_p
     for name in ("muon_default_options", "muon_plan_describe", "muon_plan_create", "muon_step",
-                 "muon_step_host", "muon_plan_destroy", "muon_plan_group_info",
+                 "muon_step_schedule", "muon_step_host", "muon_plan_destroy", "muon_plan_group_info",
                  "muon_debug_copy_update", "muon_plan_check_error",
                  "muon_plan_group_elapsed_ms"):
         getattr(L, name).restype = C.c_int

@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmuon_gb300.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
+                     "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-Werror=narrowing",
+                     "--expt-relaxed-constexpr",
                      "-I" + os.path.join(HERE, "..", "include")]
 
 

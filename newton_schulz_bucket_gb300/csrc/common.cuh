@@ -23,6 +23,13 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(v);
 }
 
+// (a, b, c) of Newton-Schulz step s: the schedule's row s, its last row past
+// the end.
+__device__ __forceinline__ const float* step_coef(const StepScalars* sc, int s) {
+  const int n = sc->n_coef;
+  return sc->coef[s < n ? s : n - 1];
+}
+
 __device__ __forceinline__ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }

@@ -10,12 +10,18 @@
 
 namespace muon {
 
+// Rows of a per-step coefficient schedule held in the step scalars.
+constexpr int32_t kMaxScheduleRows = 64;
+
 // Per-step scalars, rewritten in device memory before every step so that one
-// captured CUDA graph serves every step with the same ns_steps.
+// captured CUDA graph serves every step with the same ns_steps.  Newton-Schulz
+// step s takes coef[min(s, n_coef - 1)] as (a, b, c).
 struct StepScalars {
-  float beta, lr, wd, a, b, c;
+  float beta, lr, wd;
   int32_t ns_steps;
-  int32_t pad_;
+  int32_t n_coef;
+  int32_t pad_[3];
+  float coef[kMaxScheduleRows][3];
 };
 
 // Per-member device pointers, rewritten before every step (the caller may
@@ -59,6 +65,8 @@ struct KArgs {
   float* dbg;              // nullable: [B][rows][cols] fp32 copy of O
   int* err;                // device error word
   int32_t l2_keep_m;       // momentum kernel stores M' evict-last (it is read back soon, twice)
+  int32_t nesterov;        // orthogonalise U = G + beta M' instead of M'
+  float* u;                // nullable: [B][rows][cols] U written by the momentum kernel (direct kernel's input)
 };
 
 // Skinny path configuration of a group (a function of (rows, cols) only).
@@ -88,10 +96,10 @@ cudaError_t launch_write(const KArgs& a, const void* src, cudaStream_t s);
 
 // SIMT batched products (fp32 FMA) on the workspace type of `a`:
 //   gram:   A = (Y Y^T) / alpha^2
-//   poly:   Q = a I + b A + c A A
+//   poly:   Q = a I + b A + c A A, (a, b, c) of Newton-Schulz step `step`
 //   update: Ydst = Q Ysrc
 cudaError_t launch_simt_gram(const KArgs& a, const void* y, cudaStream_t s);
-cudaError_t launch_simt_poly(const KArgs& a, cudaStream_t s);
+cudaError_t launch_simt_poly(const KArgs& a, int step, cudaStream_t s);
 cudaError_t launch_simt_update(const KArgs& a, const void* ysrc, void* ydst, cudaStream_t s);
 
 // Skinny path, the whole step of a group: for k <= kGramSpaceMaxSteps one
@@ -124,7 +132,7 @@ struct TcMaps {
 cudaError_t tc_make_maps(const KArgs& a, TcMaps* t);
 cudaError_t prepare_tc(int ns_type);  // function attributes
 cudaError_t launch_tc_gram(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
-cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, cudaStream_t s);
+cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, int step, cudaStream_t s);  // step: schedule row
 // Y[1 - src] = Q Y[src]
 cudaError_t launch_tc_update(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
 

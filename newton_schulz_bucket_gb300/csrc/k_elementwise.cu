@@ -14,9 +14,10 @@ namespace {
 constexpr int kThreads = 256;
 
 // One CTA = one fixed chunk of one member: M' = beta M + G (stored), and the
-// chunk's sum of squares of M' (fixed-order tree) into part[b][chunk].  G and
-// M are read once (evict-first in L2).  M' is stored evict-last when the next
-// kernel reads it back twice (skinny path), so it is still in L2 then.
+// chunk's sum of squares of X = M' (Nesterov: X = U = G + beta M') by a
+// fixed-order tree into part[b][chunk]; with a.u set, U is stored there too.
+// G and M are read once (evict-first in L2).  M' is stored evict-last when the
+// next kernel reads it back twice (skinny path), so it is still in L2 then.
 template <typename TG>
 __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
   __shared__ float red[33];
@@ -28,8 +29,10 @@ __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
   const TG* G = static_cast<const TG*>(mp.G);
   float* M = mp.M;
   const float beta = a.sc->beta;
+  const bool nest = a.nesterov != 0;
+  float* U = a.u ? a.u + (int64_t)b * total : nullptr;
   float acc = 0.f;
-  const bool vec = aligned16(G) && aligned16(M);
+  const bool vec = aligned16(G) && aligned16(M) && (!U || aligned16(U));
   const uint64_t pin = l2_evict_first();
   const uint64_t pout = a.l2_keep_m ? l2_evict_last() : l2_evict_normal();
   auto load8g = [&](const TG* p, float* f) {
@@ -41,45 +44,59 @@ __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
   };
   int64_t i0 = start;
   if (vec) {
-    constexpr int U = 4;  // 4 x 8 elements in flight per thread
+    constexpr int UN = 4;  // 4 x 8 elements in flight per thread
     const int64_t stride = (int64_t)8 * kThreads;
     int64_t i = start + 8 * threadIdx.x;
-    for (; i + (U - 1) * stride + 8 <= end; i += U * stride) {
-      float g[U][8], m[U][8];
+    for (; i + (UN - 1) * stride + 8 <= end; i += UN * stride) {
+      float g[UN][8], m[UN][8];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
+      for (int u = 0; u < UN; ++u) {
         load8g(G + i + u * stride, g[u]);
         u4_to_f4x2(ld_hint(M + i + u * stride, pin), ld_hint(M + i + u * stride + 4, pin), m[u]);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
+      for (int u = 0; u < UN; ++u) {
+        float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           m[u][e] = fmaf(beta, m[u][e], g[u][e]);
-          acc = fmaf(m[u][e], m[u][e], acc);
+          x[e] = nest ? fmaf(beta, m[u][e], g[u][e]) : m[u][e];
+          acc = fmaf(x[e], x[e], acc);
         }
         st_hint(M + i + u * stride, f4_to_u4(m[u]), pout);
         st_hint(M + i + u * stride + 4, f4_to_u4(m[u] + 4), pout);
+        if (U) {
+          st_hint(U + i + u * stride, f4_to_u4(x), pout);
+          st_hint(U + i + u * stride + 4, f4_to_u4(x + 4), pout);
+        }
       }
     }
     for (; i + 8 <= end; i += stride) {
-      float g[8], m[8];
+      float g[8], m[8], x[8];
       load8g(G + i, g);
       u4_to_f4x2(ld_hint(M + i, pin), ld_hint(M + i + 4, pin), m);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         m[e] = fmaf(beta, m[e], g[e]);
-        acc = fmaf(m[e], m[e], acc);
+        x[e] = nest ? fmaf(beta, m[e], g[e]) : m[e];
+        acc = fmaf(x[e], x[e], acc);
       }
       st_hint(M + i, f4_to_u4(m), pout);
       st_hint(M + i + 4, f4_to_u4(m + 4), pout);
+      if (U) {
+        st_hint(U + i, f4_to_u4(x), pout);
+        st_hint(U + i + 4, f4_to_u4(x + 4), pout);
+      }
     }
     i0 = start + ((end - start) / 8) * 8;  // scalar tail below
   }
   for (int64_t i = i0 + threadIdx.x; i < end; i += kThreads) {
-    float v = fmaf(beta, M[i], to_f32(G[i]));
+    const float g = to_f32(G[i]);
+    const float v = fmaf(beta, M[i], g);
     M[i] = v;
-    acc = fmaf(v, v, acc);
+    const float x = nest ? fmaf(beta, v, g) : v;
+    if (U) U[i] = x;
+    acc = fmaf(x, x, acc);
   }
   const float s = block_sum(acc, red);
   if (threadIdx.x == 0) a.part[(int64_t)b * a.n_chunks + blockIdx.x] = s;
@@ -97,21 +114,35 @@ __global__ void __launch_bounds__(kThreads) k_norm_finalize(KArgs a) {
   if (threadIdx.x == 0) a.invn[b] = a.alpha / (sqrtf(s) + a.eps);
 }
 
-// Y[b] = cast(M'[b] * invn[b]) in the wide orientation: Y is m x n with row
-// pitch n_pitch; for T (rows > cols) Y = M'^T.  64 x 64 tiles through shared
-// memory so both the read of M' and the write of Y are coalesced.
+// Y[b] = cast(X[b] * invn[b]) in the wide orientation, X = M' (Nesterov:
+// U = G + beta M'): Y is m x n with row pitch n_pitch; for T (rows > cols)
+// Y = X^T.  64 x 64 tiles through shared memory so both the reads and the
+// write of Y are coalesced.
 template <typename TY>
 __global__ void __launch_bounds__(kThreads) k_normalize_cast(KArgs a, TY* __restrict__ Y) {
   __shared__ float tile[64][65];
   const int b = blockIdx.z;
   const float* Mp = a.mem[b].M;
+  const void* Gp = a.mem[b].G;
+  const bool nest = a.nesterov != 0;
+  const float beta = a.sc->beta;
   const float inv = a.invn[b];
   TY* Yb = Y + (int64_t)b * a.m * a.n_pitch;
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;  // tile origin (parameter coords)
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
   for (int rr = ty; rr < 64; rr += 4) {
     const int r = r0 + rr, c = c0 + tx;
-    tile[rr][tx] = (r < a.rows && c < a.cols) ? Mp[(int64_t)r * a.cols + c] * inv : 0.f;
+    float x = 0.f;
+    if (r < a.rows && c < a.cols) {
+      const int64_t o = (int64_t)r * a.cols + c;
+      x = Mp[o];
+      if (nest) {
+        const float g = a.mode_f32 ? static_cast<const float*>(Gp)[o]
+                                   : __bfloat162float(static_cast<const __nv_bfloat16*>(Gp)[o]);
+        x = fmaf(beta, x, g);
+      }
+    }
+    tile[rr][tx] = x * inv;
   }
   __syncthreads();
   if (!a.T) {

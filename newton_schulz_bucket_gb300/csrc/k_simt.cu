@@ -24,6 +24,7 @@ struct GemmDesc {
   int64_t lda, ldb, ldc;
   int M, N, K;
   int b_trans;  // B(k, j) = B[j * ldb + k] when set, else B[k * ldb + j]
+  int step;     // poly: Newton-Schulz step (schedule row)
 };
 
 template <typename TI, typename TO, int OP>
@@ -70,7 +71,10 @@ __global__ void __launch_bounds__(kThreads) k_simt_gemm(GemmDesc d, KArgs a) {
     __syncthreads();
   }
   float pa = 0.f, pb = 0.f, pc = 0.f, inv_a2 = 0.f;
-  if (OP == OP_POLY) { pa = a.sc->a; pb = a.sc->b; pc = a.sc->c; }
+  if (OP == OP_POLY) {
+    const float* cf = step_coef(a.sc, d.step);
+    pa = cf[0]; pb = cf[1]; pc = cf[2];
+  }
   if (OP == OP_GRAM) inv_a2 = 1.f / (a.alpha * a.alpha);
   const TI* Aux = static_cast<const TI*>(d.Aux) + b * d.sA;
 #pragma unroll
@@ -114,8 +118,9 @@ cudaError_t launch_simt_gram(const KArgs& a, const void* y, cudaStream_t s) {
   return dispatch<OP_GRAM>(d, a, s);
 }
 
-cudaError_t launch_simt_poly(const KArgs& a, cudaStream_t s) {
+cudaError_t launch_simt_poly(const KArgs& a, int step, cudaStream_t s) {
   GemmDesc d{};
+  d.step = step;
   d.A = a.A; d.B = a.A; d.C = a.Q; d.Aux = a.A;
   d.sA = d.sB = d.sC = (int64_t)a.m * a.m_pitch;
   d.lda = d.ldb = d.ldc = a.m_pitch;

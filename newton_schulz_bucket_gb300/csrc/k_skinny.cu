@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   PassCtx<MT> c;
   c.lane = lane; c.warp = warp; c.g = lane >> 2; c.t4 = lane & 3;
   c.m = m; c.n = a.n; c.c0 = (int)rank * s.W; c.NB = s.NB;
-  c.Mp = mp.M;
+  // X_0's source: M', or U = G + beta M' written by the momentum kernel
+  c.Mp = a.u ? a.u + (int64_t)b * a.rows * a.cols : mp.M;
   c.P = static_cast<__nv_bfloat16*>(mp.P);
   c.wd = Wide{a.cols, a.T};
   // pairs (i, j), (i, j+1) are adjacent in memory (fast path) when the wide
@@ -346,7 +347,6 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   c.inv = misc[0];
 
   const int ns = a.sc->ns_steps;
-  const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
   const float inv_a2 = 1.f / (a.alpha * a.alpha);
   const float lr = a.sc->lr, wdk = a.sc->wd;
   c.decay = 1.f - lr * wdk;
@@ -361,9 +361,12 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
     for (int q = 0; q < GT::N; ++q) gacc[q][0] = gacc[q][1] = gacc[q][2] = gacc[q][3] = 0.f;
   };
   // sum the Gram partials (warps in fixed order, then CTAs in rank order),
-  // form Q = a I + b A + c A A in fp32 and load its fragments
+  // form Q = a I + b A + c A A in fp32 (step p's coefficients) and load its
+  // fragments
   auto reduce_and_poly = [&](int p) {
     const int g = c.g, t4 = c.t4;
+    const float* cf = step_coef(a.sc, p);
+    const float ca = cf[0], cb = cf[1], cc = cf[2];
 #pragma unroll
     for (int q = 0; q < GT::N; ++q) {
       float* dst = wpart + (warp * GT::N + q) * 128;

@@ -1,1012 +1,24 @@
-// Skinny path for m = min(rows, cols) <= 64: the whole Muon step of a member
-// in one kernel, with Newton-Schulz evaluated in Gram space.
-//
-// «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: for
-// shapes such as [24, 10240] the per-parameter iteration is dominated by host
-// dispatch, small allocations and synchronisation, and batching every member
-// of a shape into one launch removes that (Fig. 7).  On this GPU the batched
-// work is bound by bytes moved (HBM, and L2, whose read bandwidth is close to
-// HBM's), so the kernel streams the member's data twice however many steps
-// are taken:
-//
-//   1. momentum pass: M' = beta M + G is formed and stored, and from the same
-//      registers the sum of squares ||M'||_F^2 and the Gram matrix M' M'^T
-//      (tf32 tensor-core products, fp32 accumulation: the norm is not known
-//      yet, and tf32 keeps fp32's range with an 11-bit significand);
-//   2. in m x m space, fp32: A_0 = M' M'^T / (||M'||_F + eps)^2, then per step
-//      Q = a I + b A + c A^2, Pi <- Q Pi, A <- Q A Q (3xTF32 tensor-core
-//      tiles up to m = 32, where the stage is latency-bound; fp32 FFMA
-//      above, where it is throughput-bound);
-//   3. output pass: Y_0 = alpha M' / (||M'||_F + eps) in the operand type,
-//      O = Pi_k Y_0 / alpha with Pi_k split into an operand-type high part and
-//      a residual low part, and P' = P (1 - lr wd) - lr s O.
-//
-// Each quintic step is X' = Q X with Q = a I + b A + c A^2 and A = X X^T
-// («关于分布式Muon的想法整合及讨论» §1, §2, §6).  Q is a polynomial in A, so it
-// is symmetric and commutes with A, hence A' = X' X'^T = Q A Q and
-// X_k = Pi_k X_0 with Pi_k = Q_{k-1} ... Q_0: in exact arithmetic this is the
-// iteration itself; in floating point the data is rounded to the operand
-// type once instead of once per step.  All reduction orders depend only on
-// (rows, cols), so a member gives the same bits in any batch.
-//
-// Layout: one cluster of kCL CTAs per member; CTA r owns the wide iterate's
-// columns [r W, (r + 1) W), 16 warps up to m = 32 and 8 beyond (each lane
-// then keeps Pi's fragments for four 16-row tiles, 128 registers).  Both
-// passes walk 32-column superblocks (superblock sb by warp sb % NW).  In the
-// momentum pass lane (g, t4) holds rows 16 mi + g (+ 8) and the eight
-// consecutive columns 8 t4 .. 8 t4 + 7, which stand in tf32 A-fragment slots
-// (see gs_momentum_pass); the output pass loads Y_0 straight into B
-// fragments (see gs_out_pass).  The Gram sums over all columns and Pi X acts on each column
-// alone, so these fixed permutations of a block's columns change nothing, and
-// they turn every access into a 16-byte (fp32) or 8/16-byte (bf16) vector.
-// Operands stream through a per-lane cp.async ring.
-#include "warp_mma.cuh"
+// Gram-space skinny kernel: the plain-momentum instantiations and the
+// dispatch between them and the Nesterov ones (k_skinny_gs_nesterov.cu).  The
+// kernel itself is in k_skinny_gs.cuh.
+#include "k_skinny_gs.cuh"
 
 namespace muon {
 
-namespace {
-
-constexpr int kCL = 2;  // CTAs per member (cluster size)
-
-template <int MT, int NT, bool HALF>
-struct GsLayout {
-  static constexpr int MP = 16 * MT;                    // padded m
-  static constexpr int LD = MP + 4;                     // fp32 m x m row pitch: 16-byte rows, no bank conflicts
-  static constexpr int NW = NT / 32;
-  static constexpr int R = 2 * MT - (HALF ? 1 : 0);     // rows g + 8 h a lane holds (momentum pass, output rows)
-  static constexpr int KR = 4 * MT - (HALF ? 2 : 0);    // rows 2 t4 + {0, 1, 8, 9} a lane holds (output pass)
-  static constexpr int NJ = HALF ? 2 * MT - 1 : 2 * MT; // 8-row groups of the Gram's columns
-  using GT = GramTiles<MT, NJ>;
-  // Both passes are bound by the bytes a CTA keeps in flight, so each ring
-  // takes as many rounds as shared memory holds next to the fixed part
-  // (this CTA's Gram partial, misc words, Pi's row scales, the upper-triangle
-  // index table).
-  static constexpr int kTab = ((MP * (MP + 1) / 2) * 4 + 15) / 16 * 16;
-  static constexpr int kFixed = MP * MP * 4 + 64 + MP * 4 + kTab;
-  static constexpr int kCap = 227 * 1024 - kFixed;
-  // momentum pass ring: 32 B of M and 16 B of G per row and lane; one round at a time
-  static constexpr int LB1 = 48 * R;
-  static constexpr int S1 = 4 * NW * 32 * LB1 <= kCap ? 4 : (3 * NW * 32 * LB1 <= kCap ? 3 : 2);
-  static constexpr int kRing1 = S1 * NW * 32 * LB1;
-  // output pass ring: 16 B of M' per k-row and 16 B of P per output row and lane; one round at a time
-  static constexpr int LBO = 16 * (KR + R);
-  static constexpr int SO = 4 * NW * 32 * LBO <= kCap ? 4 : (3 * NW * 32 * LBO <= kCap ? 3 : 2);
-  static constexpr int kRingO = SO * NW * 32 * LBO;
-  // between the passes the ring holds the per-warp Gram partials and sums of
-  // squares, then the m x m work arrays: A, Q, T, Pi (two) -- for m <= 32
-  // each stored as a tf32 high part and a tf32 residual, else in fp32 -- and
-  // Pi's operand-type high / low parts
-  static constexpr int kWarpPart = NW * GT::N * 128 * 4 + NW * 4 * 4;
-  static constexpr int kMat = MP * LD * 4;
-  static constexpr int kPiT = MP * (MP + 8) * 2;
-  static constexpr bool TC = MT <= 2;  // m x m products on the tensor cores (else FFMA)
-  static constexpr int kMM = (TC ? 10 : 5) * kMat + 2 * kPiT;  // A, Q, T, Pi x2, then Pi high / low
-  // the rings, the per-warp partials and the m x m arrays are live one after
-  // the other and share the same bytes
-  static constexpr int kU0 = kRing1 > kRingO ? kRing1 : kRingO;
-  static constexpr int kU1 = kWarpPart > kMM ? kWarpPart : kMM;
-  static constexpr int kU = kU0 > kU1 ? kU0 : kU1;
-  static constexpr int kCta = kU;                       // this CTA's Gram partial (peer reads it)
-  static constexpr int kMisc = kCta + MP * MP * 4;      // [0] sum of squares (peer reads it)
-  static constexpr int kRsc = kMisc + 64;               // Pi's row scales
-  static constexpr int kTabOff = kRsc + MP * 4;         // (i << 16 | j) of the upper triangle, row-major
-  static constexpr int kTotal = kTabOff + kTab;
-  static_assert(kTotal == kU + kFixed, "layout");
-  static_assert(kTotal <= 227 * 1024, "Gram-space kernel shared memory exceeds the per-CTA limit");
-};
-
-// Wide-iterate element (i, j) in the parameter's memory.
-struct Wide {
-  int cols, T;
-  __device__ __forceinline__ int64_t off(int i, int j) const {
-    return T ? (int64_t)j * cols + i : (int64_t)i * cols + j;
-  }
-};
-
-// Per-thread state of one member's two data passes.
-struct GsCtx {
-  int lane, warp, g, t4, m, n, c0, NB;  // NB: 16-column blocks of this CTA (even)
-  bool vec;            // rows <= cols, cols % 8 == 0, 32 cols < 2^31, M', G and P 16-byte aligned
-  float* Mp;
-  const __nv_bfloat16* G;
-  __nv_bfloat16* P;
-  float* dbg;
-  int cols;
-  Wide wd;
-  float beta, inv, decay, coef, inv_alpha;
-};
-
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Momentum pass over this warp's 32-column superblocks: M' = beta M + G
-// stored, ss += M'^2 per lane, and gacc += M' M'^T on the upper Gram tiles
-// (tf32).  In registers lane (g, t4) holds rows 16 mi + g (+ 8) and columns
-// J + 8 t4 .. J + 8 t4 + 7; column J + 8 t4 + 2 st + e stands in the tf32
-// A-fragment slot k = t4 + 4 e of k8 step st.  All three streams keep the
-// default L2 policy: measured, evict-first reads or evict-last stores here
-// only slowed the pass.
-template <int MT, int NT, bool HALF>
-__device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
-                                                 float (&gacc)[GsLayout<MT, NT, HALF>::GT::N][4], float& ss) {
-  using L = GsLayout<MT, NT, HALF>;
-  using GT = typename L::GT;
-  constexpr int NW = L::NW, S = L::S1, LB = L::LB1, R = L::R;
-  constexpr uint32_t kSlot = NW * 32 * LB;
-  const int lane = c.lane;
-  uint8_t* ring_warp = ring + c.warp * 32 * LB;
-  const uint32_t ring0 = smem_u32(ring_warp);
-  const int nsb = c.NB / 2;  // superblocks of this CTA
-  const int rounds = (nsb + NW - 1) / NW;
-  auto row_of = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
-  const uint64_t pol = l2_evict_normal();
-  const float2 beta2 = make_float2(c.beta, c.beta);
-  float2 ss2 = make_float2(0.f, 0.f);
-
-  // A round's slot holds the superblock as row-major tiles, so that every
-  // global access of a warp moves whole lines: M (later M') rows of 128 B
-  // whose 16-byte chunk q sits at q ^ (row & 1) (the fragment reads below are
-  // then free of bank conflicts), and G rows of 64 B.  Lanes copy in and out
-  // by rows (8 lanes per M row, 4 per G row) and read their fragments after a
-  // warp barrier.
-  constexpr int RT = 8 * R;  // rows of the tile (rows >= m are zero-filled)
-  auto mchunk = [](int row, int q) { return row * 128 + ((q ^ (row & 1)) << 4); };
-  auto issue = [&](int r, uint32_t dst) {
-    const int sb = r * NW + c.warp;
-    if (c.vec && r < rounds && sb < nsb) {
-      const int J = c.c0 + sb * 32;
-#pragma unroll
-      for (int k = 0; k < RT / 4; ++k) {
-        const int row = 4 * k + (lane >> 3), q = lane & 7;
-        const bool ok = row < c.m && J + 4 * q < c.n;
-        cp_async16_hint(dst + mchunk(row, q),
-                        ok ? (const void*)(c.Mp + (int64_t)row * c.cols + J + 4 * q) : (const void*)c.Mp,
-                        ok ? 16 : 0, pol);
-      }
-#pragma unroll
-      for (int k = 0; k < RT / 8; ++k) {
-        const int row = 8 * k + (lane >> 2), q = lane & 3;
-        const bool ok = row < c.m && J + 8 * q < c.n;
-        cp_async16_hint(dst + RT * 128 + row * 64 + q * 16,
-                        ok ? (const void*)(c.G + (int64_t)row * c.cols + J + 8 * q) : (const void*)c.G,
-                        ok ? 16 : 0, pol);
-      }
-    }
-    cp_async_commit();
-  };
-
-#pragma unroll
-  for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
-
-  auto process = [&](int r, uint8_t* st) {
-    const int sb = r * NW + c.warp;
-    if (r >= rounds || sb >= nsb) return;
-    const int J = c.c0 + sb * 32;
-    const int j0 = J + 8 * c.t4;
-    // tv[mi][st][h][e]: row 16 mi + g + 8 h, tf32 slot k = t4 + 4 e of k8 step st
-    uint32_t tv[MT][4][2][2];
-    if (c.vec) __syncwarp();  // every lane's copies of this round have landed
-#pragma unroll
-    for (int s = 0; s < R; ++s) {
-      const int i = row_of(s);
-      float v[8];
-      if (c.vec) {
-        float4* m0p = reinterpret_cast<float4*>(st + mchunk(i, 2 * c.t4));
-        float4* m1p = reinterpret_cast<float4*>(st + mchunk(i, 2 * c.t4 + 1));
-        const float4 m0 = *m0p, m1 = *m1p;
-        float gf[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + RT * 128 + i * 64 + c.t4 * 16), gf);
-        const float2 r0 = __ffma2_rn(beta2, make_float2(m0.x, m0.y), make_float2(gf[0], gf[1]));
-        const float2 r1 = __ffma2_rn(beta2, make_float2(m0.z, m0.w), make_float2(gf[2], gf[3]));
-        const float2 r2 = __ffma2_rn(beta2, make_float2(m1.x, m1.y), make_float2(gf[4], gf[5]));
-        const float2 r3 = __ffma2_rn(beta2, make_float2(m1.z, m1.w), make_float2(gf[6], gf[7]));
-        v[0] = r0.x; v[1] = r0.y; v[2] = r1.x; v[3] = r1.y;
-        v[4] = r2.x; v[5] = r2.y; v[6] = r3.x; v[7] = r3.y;
-        *m0p = make_float4(v[0], v[1], v[2], v[3]);  // M' replaces M in the tile
-        *m1p = make_float4(v[4], v[5], v[6], v[7]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          v[q] = 0.f;
-          if (i < c.m && j0 + q < c.n) {
-            const int64_t o = c.wd.off(i, j0 + q);
-            v[q] = fmaf(c.beta, c.Mp[o], __bfloat162float(c.G[o]));
-            c.Mp[o] = v[q];
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) ss2 = __ffma2_rn(make_float2(v[2 * q], v[2 * q + 1]),
-                                                  make_float2(v[2 * q], v[2 * q + 1]), ss2);
-#pragma unroll
-      for (int st4 = 0; st4 < 4; ++st4) {
-        tv[s >> 1][st4][s & 1][0] = to_tf32(v[2 * st4]);
-        tv[s >> 1][st4][s & 1][1] = to_tf32(v[2 * st4 + 1]);
-      }
-    }
-    if (c.vec) {
-      // M' out by rows, whole lines (each lane stores the chunks it will refill)
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < RT / 4; ++k) {
-        const int row = 4 * k + (lane >> 3), q = lane & 7;
-        if (row < c.m && J + 4 * q < c.n)
-          st_hint(c.Mp + (int64_t)row * c.cols + J + 4 * q,
-                  *reinterpret_cast<const uint4*>(st + mchunk(row, q)), pol);
-      }
-    }
-    if (HALF) {
-#pragma unroll
-      for (int st4 = 0; st4 < 4; ++st4) tv[MT - 1][st4][1][0] = tv[MT - 1][st4][1][1] = 0u;
-    }
-#pragma unroll
-    for (int q = 0; q < GT::N; ++q) {
-      const int mi = GT::code(q) >> 4, nj = GT::code(q) & 15;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_tf32(gacc[q], tv[mi][k][0][0], tv[mi][k][1][0], tv[mi][k][0][1], tv[mi][k][1][1],
-                 tv[nj >> 1][k][nj & 1][0], tv[nj >> 1][k][nj & 1][1]);
-    }
-  };
-
-  for (int r = 0; r < rounds; ++r) {
-    cp_async_wait<S - 1>();
-    process(r, ring_warp + (r % S) * kSlot);
-    // round r is consumed (its M' copied out): refill its slot
-    issue(r + S, ring0 + (r % S) * kSlot);
-  }
-  cp_async_wait<0>();
-  ss += ss2.x + ss2.y;
-}
-
-// The output pass's ring and its copies: round r lives in slot r % S.
-template <int MT, int NT, bool HALF>
-struct GsOutRing {
-  using L = GsLayout<MT, NT, HALF>;
-  static constexpr int NW = L::NW, S = L::SO, LB = L::LBO, R = L::R, KR = L::KR;
-  static constexpr uint32_t kSlot = NW * 32 * LB;
-  static __device__ __forceinline__ int slot(int r) { return r % S; }
-
-  // loop-invariant element offsets of this lane's rows (32 cols < 2^31 on the
-  // vector path); rows >= m read as zero
-  int moff[KR], poff[R];
-  uint32_t mok, pok;
-  uint32_t ring0;
-  int rounds, nsb;
-
-  __device__ __forceinline__ static int krow(const GsCtx& c, int kr) {
-    return (kr >> 2) * 16 + 2 * c.t4 + (kr & 1) + ((kr & 2) ? 8 : 0);
-  }
-  __device__ __forceinline__ static int orow(const GsCtx& c, int s) {
-    return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0);
-  }
-  __device__ __forceinline__ GsOutRing(const GsCtx& c, uint8_t* ring) {
-    ring0 = smem_u32(ring + c.warp * 32 * LB);
-    nsb = c.NB / 2;  // superblocks of this CTA
-    rounds = (nsb + NW - 1) / NW;
-    mok = pok = 0;
-#pragma unroll
-    for (int kr = 0; kr < KR; ++kr) {
-      moff[kr] = krow(c, kr) * c.cols;
-      if (krow(c, kr) < c.m) mok |= 1u << kr;
-    }
-#pragma unroll
-    for (int s = 0; s < R; ++s) {
-      poff[s] = orow(c, s) * c.cols;
-      if (orow(c, s) < c.m) pok |= 1u << s;
-    }
-  }
-  // round r's M' and P into its slot, as one commit group (empty past the end)
-  __device__ __forceinline__ void issue(const GsCtx& c, int r, uint64_t pol) const {
-    const int sb = r * NW + c.warp;
-    if (c.vec && r < rounds && sb < nsb) {
-      const uint32_t dst = ring0 + slot(r) * kSlot;
-      const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
-      const bool cm = jm < c.n, cpp = jp < c.n;  // n % 8 == 0: a lane's columns share fate
-#pragma unroll
-      for (int kr = 0; kr < KR; ++kr) {
-        const bool ok = cm && ((mok >> kr) & 1u);
-        cp_async16_hint(dst + kr * 512 + c.lane * 16, c.Mp + (ok ? moff[kr] + jm : 0), ok ? 16 : 0, pol);
-      }
-#pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const bool ok = cpp && ((pok >> s) & 1u);
-        cp_async16_hint(dst + (KR + s) * 512 + c.lane * 16, c.P + (ok ? poff[s] + jp : 0), ok ? 16 : 0,
-                        pol);
-      }
-    }
-    cp_async_commit();
-  }
-};
-
-// Output pass over this warp's 32-column superblocks: O = (Pi_hi + Pi_lo) Y_0
-// and P' = P (1 - lr wd) - lr s O.  Y_0 is loaded straight into B fragments:
-// lane (g, t4) holds rows 16 kk + 2 t4 + {0, 1, 8, 9} of columns
-// J + 4 g .. J + 4 g + 3, column J + 4 g + q standing at n = g of n-tile q.
-// Accumulator n of n-tile q is then column J + 4 n + q, so a lane's outputs
-// of a row are the eight consecutive columns J + 8 t4 .. J + 8 t4 + 7.
-template <typename TY, int MT, int NT, bool HALF>
-__device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
-                                            const uint32_t (&ph)[MT][MT][4], const uint32_t (&pl)[MT][MT][4],
-                                            const float (&rs)[GsLayout<MT, NT, HALF>::R]) {
-  using L = GsLayout<MT, NT, HALF>;
-  using Ring = GsOutRing<MT, NT, HALF>;
-  constexpr int NW = L::NW, S = L::SO, LB = L::LBO, KR = L::KR;
-  constexpr uint32_t kSlot = NW * 32 * LB;
-  const int lane = c.lane;
-  uint8_t* ring_warp = ring + c.warp * 32 * LB;
-  const Ring rg(c, ring);
-  const int nsb = rg.nsb, rounds = rg.rounds;
-  auto krow = [&](int kr) { return Ring::krow(c, kr); };
-  auto orow = [&](int s) { return Ring::orow(c, s); };
-  const uint64_t last_use = l2_evict_first();
-  const float2 inv2 = make_float2(c.inv, c.inv), decay2 = make_float2(c.decay, c.decay);
-  const int* poff = rg.poff;
-
-#pragma unroll
-  for (int r = 0; r < S; ++r) rg.issue(c, r, last_use);
-
-  auto process = [&](int r, const uint8_t* st) {
-    const int sb = r * NW + c.warp;
-    if (r >= rounds || sb >= nsb) return;
-    const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
-    // B fragments: b[kk][q] = rows (2 t4, 2 t4 + 1) and (2 t4 + 8, 2 t4 + 9) of column jm + q
-    uint32_t b[MT][4][2];
-#pragma unroll
-    for (int kk = 0; kk < MT; ++kk) {
-      const bool half = HALF && kk == MT - 1;
-      float v[4][4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (half && e >= 2) {
-          v[e][0] = v[e][1] = v[e][2] = v[e][3] = 0.f;
-          continue;
-        }
-        if (c.vec) {
-          const float4 t = *reinterpret_cast<const float4*>(st + (4 * kk + e) * 512 + lane * 16);
-          v[e][0] = t.x; v[e][1] = t.y; v[e][2] = t.z; v[e][3] = t.w;
-        } else {
-          const int i = krow(4 * kk + e);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v[e][q] = (i < c.m && jm + q < c.n) ? c.Mp[c.wd.off(i, jm + q)] : 0.f;
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 lo = __fmul2_rn(make_float2(v[0][q], v[1][q]), inv2);
-        b[kk][q][0] = Mma<TY>::pack(lo.x, lo.y);
-        if (half) {
-          b[kk][q][1] = 0u;
-        } else {
-          const float2 hi = __fmul2_rn(make_float2(v[2][q], v[3][q]), inv2);
-          b[kk][q][1] = Mma<TY>::pack(hi.x, hi.y);
-        }
-      }
-    }
-#pragma unroll
-    for (int mi = 0; mi < MT; ++mi) {
-      float d[4][4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < MT; ++kk) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (HALF && kk == MT - 1) {  // rows 8..15 of this k-tile are padding
-            Mma<TY>::run8(d[q], ph[mi][kk], b[kk][q][0]);
-            Mma<TY>::run8(d[q], pl[mi][kk], b[kk][q][0]);
-          } else {
-            Mma<TY>::run(d[q], ph[mi][kk], b[kk][q][0], b[kk][q][1]);
-            Mma<TY>::run(d[q], pl[mi][kk], b[kk][q][0], b[kk][q][1]);
-          }
-        }
-      }
-      // rows 16 mi + g (h = 0) and 16 mi + g + 8 (h = 1), columns jp .. jp + 7
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (HALF && mi == MT - 1 && h == 1) continue;
-        const int s = 2 * mi + h;
-        const int i = orow(s);
-        if (i >= c.m || jp >= c.n) continue;
-        const float o[8] = {d[0][2 * h], d[1][2 * h], d[2][2 * h], d[3][2 * h],
-                            d[0][2 * h + 1], d[1][2 * h + 1], d[2][2 * h + 1], d[3][2 * h + 1]};
-        const float coef = c.coef * rs[s], oscale = c.inv_alpha * rs[s];  // row scale of Pi undone
-        if (c.vec) {
-          const uint4 praw = *reinterpret_cast<const uint4*>(st + (KR + s) * 512 + lane * 16);
-          float pf[8];
-          bf16x8_to_f32(praw, pf);
-          const float2 nc2 = make_float2(-coef, -coef);
-          float w[8];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float2 wv = __ffma2_rn(nc2, make_float2(o[e], o[e + 1]),
-                                         __fmul2_rn(make_float2(pf[e], pf[e + 1]), decay2));
-            w[e] = wv.x;
-            w[e + 1] = wv.y;
-          }
-          const int off = poff[s] + jp;
-          *reinterpret_cast<uint4*>(c.P + off) = f32_to_bf16x8(w);
-          if (c.dbg) {
-            float* dp = c.dbg + off;
-            *reinterpret_cast<float4*>(dp) =
-                make_float4(o[0] * oscale, o[1] * oscale, o[2] * oscale, o[3] * oscale);
-            *reinterpret_cast<float4*>(dp + 4) =
-                make_float4(o[4] * oscale, o[5] * oscale, o[6] * oscale, o[7] * oscale);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (jp + e >= c.n) continue;
-            const int64_t off = c.wd.off(i, jp + e);
-            c.P[off] = __float2bfloat16_rn(fmaf(-coef, o[e], __bfloat162float(c.P[off]) * c.decay));
-            if (c.dbg) c.dbg[off] = o[e] * oscale;
-          }
-        }
-      }
-    }
-  };
-
-  for (int r = 0; r < rounds; ++r) {
-    cp_async_wait<S - 1>();
-    uint8_t* st = ring_warp + Ring::slot(r) * kSlot;
-    process(r, st);
-    // round r now lives in registers / is written: refill its slot
-    rg.issue(c, r + S, last_use);
-  }
-  cp_async_wait<0>();
-}
-
-// An m x m fp32 matrix kept as two tf32 parts, x = hi + lo (both exact
-// tf32 values, pitch LD), so that the tensor-core products below read their
-// operands already split.
-struct SplitMat {
-  uint32_t* hi;
-  uint32_t* lo;
-};
-template <int LD>
-__device__ __forceinline__ void put(const SplitMat& X, int i, int j, float v) {
-  const uint32_t h = to_tf32(v);
-  X.hi[i * LD + j] = h;
-  X.lo[i * LD + j] = to_tf32(v - __uint_as_float(h));
-}
-template <int LD>
-__device__ __forceinline__ float get(const SplitMat& X, int i, int j) {
-  return __uint_as_float(X.hi[i * LD + j]) + __uint_as_float(X.lo[i * LD + j]);
-}
-
-// One m16 x n8 tile of C = X Y (MP x MP, zero beyond m), on the tensor cores
-// with the 3xTF32 split: x y ~ x_hi y_hi + x_hi y_lo + x_lo y_hi (the dropped
-// x_lo y_lo is ~2^-22 relative).  k8 steps beyond m (ks of them are live)
-// are skipped.  d[0..3] = C at rows 16 mi + g (+ 8), columns 8 nj + 2 t4
-// (+ 1).
-template <int MP, int LD>
-__device__ __forceinline__ void mm_tile(const SplitMat& X, const SplitMat& Y, int tile, int ks, int g,
-                                        int t4, float (&d)[4]) {
-  const int mi = tile / (MP / 8), nj = tile % (MP / 8);
-  // one accumulator per k8 step: independent chains of three products,
-  // summed in a fixed order at the end (the stage is latency-bound)
-  float acc[MP / 8][4];
-#pragma unroll
-  for (int kk = 0; kk < MP / 8; ++kk) {
-    acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
-    if (kk < ks) {
-      const int xo = (mi * 16 + g) * LD + kk * 8 + t4;
-      const int yo = (kk * 8 + t4) * LD + nj * 8 + g;
-      const uint32_t ah0 = X.hi[xo], ah1 = X.hi[xo + 8 * LD], ah2 = X.hi[xo + 4], ah3 = X.hi[xo + 8 * LD + 4];
-      const uint32_t al0 = X.lo[xo], al1 = X.lo[xo + 8 * LD], al2 = X.lo[xo + 4], al3 = X.lo[xo + 8 * LD + 4];
-      const uint32_t bh0 = Y.hi[yo], bh1 = Y.hi[yo + 4 * LD], bl0 = Y.lo[yo], bl1 = Y.lo[yo + 4 * LD];
-      mma_tf32(acc[kk], al0, al1, al2, al3, bh0, bh1);
-      mma_tf32(acc[kk], ah0, ah1, ah2, ah3, bl0, bl1);
-      mma_tf32(acc[kk], ah0, ah1, ah2, ah3, bh0, bh1);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float v = acc[0][q];
-#pragma unroll
-    for (int kk = 1; kk < MP / 8; ++kk) v += acc[kk][q];
-    d[q] = v;
-  }
-}
-
-// The m x m stage in plain fp32 (FFMA), for m > 32.  Every left operand there (A, Q and
-// Q^2) is symmetric, so C = X Y is formed as C[i][j] = sum_k X[k][i] Y[k][j]:
-// both operands read by rows, k ascending, one fixed order per element.
-// Thread t < 256 owns the RI x CJ block at rows RI (t / BJ) + r, columns
-// CJ (t % BJ) + c.
-template <int MP, int NT>
-struct MmBlk {
-  static constexpr int RI = MP / 16, CJ = RI;
-  static constexpr int BI = MP / RI, BJ = MP / CJ;
-  static_assert(BI * BJ <= NT, "one block per thread");
-};
-
-template <int N>
-__device__ __forceinline__ void lds_run(const float* p, float (&v)[N]) {
-  if constexpr (N == 4) {
-    const float4 t = *reinterpret_cast<const float4*>(p);
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-  } else if constexpr (N == 2) {
-    const float2 t = *reinterpret_cast<const float2*>(p);
-    v[0] = t.x; v[1] = t.y;
-  } else {
-#pragma unroll
-    for (int e = 0; e < N; ++e) v[e] = p[e];
-  }
-}
-
-// acc[y] = this thread's block of X^T Y_y over k < m, for NY right operands
-// sharing the left one.
-template <int LD, int RI, int CJ, int NY>
-__device__ __forceinline__ void mm_blk(const float* X, const float* const (&Y)[NY], int m, int i0, int j0,
-                                       float (&acc)[NY][RI][CJ]) {
-#pragma unroll
-  for (int y = 0; y < NY; ++y)
-#pragma unroll
-    for (int r = 0; r < RI; ++r)
-#pragma unroll
-      for (int c = 0; c < CJ; ++c) acc[y][r][c] = 0.f;
-#pragma unroll 2
-  for (int k = 0; k < m; ++k) {
-    float x[RI];
-    lds_run<RI>(X + k * LD + i0, x);
-#pragma unroll
-    for (int y = 0; y < NY; ++y) {
-      float v[CJ];
-      lds_run<CJ>(Y[y] + k * LD + j0, v);
-#pragma unroll
-      for (int r = 0; r < RI; ++r) {
-        if constexpr (CJ % 2 == 0) {
-#pragma unroll
-          for (int c = 0; c < CJ; c += 2) {
-            const float2 t = __ffma2_rn(make_float2(x[r], x[r]), make_float2(v[c], v[c + 1]),
-                                        make_float2(acc[y][r][c], acc[y][r][c + 1]));
-            acc[y][r][c] = t.x;
-            acc[y][r][c + 1] = t.y;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < CJ; ++c) acc[y][r][c] = fmaf(x[r], v[c], acc[y][r][c]);
-        }
-      }
-    }
-  }
-}
-
-// The m x m work arrays A, Q, T, Pi (two): matrix k at base, either split
-// into tf32 high / low parts (tensor-core form, m <= 32) or plain fp32.
-template <int MP, int LD, bool TC>
-struct MmMats {
-  uint32_t* base;
-  static constexpr int kWords = (TC ? 10 : 5) * MP * LD;
-  __device__ __forceinline__ SplitMat split(int k) const {
-    return SplitMat{base + (2 * k) * MP * LD, base + (2 * k + 1) * MP * LD};
-  }
-  __device__ __forceinline__ float* plain(int k) const { return reinterpret_cast<float*>(base) + k * MP * LD; }
-  __device__ __forceinline__ float get(int k, int i, int j) const {
-    if constexpr (TC) return ::muon::get<LD>(split(k), i, j);
-    else return plain(k)[i * LD + j];
-  }
-  __device__ __forceinline__ void put(int k, int i, int j, float v) const {
-    if constexpr (TC) ::muon::put<LD>(split(k), i, j, v);
-    else plain(k)[i * LD + j] = v;
-  }
-};
-
-template <typename TY, int MT, int NT, bool HALF>
-__global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
-  using L = GsLayout<MT, NT, HALF>;
-  using GT = typename L::GT;
-  constexpr int MP = L::MP, LD = L::LD, NW = L::NW;
-  extern __shared__ __align__(128) uint8_t smem[];
-  float* cpart = reinterpret_cast<float*>(smem + L::kCta);
-  float* misc = reinterpret_cast<float*>(smem + L::kMisc);
-  float* rsc = reinterpret_cast<float*>(smem + L::kRsc);         // per-row power-of-two scale of Pi
-  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + L::kTabOff);  // upper triangle (i << 16 | j)
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t rank = cluster_rank();
-  const int b = blockIdx.x / kCL;
-  const int m = a.m;
-  const MemberPtrs mp = a.mem[b];
-
-  GsCtx c;
-  c.lane = lane; c.warp = warp; c.g = lane >> 2; c.t4 = lane & 3;
-  c.m = m; c.n = a.n; c.c0 = (int)rank * W; c.NB = NB;
-  c.Mp = mp.M;
-  c.G = static_cast<const __nv_bfloat16*>(mp.G);
-  c.P = static_cast<__nv_bfloat16*>(mp.P);
-  c.cols = a.cols;
-  c.wd = Wide{a.cols, a.T};
-  c.vec = !a.T && (a.cols % 8 == 0) && 32ll * a.cols < (1ll << 31) && aligned16(c.Mp) &&
-          aligned16(c.G) && aligned16(c.P);
-  c.dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
-  const int ns = a.sc->ns_steps;
-  c.beta = a.sc->beta;
-  const float lr = a.sc->lr;
-  c.decay = 1.f - lr * a.sc->wd;
-  c.inv_alpha = 1.f / a.alpha;
-  c.coef = lr * a.scale * c.inv_alpha;
-
-  // m x m work arrays (aliasing the ring between the two passes)
-  float* wpart = reinterpret_cast<float*>(smem);
-  float* wss = wpart + NW * GT::N * 128;
-  using Mats = MmMats<MP, LD, L::TC>;
-  const Mats mats{reinterpret_cast<uint32_t*>(smem)};
-  TY* Ph = reinterpret_cast<TY*>(smem + Mats::kWords * 4);
-  TY* Pl = Ph + MP * (MP + 8);
-  int ip = 3;  // matrix index of the final Pi (3 or 4)
-  const int nup = m * (m + 1) / 2;
-  for (int e = tid; e < nup; e += NT) {
-    // e -> (i, j), i <= j, row-major over the upper triangle
-    int i = 0, rem = e;
-    while (rem >= m - i) { rem -= m - i; ++i; }
-    tab[e] = (uint32_t)(i << 16 | (i + rem));
-  }
-
-  // 1. momentum, sum of squares and Gram matrix
-  float gacc[GT::N][4];
-#pragma unroll
-  for (int q = 0; q < GT::N; ++q) gacc[q][0] = gacc[q][1] = gacc[q][2] = gacc[q][3] = 0.f;
-  float ss = 0.f;
-  gs_momentum_pass<MT, NT, HALF>(c, smem, gacc, ss);
-  // Hint: move this CTA's slice of P into L2 while the m x m work runs.
-  if (c.vec && warp == NW - 1 && c.c0 < c.n) {
-    const int ncol = min(W, c.n - c.c0);
-    const uint32_t bytes = (uint32_t)(ncol * 2) & ~15u;
-    if (bytes)
-      for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * a.cols + c.c0, bytes);
-  }
-  __syncthreads();  // every warp's ring is drained before it is reused
-  // per-warp partials, then warps summed in a fixed order into this CTA's partial
-  ss = warp_sum(ss);
-  if (lane == 0) wss[warp] = ss;
-#pragma unroll
-  for (int q = 0; q < GT::N; ++q) {
-    float* dst = wpart + (warp * GT::N + q) * 128;
-    dst[c.g * 8 + 2 * c.t4] = gacc[q][0];
-    dst[c.g * 8 + 2 * c.t4 + 1] = gacc[q][1];
-    dst[(c.g + 8) * 8 + 2 * c.t4] = gacc[q][2];
-    dst[(c.g + 8) * 8 + 2 * c.t4 + 1] = gacc[q][3];
-  }
-  __syncthreads();
-  for (int e = tid; e < GT::N * 128; e += NT) {
-    const int q = e >> 7, w = e & 127;
-    float acc = 0.f;
-    for (int k = 0; k < NW; ++k) acc += wpart[(k * GT::N + q) * 128 + w];
-    const int code = GT::code(q);
-    cpart[((code >> 4) * 16 + (w >> 3)) * MP + (code & 15) * 8 + (w & 7)] = acc;
-  }
-  if (tid == 0) {
-    float acc = 0.f;
-    for (int k = 0; k < NW; ++k) acc += wss[k];
-    misc[0] = acc;
-  }
-  cluster_sync();  // (also a CTA barrier: the partials are consumed)
-  for (int e = tid; e < Mats::kWords; e += NT) mats.base[e] = 0u;  // m x m arrays, padding included
-  __syncthreads();
-  // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: CTAs summed in rank order
-  float ssum = 0.f;
-#pragma unroll
-  for (int r = 0; r < kCL; ++r) ssum += ld_dsmem_f32(&misc[0], (uint32_t)r);
-  const float inv_raw = 1.f / (sqrtf(ssum) + a.eps);
-  c.inv = a.alpha * inv_raw;
-  const float inv2 = inv_raw * inv_raw;
-  for (int e = tid; e < nup; e += NT) {
-    const int i = tab[e] >> 16, j = tab[e] & 0xffff;
-    float acc = 0.f;
-#pragma unroll
-    for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
-    acc *= inv2;
-    mats.put(0, i, j, acc);
-    mats.put(0, j, i, acc);
-  }
-  cluster_arrive();  // done reading the peer's partials
-  __syncthreads();
-
-  // 2. the k steps in m x m space: for m <= 32 m16 x n8 tiles dealt to the
-  // warps on the tensor cores (3xTF32; the stage is latency-bound there),
-  // else fp32 FFMA blocks, one per thread (throughput-bound)
-  if (ns > 0) {
-    if constexpr (L::TC) {
-      constexpr int TPP = (MP / 16) * (MP / 8);  // tiles of one product
-      SplitMat Am = mats.split(0), Qm = mats.split(1), Tm = mats.split(2), Pi0 = mats.split(3);
-      SplitMat Pi1 = mats.split(4), Pi = Pi0;
-      const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
-      const int ks = (m + 7) / 8;  // live k8 steps
-      // a tile wholly beyond m (rows or columns) stays zero and is skipped
-      auto live = [&](int tile) { return (tile / (MP / 8)) * 16 < m && (tile % (MP / 8)) * 8 < m; };
-      // element (i, j) of this lane's accumulator slot q in tile `tile`
-      auto at = [&](int tile, int q, int& i, int& j) {
-        i = (tile / (MP / 8)) * 16 + c.g + ((q & 2) ? 8 : 0);
-        j = (tile % (MP / 8)) * 8 + 2 * c.t4 + (q & 1);
-      };
-      for (int s = 0; s < ns; ++s) {
-        const bool more = s + 1 < ns;
-        // Q = a I + b A + c A^2 (zero outside m x m)
-        for (int tile = warp; tile < TPP; tile += NW) {
-          if (!live(tile)) continue;
-          float d[4];
-          mm_tile<MP, LD>(Am, Am, tile, ks, c.g, c.t4, d);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            int i, j;
-            at(tile, q, i, j);
-            float v = 0.f;
-            if (i < m && j < m) v = fmaf(cc, d[q], fmaf(cb, get<LD>(Am, i, j), i == j ? ca : 0.f));
-            put<LD>(Qm, i, j, v);
-          }
-        }
-        __syncthreads();
-        // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
-        SplitMat Pn = Pi.hi == Pi0.hi ? Pi1 : Pi0;
-        for (int t = warp; t < 2 * TPP; t += NW) {
-          if (t < TPP) {
-            if (!more || !live(t)) continue;
-            float d[4];
-            mm_tile<MP, LD>(Qm, Qm, t, ks, c.g, c.t4, d);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              int i, j;
-              at(t, q, i, j);
-              put<LD>(Tm, i, j, d[q]);
-            }
-            continue;
-          }
-          const int tile = t - TPP;
-          if (!live(tile)) continue;
-          float d[4];
-          if (s > 0) mm_tile<MP, LD>(Qm, Pi, tile, ks, c.g, c.t4, d);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            int i, j;
-            at(tile, q, i, j);
-            if (s > 0) {
-              put<LD>(Pn, i, j, d[q]);
-            } else {
-              Pn.hi[i * LD + j] = Qm.hi[i * LD + j];
-              Pn.lo[i * LD + j] = Qm.lo[i * LD + j];
-            }
-          }
-        }
-        Pi = Pn;
-        __syncthreads();
-        if (more) {
-          // A <- Q^2 A (written over Q, then the two swap roles)
-          for (int tile = warp; tile < TPP; tile += NW) {
-            if (!live(tile)) continue;
-            float d[4];
-            mm_tile<MP, LD>(Tm, Am, tile, ks, c.g, c.t4, d);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              int i, j;
-              at(tile, q, i, j);
-              put<LD>(Qm, i, j, d[q]);
-            }
-          }
-          const SplitMat t = Am; Am = Qm; Qm = t;
-          __syncthreads();
-        }
-      }
-      ip = Pi.hi == Pi0.hi ? 3 : 4;
-    } else {
-      using B = MmBlk<MP, NT>;
-      constexpr int RI = B::RI, CJ = B::CJ;
-      const float ca = a.sc->a, cb = a.sc->b, cc = a.sc->c;
-      const int i0 = RI * (tid / B::BJ), j0 = CJ * (tid % B::BJ);
-      const bool own = tid < B::BI * B::BJ;
-      // this thread's block into C, zero outside m x m
-      auto store = [&](float* C, const float (&v)[RI][CJ]) {
-#pragma unroll
-        for (int r = 0; r < RI; ++r)
-#pragma unroll
-          for (int q = 0; q < CJ; ++q) {
-            const int i = i0 + r, j = j0 + q;
-            C[i * LD + j] = (i < m && j < m) ? v[r][q] : 0.f;
-          }
-      };
-      float *Am = mats.plain(0), *Qm = mats.plain(1), *Tm = mats.plain(2);
-      float *Pi0 = mats.plain(3), *Pi1 = mats.plain(4), *Pi = Pi0;
-      for (int s = 0; s < ns; ++s) {
-        const bool more = s + 1 < ns;
-        // Q = a I + b A + c A^2
-        if (own) {
-          float acc[1][RI][CJ];
-          mm_blk<LD, RI, CJ, 1>(Am, {Am}, m, i0, j0, acc);
-#pragma unroll
-          for (int r = 0; r < RI; ++r)
-#pragma unroll
-            for (int q = 0; q < CJ; ++q) {
-              const int i = i0 + r, j = j0 + q;
-              acc[0][r][q] = fmaf(cc, acc[0][r][q], fmaf(cb, Am[i * LD + j], i == j ? ca : 0.f));
-            }
-          store(Qm, acc[0]);
-        }
-        __syncthreads();
-        // Pi <- Q Pi (Pi_1 = Q_0) and T = Q^2 (needed for the next A)
-        float* Pn = Pi == Pi0 ? Pi1 : Pi0;
-        if (own) {
-          if (s > 0 && more) {
-            float acc[2][RI][CJ];
-            mm_blk<LD, RI, CJ, 2>(Qm, {Qm, Pi}, m, i0, j0, acc);
-            store(Tm, acc[0]);
-            store(Pn, acc[1]);
-          } else if (s > 0) {
-            float acc[1][RI][CJ];
-            mm_blk<LD, RI, CJ, 1>(Qm, {Pi}, m, i0, j0, acc);
-            store(Pn, acc[0]);
-          } else {
-            if (more) {
-              float acc[1][RI][CJ];
-              mm_blk<LD, RI, CJ, 1>(Qm, {Qm}, m, i0, j0, acc);
-              store(Tm, acc[0]);
-            }
-#pragma unroll
-            for (int r = 0; r < RI; ++r)
-#pragma unroll
-              for (int q = 0; q < CJ; ++q) Pn[(i0 + r) * LD + j0 + q] = Qm[(i0 + r) * LD + j0 + q];
-          }
-        }
-        Pi = Pn;
-        __syncthreads();
-        if (more) {
-          // A <- Q^2 A (written over Q, then the two swap roles)
-          if (own) {
-            float acc[1][RI][CJ];
-            mm_blk<LD, RI, CJ, 1>(Tm, {Am}, m, i0, j0, acc);
-            store(Qm, acc[0]);
-          }
-          float* t = Am; Am = Qm; Qm = t;
-          __syncthreads();
-        }
-      }
-      ip = Pi == Pi0 ? 3 : 4;
-    }
-    // Along an exact null direction of X_0 (a zero row, say) Pi grows like
-    // a^k while O does not: scale each row i of Pi by 2^-e_i into the operand
-    // type's range, and O's row i by 2^e_i in the epilogue.
-    for (int i = warp; i < MP; i += NW) {  // one warp per row: lanes over columns
-      float mx = 0.f;
-      for (int k = lane; k < m && i < m; k += 32) mx = fmaxf(mx, fabsf(mats.get(ip, i, k)));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const int ex = mx >= 32768.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
-      if (lane == 0) rsc[i] = exp2f((float)ex);
-    }
-    __syncthreads();
-    // Pi in the operand type: high part and residual, zero outside m x m
-    for (int e = tid; e < MP * MP; e += NT) {
-      const int i = e / MP, j = e - (e / MP) * MP;
-      float v = 0.f;
-      if (i < m && j < m) v = mats.get(ip, i, j) / rsc[i];
-      const TY hi = from_f32<TY>(v);
-      Ph[i * (MP + 8) + j] = hi;
-      Pl[i * (MP + 8) + j] = from_f32<TY>(v - to_f32(hi));
-    }
-  } else {
-    // no step: O = X_0 (Pi = I, exact in the operand type)
-    for (int i = tid; i < MP; i += NT) rsc[i] = 1.f;
-    for (int e = tid; e < MP * MP; e += NT) {
-      const int i = e / MP, j = e - (e / MP) * MP;
-      Ph[i * (MP + 8) + j] = from_f32<TY>(i == j && i < m ? 1.f : 0.f);
-      Pl[i * (MP + 8) + j] = from_f32<TY>(0.f);
-    }
-  }
-  __syncthreads();
-  uint32_t ph[MT][MT][4], pl[MT][MT][4];
-  {
-    const uint32_t hb = smem_u32(Ph), lb = smem_u32(Pl);
-#pragma unroll
-    for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-      for (int kk = 0; kk < MT; ++kk) {
-        const uint32_t o = 2u * ((mi * 16 + (lane & 15)) * (MP + 8) + kk * 16 + (lane >> 4) * 8);
-        ldsm_x4(hb + o, ph[mi][kk]);
-        ldsm_x4(lb + o, pl[mi][kk]);
-      }
-  }
-  float rs[L::R];
-#pragma unroll
-  for (int s = 0; s < L::R; ++s) rs[s] = rsc[(s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0)];
-  __syncthreads();  // the ring's bytes are reused by the output pass
-
-  // 3. O = Pi_k Y_0 and the parameter write
-  gs_out_pass<TY, MT, NT, HALF>(c, smem, ph, pl, rs);
-  cluster_wait();  // the peer may still read this CTA's partials
-}
-
-// Threads per CTA: 16 warps up to m = 32; beyond, 8 warps, each with the
-// registers for Pi's fragments of all 16-row tiles.
-template <int MT>
-constexpr int gs_threads() { return MT <= 2 ? 512 : 256; }
-
-template <typename TY, int MT, bool HALF>
-cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
-  constexpr int NT = gs_threads<MT>();
-  auto fn = k_skinny_gs<TY, MT, NT, HALF>;
-  constexpr int smem = GsLayout<MT, NT, HALF>::kTotal;
-  if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(a.B * kCL);
-  lc.blockDim = dim3(NT);
-  lc.dynamicSmemBytes = smem;
-  lc.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, fn, a, (int)cfg.width, (int)(cfg.width / 16));
-}
-
-template <typename TY, int MT, bool HALF>
-int gs_clusters_of() {
-  constexpr int NT = gs_threads<MT>();
-  auto fn = k_skinny_gs<TY, MT, NT, HALF>;
-  cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(kCL * 1024);
-  lc.blockDim = dim3(NT);
-  lc.dynamicSmemBytes = GsLayout<MT, NT, HALF>::kTotal;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  int n = 0;
-  return cudaOccupancyMaxActiveClusters(&n, fn, &lc) == cudaSuccess ? n : -1;
-}
-
-// HALF (a last 16-row tile of at most 8 rows, stored as half a tile) is
-// instantiated up to m = 32; beyond, such a tile is padded to 16 rows.
-template <typename TY>
-cudaError_t gs_launch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
-  const bool half = a.m - 16 * (cfg.mtiles - 1) <= 8;
-  switch (cfg.mtiles) {
-    case 1: return half ? launch_gs_t<TY, 1, true>(a, cfg, st, prep) : launch_gs_t<TY, 1, false>(a, cfg, st, prep);
-    case 2: return half ? launch_gs_t<TY, 2, true>(a, cfg, st, prep) : launch_gs_t<TY, 2, false>(a, cfg, st, prep);
-    case 3: return launch_gs_t<TY, 3, false>(a, cfg, st, prep);
-    default: return launch_gs_t<TY, 4, false>(a, cfg, st, prep);
-  }
-}
-
-template <typename TY>
-int gs_clusters_ty(int m) {
-  const int mt = (m + 15) / 16;
-  const bool half = m - 16 * (mt - 1) <= 8;
-  switch (mt) {
-    case 1: return half ? gs_clusters_of<TY, 1, true>() : gs_clusters_of<TY, 1, false>();
-    case 2: return half ? gs_clusters_of<TY, 2, true>() : gs_clusters_of<TY, 2, false>();
-    case 3: return gs_clusters_of<TY, 3, false>();
-    default: return gs_clusters_of<TY, 4, false>();
-  }
-}
-
-}  // namespace
+cudaError_t gs_dispatch_nesterov(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare);
+int gs_max_active_clusters_nesterov(int ns_type, int m);
 
 cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare) {
-  if (a.mode_f32 || cfg.mtiles < 1 || cfg.mtiles > 4) return cudaErrorInvalidValue;
-  return a.ns_type == NS_F16 ? gs_launch_ty<__half>(a, cfg, s, prepare)
-                             : gs_launch_ty<__nv_bfloat16>(a, cfg, s, prepare);
+  if (prepare) {  // both settings, so that either may run
+    const cudaError_t e = gs::gs_dispatch_t<false>(a, cfg, s, true);
+    return e != cudaSuccess ? e : gs_dispatch_nesterov(a, cfg, s, true);
+  }
+  return a.nesterov ? gs_dispatch_nesterov(a, cfg, s, false) : gs::gs_dispatch_t<false>(a, cfg, s, false);
 }
 
 int gs_max_active_clusters(int ns_type, int m) {
-  if (m < 1 || m > 64) return -1;
-  return ns_type == NS_F16 ? gs_clusters_ty<__half>(m) : gs_clusters_ty<__nv_bfloat16>(m);
+  const int p = gs::gs_clusters_t<false>(ns_type, m), q = gs_max_active_clusters_nesterov(ns_type, m);
+  return p < q ? p : q;
 }
 
 }  // namespace muon

@@ -39,6 +39,7 @@ struct TcArgs {
   void* C;
   const void* aux;        // POLY: the A matrix (same layout as C)
   const StepScalars* sc;
+  int step;               // POLY: Newton-Schulz step (schedule row)
   float scale;            // GRAM: 1 / alpha^2
   int* err;
 };
@@ -253,7 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
     float ca = 0.f, cb = 0.f, cc = 0.f;
-    if (OP == TC_POLY) { ca = p.sc->a; cb = p.sc->b; cc = p.sc->c; }
+    if (OP == TC_POLY) {
+      const float* cf = step_coef(p.sc, p.step);
+      ca = cf[0]; cb = cf[1]; cc = cf[2];
+    }
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -452,8 +456,9 @@ cudaError_t launch_tc_gram(const KArgs& a, const TcMaps& t, int src, cudaStream_
   return run_bn<TC_GRAM>(t.bn_sq, a.ns_type, t.y_k128[src], t.y_ksq[src], p, s, false);
 }
 
-cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, cudaStream_t s) {
+cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, int step, cudaStream_t s) {
   TcArgs p = base_args(a);
+  p.step = step;
   p.M = a.m; p.N = a.m; p.K = a.m;
   p.tiles_m = (a.m + BM - 1) / BM;
   p.tiles_n = (a.m + t.bn_sq - 1) / t.bn_sq;

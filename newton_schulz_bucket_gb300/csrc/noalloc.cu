@@ -145,7 +145,11 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
   k.y0 = base + off_ws;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const StepScalars hs{beta, lr, wd, a, b, c, ns_steps, 0};
+  StepScalars hs{};
+  hs.beta = beta; hs.lr = lr; hs.wd = wd;
+  hs.ns_steps = ns_steps;
+  hs.n_coef = 1;
+  hs.coef[0][0] = a; hs.coef[0][1] = b; hs.coef[0][2] = c;
   k_static_setup<<<1, 32, 0, s>>>(hs, params, grads, momenta, batch, rows * cols, sc, mem);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_skinny(k, cfg, ns_steps, s);

@@ -62,6 +62,7 @@ struct GroupPlan {
   SkinnyCfg sk{};
   TcMaps tc{};          // TENSOR path: TMA descriptors of the workspace
   size_t off_y0 = 0, off_y1 = 0, off_a = 0, off_q = 0, off_part = 0, off_invn = 0, off_dbg = 0;
+  size_t off_u = 0;  // skinny groups under Nesterov: U for the direct kernel (0: none)
   size_t ws_bytes = 0;  // this group's scratch (from the group base)
   size_t base = 0;      // offset of the group's scratch in the plan workspace
   double cost = 0;      // flops-ish estimate, for stream assignment
@@ -99,7 +100,7 @@ muon_status_t check_options(const muon_plan_options& o) {
   if (o.skinny_threshold < -1 || o.skinny_threshold > 64)
     return fail(MUON_ERR_INVALID_ARG, "skinny_threshold must be in [-1, 64]");
   if (o.flags & ~(MUON_FLAG_KEEP_UPDATE | MUON_FLAG_NO_GRAPH | MUON_FLAG_HOST_STAGING |
-                  MUON_FLAG_GROUP_TIMING))
+                  MUON_FLAG_GROUP_TIMING | MUON_FLAG_NESTEROV))
     return fail(MUON_ERR_INVALID_ARG, "unknown flag bits 0x%x", o.flags);
   for (int i = 0; i < 8; ++i)
     if (o.reserved[i] != 0) return fail(MUON_ERR_INVALID_ARG, "reserved option fields must be 0");
@@ -208,6 +209,9 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
     if (path == PATH_SKINNY) {
       gp.off_y0 = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.sk.ws_bytes, kAlign);
       gp.off_part = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.n_chunks * 4, kAlign);
+      if (o.flags & MUON_FLAG_NESTEROV) {  // read only by the direct kernel (k > kGramSpaceMaxSteps)
+        gp.off_u = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.rows * gp.cols * 4, kAlign);
+      }
     } else {
       const size_t es = ns_esize(gp.ns_type);
       const size_t yb = (size_t)gp.batch * gp.m * gp.n_pitch * es;
@@ -298,6 +302,8 @@ KArgs make_args(const muon_plan_s* p, const GroupPlan& g) {
                                                    : nullptr;
   a.err = reinterpret_cast<int*>(p->ws + p->d.off_err);
   a.l2_keep_m = g.path == PATH_SKINNY;
+  a.nesterov = (p->d.opt.flags & MUON_FLAG_NESTEROV) ? 1 : 0;
+  a.u = (g.path == PATH_SKINNY && a.nesterov) ? reinterpret_cast<float*>(base + g.off_u) : nullptr;
   return a;
 }
 
@@ -314,7 +320,7 @@ cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int3
     int src = 0;
     for (int32_t it = 0; it < k; ++it) {
       if ((e = launch_tc_gram(a, g.tc, src, s))) return e;
-      if ((e = launch_tc_poly(a, g.tc, s))) return e;
+      if ((e = launch_tc_poly(a, g.tc, it, s))) return e;
       if ((e = launch_tc_update(a, g.tc, src, s))) return e;
       src ^= 1;
     }
@@ -324,7 +330,7 @@ cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int3
   void* yd = a.y1;
   for (int32_t it = 0; it < k; ++it) {
     if ((e = launch_simt_gram(a, ys, s))) return e;
-    if ((e = launch_simt_poly(a, s))) return e;
+    if ((e = launch_simt_poly(a, it, s))) return e;
     if ((e = launch_simt_update(a, ys, yd, s))) return e;
     std::swap(ys, yd);
   }
@@ -599,16 +605,25 @@ muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
   return MUON_OK;
 }
 
-muon_status_t muon_step(muon_plan_t p, void* const* params, const void* const* grads,
+namespace {
+
+// The one step of muon_step and muon_step_schedule: `coef` holds n_coef
+// (a, b, c) rows (host memory).
+muon_status_t step_impl(muon_plan_t p, void* const* params, const void* const* grads,
                         float* const* momenta, float beta, float lr, float wd, int32_t ns_steps,
-                        float a, float b, float c, void* stream) {
+                        const float* coef, int32_t n_coef, void* stream) {
   if (!p) return fail(MUON_ERR_INVALID_ARG, "plan is NULL");
   if (!params || !grads || !momenta) return fail(MUON_ERR_INVALID_ARG, "NULL pointer array");
   if (ns_steps < 0 || ns_steps > 1000)
     return fail(MUON_ERR_INVALID_ARG, "ns_steps %d out of [0, 1000]", ns_steps);
-  const float sc[6] = {beta, lr, wd, a, b, c};
+  if (!coef) return fail(MUON_ERR_INVALID_ARG, "coefficient schedule is NULL");
+  if (n_coef < 1 || n_coef > kMaxScheduleRows)
+    return fail(MUON_ERR_INVALID_ARG, "schedule rows %d out of [1, %d]", n_coef, kMaxScheduleRows);
+  const float sc[3] = {beta, lr, wd};
   for (float v : sc)
     if (!std::isfinite(v)) return fail(MUON_ERR_INVALID_ARG, "non-finite step scalar");
+  for (int32_t i = 0; i < 3 * n_coef; ++i)
+    if (!std::isfinite(coef[i])) return fail(MUON_ERR_INVALID_ARG, "non-finite coefficient");
   const int32_t np = (int32_t)p->d.param_E.size();
   for (int32_t i = 0; i < np; ++i)
     if (!params[i] || !grads[i] || !momenta[i])
@@ -620,7 +635,11 @@ muon_status_t muon_step(muon_plan_t p, void* const* params, const void* const* g
   p->slot = (p->slot + 1) % kRingSlots;
   CUDA_TRY(cudaEventSynchronize(p->slot_ev[slot]));
   unsigned char* host = p->pinned + (size_t)slot * p->d.pb_bytes;
-  StepScalars ss{beta, lr, wd, a, b, c, ns_steps, 0};
+  StepScalars ss{};
+  ss.beta = beta; ss.lr = lr; ss.wd = wd;
+  ss.ns_steps = ns_steps;
+  ss.n_coef = n_coef;
+  std::memcpy(ss.coef, coef, sizeof(float) * 3 * (size_t)n_coef);
   std::memcpy(host, &ss, sizeof ss);
   MemberPtrs* mp = reinterpret_cast<MemberPtrs*>(host + align_up(sizeof(StepScalars), 16));
   const size_t pes = p_esize(p);
@@ -646,6 +665,22 @@ muon_status_t muon_step(muon_plan_t p, void* const* params, const void* const* g
   if (muon_status_t st = get_graph(p, ns_steps, &exec)) return st;
   CUDA_TRY(cudaGraphLaunch(exec, s));
   return MUON_OK;
+}
+
+}  // namespace
+
+muon_status_t muon_step(muon_plan_t p, void* const* params, const void* const* grads,
+                        float* const* momenta, float beta, float lr, float wd, int32_t ns_steps,
+                        float a, float b, float c, void* stream) {
+  const float coef[3] = {a, b, c};
+  return step_impl(p, params, grads, momenta, beta, lr, wd, ns_steps, coef, 1, stream);
+}
+
+muon_status_t muon_step_schedule(muon_plan_t p, void* const* params, const void* const* grads,
+                                 float* const* momenta, float beta, float lr, float wd,
+                                 int32_t ns_steps, const float* coeffs, int32_t n_rows,
+                                 void* stream) {
+  return step_impl(p, params, grads, momenta, beta, lr, wd, ns_steps, coeffs, n_rows, stream);
 }
 
 muon_status_t muon_step_host(muon_plan_t p, void* const* hp, const void* const* hg,

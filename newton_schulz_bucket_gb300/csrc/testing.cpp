@@ -22,7 +22,10 @@ extern "C" muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int3
   int* err = nullptr;
   if (cudaMalloc(&sc, sizeof(StepScalars)) != cudaSuccess) return MUON_ERR_OOM;
   if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) { cudaFree(sc); return MUON_ERR_OOM; }
-  StepScalars h{0.f, 0.f, 0.f, pa, pb, pc, 1, 0};
+  StepScalars h{};
+  h.ns_steps = 1;
+  h.n_coef = 1;
+  h.coef[0][0] = pa; h.coef[0][1] = pb; h.coef[0][2] = pc;
   muon_status_t st = MUON_OK;
   cudaError_t e = cudaMemcpy(sc, &h, sizeof h, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(err, 0, sizeof(int));
@@ -40,7 +43,7 @@ extern "C" muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int3
   if (e == cudaSuccess) e = prepare_tc(k.ns_type);
   if (e == cudaSuccess) {
     if (op == 0) e = launch_tc_gram(k, t, 0, s);
-    else if (op == 1) e = launch_tc_poly(k, t, s);
+    else if (op == 1) e = launch_tc_poly(k, t, 0, s);
     else e = launch_tc_update(k, t, 0, s);
   }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);

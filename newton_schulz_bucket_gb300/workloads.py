@@ -31,7 +31,8 @@ class Workload:
     lr: float
     wd: float
     ns_steps: int
-    coeffs: tuple = QUINTIC
+    coeffs: tuple = QUINTIC        # (a, b, c), or a per-step schedule [(a_0, b_0, c_0), ...]
+    nesterov: bool = False         # orthogonalise U = G + beta M' instead of M'
     p_std: List[float] = field(default_factory=list)     # per parameter
     g_std: List[object] = field(default_factory=list)    # per parameter: float or per-expert list
     m_zero: bool = False

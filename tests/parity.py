@@ -52,8 +52,13 @@ class GpuRun:
         self.inp = {(i, e): (host64(sl(P[i], d3(i), e)), host64(sl(G[i], d3(i), e)),
                              host64(sl(M[i], d3(i), e))) for (i, e) in self.members}
         plan_opts.setdefault("keep_update", True)
+        plan_opts.setdefault("nesterov", w.nesterov)
         self.plan = pkg.MuonPlan(w.shapes, mode=w.mode, **plan_opts)
-        self.coeffs = tuple(F32(v) for v in w.coeffs)
+        self.nesterov = plan_opts["nesterov"]
+        if isinstance(w.coeffs[0], (tuple, list)):  # per-step schedule
+            self.coeffs = [tuple(F32(v) for v in r) for r in w.coeffs]
+        else:
+            self.coeffs = tuple(F32(v) for v in w.coeffs)
         for _ in range(steps):
             self.plan.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, self.coeffs)
         torch.cuda.synchronize()
@@ -76,9 +81,11 @@ class GpuRun:
 
 def oracle_member(run: GpuRun, i: int, e: int, scale_mode="sqrt_aspect", eps=1e-7):
     w = run.w
-    a, b, c = run.coeffs
+    schedule = run.coeffs if isinstance(run.coeffs, list) else None
+    a, b, c = schedule[0] if schedule else run.coeffs
     return muon_ref.muon_update_ref(run.p0(i, e), run.g0(i, e), run.m0(i, e), F32(w.beta),
-                                    F32(w.lr), F32(w.wd), w.ns_steps, a, b, c, eps, scale_mode)
+                                    F32(w.lr), F32(w.wd), w.ns_steps, a, b, c, eps, scale_mode,
+                                    run.nesterov, schedule)
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:

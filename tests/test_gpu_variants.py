@@ -1,0 +1,107 @@
+"""GPU parity of the step's variants against the oracle: per-step coefficient
+schedules (muon_step_schedule) and the Nesterov input U = G + beta M'
+(MUON_FLAG_NESTEROV), on every path."""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import newton_schulz_bucket_gb300 as pkg
+from newton_schulz_bucket_gb300 import workloads as W
+
+from oracle_pins import SCHEDULE
+from parity import GpuRun, check_all
+
+pytestmark = pytest.mark.gpu
+
+# (shapes, plan options, ns_steps): one case per path
+PATHS = [
+    ([[24, 4096], [40, 1000], [2, 64, 2048]], {}, 6),      # skinny, Gram space (m <= 64)
+    ([[24, 2048], [48, 1000]], {}, 70),                     # skinny, direct iteration (k > 64)
+    ([[256, 512], [512, 256]], {}, 6),                      # tensor cores (tcgen05)
+    ([[96, 200], [2, 70, 33]], {"path": "simt"}, 6),        # SIMT, bf16 mode
+]
+IDS = ["gram_space", "direct", "tensor", "simt"]
+
+
+def _workload(shapes, k, seed, mode="bf16", **kw):
+    w = W.custom(shapes, mode=mode, seed=seed, ns_steps=k)
+    for key, v in kw.items():
+        setattr(w, key, v)
+    return w
+
+
+@pytest.mark.parametrize("shapes,opts,k", PATHS, ids=IDS)
+def test_schedule_matches_oracle(shapes, opts, k):
+    w = _workload(shapes, k, 31, coeffs=SCHEDULE)
+    run = GpuRun(w, **opts)
+    check_all(run)
+    run.close()
+
+
+@pytest.mark.parametrize("shapes,opts,k", PATHS, ids=IDS)
+def test_nesterov_matches_oracle(shapes, opts, k):
+    w = _workload(shapes, 5 if k < 64 else k, 32, nesterov=True)
+    run = GpuRun(w, **opts)
+    check_all(run)
+    run.close()
+
+
+def test_fp32_mode_schedule_and_nesterov():
+    w = _workload([[64, 128], [30, 70]], 7, 33, mode="fp32", coeffs=SCHEDULE, nesterov=True)
+    run = GpuRun(w)
+    errs = check_all(run)
+    assert max(errs) <= 1e-4
+    run.close()
+
+
+def test_one_row_schedule_equals_constant_coefficients():
+    """A one-row schedule is muon_step itself: same bits on every path."""
+    shapes = [[24, 4096], [256, 512], [24, 2048]]
+    w = W.custom(shapes, seed=34, ns_steps=5)
+    outs = []
+    for coeffs in (pkg.QUINTIC, [pkg.QUINTIC]):
+        P, G, M = W.make_tensors(w, "cuda")
+        plan = pkg.MuonPlan(w.shapes)
+        plan.step(P, G, M, w.beta, w.lr, w.wd, 5, coeffs)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in P + M])
+        plan.close()
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+
+
+def test_nesterov_batch_invariance_bitwise():
+    """Under Nesterov a member alone equals the member inside a batch."""
+    w = W.custom([[24, 4096]] * 6 + [[64, 1024]] * 3, seed=35)
+    w.nesterov = True
+    P, G, M = W.make_tensors(w, "cuda")
+    keep = [t.clone() for t in P + G + M]
+    full = GpuRun(w, tensors=(P, G, M))
+    n = len(w.shapes)
+    for i in (4, 7):
+        sub = W.custom([w.shapes[i]], seed=0)
+        sub.nesterov = True
+        one = GpuRun(sub, tensors=([keep[i].clone()], [keep[n + i].clone()], [keep[2 * n + i].clone()]))
+        assert np.array_equal(one.p1(0), full.p1(i))
+        assert np.array_equal(one.m1(0), full.m1(i))
+        assert np.array_equal(one.O(0), full.O(i))
+        one.close()
+    full.close()
+
+
+def test_schedule_argument_errors():
+    w = W.custom([[24, 512]], seed=36)
+    P, G, M = W.make_tensors(w, "cuda")
+    plan = pkg.MuonPlan(w.shapes)
+    L = pkg.load_library()
+    Pp, Gp, Mp = plan.bind(P, G, M)
+    st = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rows = (C.c_float * 6)(3.0, -3.2, 1.2, float("nan"), 0.0, 0.0)
+    for ptr, n in ((rows, 0), (rows, 65), (None, 1), (rows, 2)):
+        r = L.muon_step_schedule(plan._h, Pp, Gp, Mp, 0.9, 0.02, 0.1, 5, ptr, n, st)
+        assert r == 1, (n, r)  # MUON_ERR_INVALID_ARG
+    assert L.muon_step_schedule(plan._h, Pp, Gp, Mp, 0.9, 0.02, 0.1, 5, rows, 1, st) == 0
+    torch.cuda.synchronize()
+    plan.close()
