@@ -17,6 +17,13 @@
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Every wait is bounded: on timeout the kernel sets the plan's error
 // word and all roles leave their loops.
+//
+// GRAM and POLY outputs are symmetric (Y Y^T, and a polynomial in the
+// symmetric A), so only the tiles that reach the upper triangle (j >= i) are
+// computed; each writes its elements with j >= i in place and mirrors those
+// with j > i to (j, i).  Every element is written exactly once and the stored
+// matrix is exactly symmetric.  For m = 4096 (BN = 256) that is 272 of 512
+// tiles.
 #include <cuda.h>
 
 #include <type_traits>
@@ -35,6 +42,7 @@ enum TcOp { TC_GRAM = 0, TC_POLY = 1, TC_UPDATE = 2 };
 struct TcArgs {
   int B, M, N, K;
   int tiles_m, tiles_n;
+  int tiles_sym;          // GRAM / POLY: tiles per batch reaching the upper triangle (set at launch)
   int64_t ldc, sC;        // output row pitch / batch stride (elements)
   void* C;
   const void* aux;        // POLY: the A matrix (same layout as C)
@@ -131,6 +139,36 @@ __device__ __forceinline__ void decode_tile(int t, const TcArgs& p, int& b, int&
   tn = r / gsz;
 }
 
+// First tile column of tile row tm that reaches the upper triangle.
+template <int BN>
+__host__ __device__ __forceinline__ int first_tn(int tm) { return tm * BM / BN; }
+template <int BN>
+__host__ __device__ inline int sym_tiles_per_batch(int tiles_m, int tiles_n) {
+  int u = 0;
+  for (int tm = 0; tm < tiles_m; ++tm) {
+    const int c = tiles_n - first_tn<BN>(tm);
+    u += c > 0 ? c : 0;
+  }
+  return u;
+}
+// Tile t of a symmetric output: batch-major, then tile rows, then the tile
+// columns from first_tn(tm).
+template <int OP, int BN>
+__device__ __forceinline__ void decode(int t, const TcArgs& p, int& b, int& tm, int& tn) {
+  if constexpr (OP == TC_UPDATE) {
+    decode_tile(t, p, b, tm, tn);
+  } else {
+    b = t / p.tiles_sym;
+    int r = t - b * p.tiles_sym;
+    tm = 0;
+    while (tm + 1 < p.tiles_m && r >= p.tiles_n - first_tn<BN>(tm)) {
+      r -= p.tiles_n - first_tn<BN>(tm);
+      ++tm;
+    }
+    tn = first_tn<BN>(tm) + r;
+  }
+}
+
 template <typename TY>
 __device__ __forceinline__ void store_row32(TY* dst, const float* v, int nvalid) {
   if (nvalid >= 32) {
@@ -191,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_tiles = p.B * p.tiles_m * p.tiles_n;
+  const int num_tiles = p.B * (OP == TC_UPDATE ? p.tiles_m * p.tiles_n : p.tiles_sym);
   const int kblocks = (p.K + BK - 1) / BK;
   constexpr bool kMN = OP == TC_UPDATE;  // B operand is N-contiguous (MN-major)
 
@@ -201,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int b, tm, tn;
-        decode_tile(t, p, b, tm, tn);
+        decode<OP, BN>(t, p, b, tm, tn);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err, 1)) goto producer_done;
           mbar_expect_tx(full(s), L::kStage);
@@ -262,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int b, tm, tn;
-      decode_tile(t, p, b, tm, tn);
+      decode<OP, BN>(t, p, b, tm, tn);
       if (!mbar_wait(tfull(acc), aph, abort_flag, p.err, 8)) break;
       tc_fence_after();
       const int row = tm * BM + row_in_tile;
@@ -306,7 +344,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col0 + i == row) v[i] += ca;
           }
         }
-        store_row32<TY>(crow + col0, v, nvalid);
+        if constexpr (OP == TC_UPDATE) {
+          store_row32<TY>(crow + col0, v, nvalid);
+        } else {
+          // on and above the diagonal in place, strictly above also at (j, i);
+          // for a fixed i the warp's lanes (rows) write one contiguous run
+          if (col0 >= row) {
+            store_row32<TY>(crow + col0, v, nvalid);
+          } else if (col0 + 31 >= row) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid && col0 + i >= row) crow[col0 + i] = from_f32<TY>(v[i]);
+          }
+          TY* cbase = static_cast<TY*>(p.C) + (int64_t)b * p.sC;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid && col0 + i > row) cbase[(int64_t)(col0 + i) * p.ldc + row] = from_f32<TY>(v[i]);
+        }
       }
       tc_fence_before();
       mbar_arrive(tempty(acc));
@@ -383,9 +437,11 @@ cudaError_t run(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& p, c
   if (prepare)
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 TcSmem<BN>::kTotal);
-  const int tiles = p.B * p.tiles_m * p.tiles_n;
+  TcArgs q = p;
+  if (OP != TC_UPDATE) q.tiles_sym = sym_tiles_per_batch<BN>(p.tiles_m, p.tiles_n);
+  const int tiles = q.B * (OP == TC_UPDATE ? q.tiles_m * q.tiles_n : q.tiles_sym);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  fn<<<grid, kThreads, TcSmem<BN>::kTotal, s>>>(ma, mb, p);
+  fn<<<grid, kThreads, TcSmem<BN>::kTotal, s>>>(ma, mb, q);
   return cudaGetLastError();
 }
 
