@@ -224,6 +224,19 @@ def executed_flop_fraction(rows, cols):
     return (sym * (2 * m * m * n + 2 * m ** 3) + 2 * m * m * n) / dense
 
 
+def executed_flops(w):
+    """Newton-Schulz FLOPs the step executes (the dense count, with the
+    symmetric products of tensor-path groups reduced to their computed tiles;
+    skinny groups are counted dense)."""
+    pkg = __import__("newton_schulz_bucket_gb300")
+    tot = 0.0
+    for g in pkg.describe(w.shapes, mode=w.mode)["groups"]:
+        m, n = min(g["rows"], g["cols"]), max(g["rows"], g["cols"])
+        f = w.ns_steps * (4 * m * m * n + 2 * m ** 3) * g["batch"]
+        tot += f * (executed_flop_fraction(g["rows"], g["cols"]) if g["path"] == "tensor" else 1.0)
+    return tot
+
+
 def headline(w, byts, flops, seconds):
     """GB/s for workloads of skinny groups only, else TFLOP/s."""
     from newton_schulz_bucket_gb300 import describe
@@ -471,6 +484,7 @@ def main():
                            "parallelism": f"replicas x{world}"},
                 "matrices_per_s": sum(g["batch"] for g in groups) * world / sec,
                 "tflops": flops * world / sec / 1e12, "gbs": byts * world / sec / 1e9,
+                "tflops_executed": executed_flops(w) * world / sec / 1e12,
                 "per_group": per_group, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk.summary(),
                 "wall_s_timed": t_wall}

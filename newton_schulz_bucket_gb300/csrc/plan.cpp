@@ -251,6 +251,7 @@ using namespace muon;
 struct muon_plan_s {
   PlanDesc d;
   int device = 0;
+  int num_sms = 1;
   unsigned char* ws = nullptr;        // device scratch
   unsigned char* pinned = nullptr;    // kRingSlots parameter blocks
   std::vector<unsigned char> last_pb; // contents of the last uploaded parameter block
@@ -351,19 +352,37 @@ cudaError_t enqueue_group(const muon_plan_s* p, size_t gi, int32_t k, cudaStream
   return cudaSuccess;
 }
 
+// A group whose kernels alone occupy every SM: its update GEMM has at least
+// one 128-row tile per SM (tensor path), or its clusters cover the SMs.
+bool fills_gpu(const muon_plan_s* p, const GroupPlan& g) {
+  if (g.path == PATH_TENSOR) {
+    const int64_t bn = g.n >= 256 ? 256 : 128;
+    return g.batch * ((g.m + 127) / 128) * ((g.n + bn - 1) / bn) >= p->num_sms;
+  }
+  return g.path == PATH_SKINNY && g.batch * g.sk.cluster >= p->num_sms;
+}
+
 muon_status_t enqueue_all(muon_plan_s* p, int32_t k, cudaStream_t s, bool fork) {
   std::vector<size_t> order(p->d.groups.size());
   for (size_t i = 0; i < order.size(); ++i) order[i] = i;
   std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) {
     return p->d.groups[x].cost > p->d.groups[y].cost;
   });
+  // Groups that fill the GPU run one after another on the caller's stream:
+  // side by side, persistent kernels would only split the SMs between them
+  // and share L2.  The others are dealt to the auxiliary streams, where they
+  // overlap with one another and with the big ones.
   const size_t ns = fork ? std::min(order.size(), p->aux.size() + 1) : 1;
+  std::vector<size_t> lane_of(order.size(), 0);
+  size_t next = 0;
+  for (size_t i = 0; i < order.size(); ++i)
+    if (ns > 1 && !fills_gpu(p, p->d.groups[order[i]])) lane_of[i] = 1 + (next++ % (ns - 1));
   if (ns > 1) {
     CUDA_TRY(cudaEventRecord(p->fork_ev, s));
     for (size_t i = 0; i + 1 < ns; ++i) CUDA_TRY(cudaStreamWaitEvent(p->aux[i], p->fork_ev, 0));
   }
   for (size_t i = 0; i < order.size(); ++i) {
-    const size_t lane = i % ns;
+    const size_t lane = lane_of[i];
     cudaStream_t st = lane == 0 ? s : p->aux[lane - 1];
     cudaError_t e = enqueue_group(p, order[i], k, st);
     if (e != cudaSuccess)
@@ -552,6 +571,7 @@ muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
                        "%s failed: %s", #expr, cudaGetErrorString(e_)));                  \
   } while (0)
   PLAN_TRY(cudaSetDevice(device));
+  PLAN_TRY(cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device));
   PLAN_TRY(cudaMalloc(&p->ws, p->d.ws_bytes));
   PLAN_TRY(cudaMemset(p->ws, 0, p->d.ws_bytes));
   PLAN_TRY(cudaHostAlloc(&p->pinned, kRingSlots * p->d.pb_bytes, cudaHostAllocDefault));
