@@ -112,6 +112,13 @@ typedef struct {
  * then also read G in the output pass, and for ns_steps > 64 (direct
  * iteration) keep U in the workspace (4 bytes per element). */
 #define MUON_FLAG_NESTEROV    16u
+/* Orientation-canonical buckets: [r, c] and [c, r] parameters share one group
+ * keyed by (min, max), so the batch is larger («MindSpore HyperParallel X
+ * 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: fusing more matrices per
+ * launch).  Each member keeps its own orientation: it is iterated in the wide
+ * form and written back transposed if its rows > cols, with its own scale
+ * s(rows, cols), so its result is the same as in an unmerged plan. */
+#define MUON_FLAG_MERGE_TRANSPOSED 32u
 
 /* Rows a per-step coefficient schedule may have (muon_step_schedule). */
 #define MUON_MAX_SCHEDULE_ROWS 64
@@ -129,10 +136,12 @@ typedef struct {
 } muon_plan_options;
 
 typedef struct {
-  int64_t rows, cols;        /* the trailing dims every member shares              */
+  int64_t rows, cols;        /* the trailing dims every member shares (with      */
+                             /* MUON_FLAG_MERGE_TRANSPOSED: the first member's)   */
   int64_t batch;             /* number of member matrices                         */
   int64_t first_member;      /* index of the group's first member (see below)     */
-  int32_t transposed;        /* rows > cols: the iteration runs on the transpose  */
+  int32_t transposed;        /* 1: every member has rows > cols (iterated on its  */
+                             /* transpose); 0: none; 2: both orientations (merge) */
   int32_t path;              /* muon_path_t chosen for the group                  */
   int64_t workspace_bytes;   /* device bytes of the group's scratch               */
 } muon_group_info_t;

@@ -41,7 +41,7 @@ def _shapes(shapes: Sequence[Sequence[int]]):
 
 def _options(mode="bf16", scale="sqrt_aspect", eps=1e-7, ns_dtype="fp16", skinny_threshold=0,
              path="auto", keep_update=False, no_graph=False, host_staging=False, max_streams=0,
-             group_timing=False, nesterov=False):
+             group_timing=False, nesterov=False, merge_transposed=False):
     L = _c.load()
     o = _c.muon_plan_options()
     _c.check(L.muon_default_options(C.byref(o)), "muon_default_options")
@@ -55,14 +55,16 @@ def _options(mode="bf16", scale="sqrt_aspect", eps=1e-7, ns_dtype="fp16", skinny
                | (_c.MUON_FLAG_NO_GRAPH if no_graph else 0)
                | (_c.MUON_FLAG_HOST_STAGING if host_staging else 0)
                | (_c.MUON_FLAG_GROUP_TIMING if group_timing else 0)
-               | (_c.MUON_FLAG_NESTEROV if nesterov else 0))
+               | (_c.MUON_FLAG_NESTEROV if nesterov else 0)
+               | (_c.MUON_FLAG_MERGE_TRANSPOSED if merge_transposed else 0))
     o.max_streams = int(max_streams)
     return o
 
 
 def _group_dict(g) -> Dict:
     return {"rows": g.rows, "cols": g.cols, "batch": g.batch, "first_member": g.first_member,
-            "transposed": bool(g.transposed), "path": PATH_NAMES.get(g.path, g.path),
+            "transposed": {0: False, 1: True}.get(g.transposed, "mixed"),
+            "path": PATH_NAMES.get(g.path, g.path),
             "workspace_bytes": g.workspace_bytes}
 
 

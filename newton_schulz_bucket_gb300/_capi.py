@@ -33,6 +33,7 @@ MUON_FLAG_NO_GRAPH = 2
 MUON_FLAG_HOST_STAGING = 4
 MUON_FLAG_GROUP_TIMING = 8
 MUON_FLAG_NESTEROV = 16
+MUON_FLAG_MERGE_TRANSPOSED = 32
 MUON_MAX_SCHEDULE_ROWS = 64
 
 

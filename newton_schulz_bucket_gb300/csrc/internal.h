@@ -25,11 +25,15 @@ struct StepScalars {
 };
 
 // Per-member device pointers, rewritten before every step (the caller may
-// pass different buffers each step).  P and G are bf16 or fp32 by mode.
+// pass different buffers each step).  P and G are bf16 or fp32 by mode.  A
+// member's parameter is [m, n] (T = 0) or [n, m] (T = 1) for its group's
+// (m, n); scale is its s(rows, cols).
 struct MemberPtrs {
   void* P;
   const void* G;
   float* M;
+  int32_t T;
+  float scale;
 };
 
 enum Path : int32_t { PATH_AUTO = 0, PATH_SKINNY = 1, PATH_TENSOR = 2, PATH_SIMT = 3 };
@@ -45,9 +49,9 @@ struct KArgs {
   const StepScalars* sc;   // device
   const MemberPtrs* mem;   // device, already offset to the group's first member
   int32_t B;               // members in the group
-  int32_t rows, cols;      // parameter dims
+  int32_t rows, cols;      // parameter dims of the group's first member (kernels use m, n and MemberPtrs::T)
   int32_t m, n;            // min / max of (rows, cols)
-  int32_t T;               // rows > cols
+  int32_t T;               // rows > cols for the group's first member
   int32_t mode_f32;        // 1: P, G fp32 ; 0: P, G bf16
   int32_t ns_type;         // NsType of y0/y1/A/Q
   int64_t n_pitch;         // row pitch (elements) of the m x n iterate

@@ -22,7 +22,7 @@ template <typename TG>
 __global__ void __launch_bounds__(kThreads) k_momentum_partial(KArgs a) {
   __shared__ float red[33];
   const int b = blockIdx.y;
-  const int64_t total = (int64_t)a.rows * a.cols;
+  const int64_t total = (int64_t)a.m * a.n;
   const int64_t start = (int64_t)blockIdx.x * kMomentumChunk;
   const int64_t end = min(start + kMomentumChunk, total);
   const MemberPtrs mp = a.mem[b];
@@ -128,13 +128,17 @@ __global__ void __launch_bounds__(kThreads) k_normalize_cast(KArgs a, TY* __rest
   const float beta = a.sc->beta;
   const float inv = a.invn[b];
   TY* Yb = Y + (int64_t)b * a.m * a.n_pitch;
-  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;  // tile origin (parameter coords)
+  // the grid walks the wide m x n iterate; in parameter coordinates a tile
+  // keeps its origin, or swaps it for a transposed member
+  const bool T = a.mem[b].T != 0;
+  const int rows = T ? a.n : a.m, cols = T ? a.m : a.n;
+  const int r0 = (T ? blockIdx.x : blockIdx.y) * 64, c0 = (T ? blockIdx.y : blockIdx.x) * 64;
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
   for (int rr = ty; rr < 64; rr += 4) {
     const int r = r0 + rr, c = c0 + tx;
     float x = 0.f;
-    if (r < a.rows && c < a.cols) {
-      const int64_t o = (int64_t)r * a.cols + c;
+    if (r < rows && c < cols) {
+      const int64_t o = (int64_t)r * cols + c;
       x = Mp[o];
       if (nest) {
         const float g = a.mode_f32 ? static_cast<const float*>(Gp)[o]
@@ -145,16 +149,16 @@ __global__ void __launch_bounds__(kThreads) k_normalize_cast(KArgs a, TY* __rest
     tile[rr][tx] = x * inv;
   }
   __syncthreads();
-  if (!a.T) {
+  if (!T) {
     for (int rr = ty; rr < 64; rr += 4) {
       const int r = r0 + rr, c = c0 + tx;
-      if (r < a.rows && c < a.cols) Yb[(int64_t)r * a.n_pitch + c] = from_f32<TY>(tile[rr][tx]);
+      if (r < rows && c < cols) Yb[(int64_t)r * a.n_pitch + c] = from_f32<TY>(tile[rr][tx]);
     }
   } else {
     // Y[c][r] = M'[r][c]: Y row index = parameter column
     for (int cc = ty; cc < 64; cc += 4) {
       const int c = c0 + cc, r = r0 + tx;
-      if (r < a.rows && c < a.cols) Yb[(int64_t)c * a.n_pitch + r] = from_f32<TY>(tile[tx][cc]);
+      if (r < rows && c < cols) Yb[(int64_t)c * a.n_pitch + r] = from_f32<TY>(tile[tx][cc]);
     }
   }
 }
@@ -169,32 +173,36 @@ __global__ void __launch_bounds__(kThreads) k_write(KArgs a, const TY* __restric
   const TY* Yb = Y + (int64_t)b * a.m * a.n_pitch;
   const float lr = a.sc->lr, wd = a.sc->wd;
   const float decay = 1.f - lr * wd;
-  const float coef = lr * a.scale / a.alpha;  // alpha is a power of two
+  const MemberPtrs mp = a.mem[b];
+  const float coef = lr * mp.scale / a.alpha;  // alpha is a power of two
   const float inv_alpha = 1.f / a.alpha;
-  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  const bool T = mp.T != 0;
+  const int rows = T ? a.n : a.m, cols = T ? a.m : a.n;
+  const int r0 = (T ? blockIdx.x : blockIdx.y) * 64, c0 = (T ? blockIdx.y : blockIdx.x) * 64;
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-  if (a.T) {
+  if (T) {
     // stage the Y tile Y[c0..c0+64)[r0..r0+64) so reads are coalesced along r
     for (int cc = ty; cc < 64; cc += 4) {
       const int c = c0 + cc, r = r0 + tx;
-      tile[tx][cc] = (r < a.rows && c < a.cols) ? to_f32(Yb[(int64_t)c * a.n_pitch + r]) : 0.f;
+      tile[tx][cc] = (r < rows && c < cols) ? to_f32(Yb[(int64_t)c * a.n_pitch + r]) : 0.f;
     }
     __syncthreads();
   }
-  float* dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+  float* dbg = a.dbg ? a.dbg + (int64_t)b * a.m * a.n : nullptr;
   for (int rr = ty; rr < 64; rr += 4) {
     const int r = r0 + rr, c = c0 + tx;
-    if (r >= a.rows || c >= a.cols) continue;
-    const float y = a.T ? tile[rr][tx] : to_f32(Yb[(int64_t)r * a.n_pitch + c]);
-    const int64_t idx = (int64_t)r * a.cols + c;
+    if (r >= rows || c >= cols) continue;
+    const float y = T ? tile[rr][tx] : to_f32(Yb[(int64_t)r * a.n_pitch + c]);
+    const int64_t idx = (int64_t)r * cols + c;
     const float p = to_f32(P[idx]);
     P[idx] = from_f32<TP>(fmaf(-coef, y, p * decay));
     if (dbg) dbg[idx] = y * inv_alpha;
   }
 }
 
+// 64 x 64 tiles of the wide m x n iterate (x: columns, y: rows)
 dim3 tiles_of(const KArgs& a) {
-  return dim3((a.cols + 63) / 64, (a.rows + 63) / 64, a.B);
+  return dim3((a.n + 63) / 64, (a.m + 63) / 64, a.B);
 }
 
 }  // namespace

@@ -316,22 +316,24 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   c.lane = lane; c.warp = warp; c.g = lane >> 2; c.t4 = lane & 3;
   c.m = m; c.n = a.n; c.c0 = (int)rank * s.W; c.NB = s.NB;
   // X_0's source: M', or U = G + beta M' written by the momentum kernel
-  c.Mp = a.u ? a.u + (int64_t)b * a.rows * a.cols : mp.M;
+  c.Mp = a.u ? a.u + (int64_t)b * m * a.n : mp.M;
   c.P = static_cast<__nv_bfloat16*>(mp.P);
-  c.wd = Wide{a.cols, a.T};
+  const bool T = mp.T != 0;           // this member's parameter is [n, m]
+  const int cols = T ? m : a.n;       // the parameter's row pitch
+  c.wd = Wide{cols, (int)T};
   // pairs (i, j), (i, j+1) are adjacent in memory (fast path) when the wide
   // iterate is the parameter itself, its rows are even and bases are aligned
-  c.pairs = !a.T && (a.cols % 2 == 0) &&
+  c.pairs = !T && (cols % 2 == 0) &&
             ((reinterpret_cast<uintptr_t>(c.Mp) | reinterpret_cast<uintptr_t>(c.P)) & 7) == 0;
   c.ws = s.ws + ((int64_t)b * kCL + rank) * s.NB * s.blk;
-  c.dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+  c.dbg = a.dbg ? a.dbg + (int64_t)b * m * a.n : nullptr;
 #pragma unroll
   for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = mi * 16 + c.g + 8 * h;
       c.rv[mi][h] = i < m;
-      c.roff[mi][h] = (int64_t)i * a.cols + 2 * c.t4;
+      c.roff[mi][h] = (int64_t)i * cols + 2 * c.t4;
     }
 
   // Q = 0 outside the m x m block; zero once
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   const float lr = a.sc->lr, wdk = a.sc->wd;
   c.decay = 1.f - lr * wdk;
   c.inv_alpha = 1.f / a.alpha;
-  c.coef = lr * a.scale * c.inv_alpha;
+  c.coef = lr * mp.scale * c.inv_alpha;
   uint8_t* stage_warp = smem + L::kStage + warp * 32 * L::LB;
 
   uint32_t qf[MT][MT][4];

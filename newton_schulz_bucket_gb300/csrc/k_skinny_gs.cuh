@@ -656,17 +656,18 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   c.Mp = mp.M;
   c.G = static_cast<const __nv_bfloat16*>(mp.G);
   c.P = static_cast<__nv_bfloat16*>(mp.P);
-  c.cols = a.cols;
-  c.wd = Wide{a.cols, a.T};
-  c.vec = !a.T && (a.cols % 8 == 0) && 32ll * a.cols < (1ll << 31) && aligned16(c.Mp) &&
+  const bool T = mp.T != 0;  // this member's parameter is [n, m]
+  c.cols = T ? m : a.n;      // the parameter's row pitch
+  c.wd = Wide{c.cols, (int)T};
+  c.vec = !T && (c.cols % 8 == 0) && 32ll * c.cols < (1ll << 31) && aligned16(c.Mp) &&
           aligned16(c.G) && aligned16(c.P);
-  c.dbg = a.dbg ? a.dbg + (int64_t)b * a.rows * a.cols : nullptr;
+  c.dbg = a.dbg ? a.dbg + (int64_t)b * m * a.n : nullptr;
   const int ns = a.sc->ns_steps;
   c.beta = a.sc->beta;
   const float lr = a.sc->lr;
   c.decay = 1.f - lr * a.sc->wd;
   c.inv_alpha = 1.f / a.alpha;
-  c.coef = lr * a.scale * c.inv_alpha;
+  c.coef = lr * mp.scale * c.inv_alpha;
 
   // m x m work arrays (aliasing the ring between the two passes)
   float* wpart = reinterpret_cast<float*>(smem);
@@ -699,7 +700,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     const int ncol = min(W, c.n - c.c0);
     const uint32_t bytes = (uint32_t)(ncol * 2) & ~15u;
     if (bytes)
-      for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * a.cols + c.c0, bytes);
+      for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * c.cols + c.c0, bytes);
   }
   __syncthreads();  // every warp's ring is drained before it is reused
   // per-warp partials, then warps summed in a fixed order into this CTA's partial

@@ -49,13 +49,16 @@ muon_status_t static_fail(muon_status_t st, const char* msg) {
 // kernel's own arguments (so the call needs neither an allocation nor a host
 // staging buffer).
 __global__ void k_static_setup(StepScalars sc, void* P, const void* G, float* M, int batch,
-                               int64_t per, StepScalars* sc_out, MemberPtrs* mem_out) {
+                               int64_t per, int32_t T, float scale, StepScalars* sc_out,
+                               MemberPtrs* mem_out) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   *sc_out = sc;
   for (int b = 0; b < batch; ++b) {
     mem_out[b].P = static_cast<__nv_bfloat16*>(P) + b * per;
     mem_out[b].G = static_cast<const __nv_bfloat16*>(G) + b * per;
     mem_out[b].M = M + b * per;
+    mem_out[b].T = T;
+    mem_out[b].scale = scale;
   }
 }
 
@@ -150,7 +153,7 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
   hs.ns_steps = ns_steps;
   hs.n_coef = 1;
   hs.coef[0][0] = a; hs.coef[0][1] = b; hs.coef[0][2] = c;
-  k_static_setup<<<1, 32, 0, s>>>(hs, params, grads, momenta, batch, rows * cols, sc, mem);
+  k_static_setup<<<1, 32, 0, s>>>(hs, params, grads, momenta, batch, rows * cols, k.T, k.scale, sc, mem);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_skinny(k, cfg, ns_steps, s);
   if (e != cudaSuccess) return static_fail(MUON_ERR_CUDA, cudaGetErrorString(e));

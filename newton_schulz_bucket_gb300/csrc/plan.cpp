@@ -73,6 +73,7 @@ struct PlanDesc {
   std::vector<GroupPlan> groups;
   std::vector<int32_t> member_param, member_expert;
   std::vector<int64_t> param_E, param_rows, param_cols;
+  std::vector<float> param_scale;  // s(rows, cols) of each parameter
   size_t ws_bytes = 0;      // total device scratch incl. tables
   size_t off_scalars = 0;   // StepScalars + MemberPtrs table
   size_t off_err = 0;
@@ -100,7 +101,7 @@ muon_status_t check_options(const muon_plan_options& o) {
   if (o.skinny_threshold < -1 || o.skinny_threshold > 64)
     return fail(MUON_ERR_INVALID_ARG, "skinny_threshold must be in [-1, 64]");
   if (o.flags & ~(MUON_FLAG_KEEP_UPDATE | MUON_FLAG_NO_GRAPH | MUON_FLAG_HOST_STAGING |
-                  MUON_FLAG_GROUP_TIMING | MUON_FLAG_NESTEROV))
+                  MUON_FLAG_GROUP_TIMING | MUON_FLAG_NESTEROV | MUON_FLAG_MERGE_TRANSPOSED))
     return fail(MUON_ERR_INVALID_ARG, "unknown flag bits 0x%x", o.flags);
   for (int i = 0; i < 8; ++i)
     if (o.reserved[i] != 0) return fail(MUON_ERR_INVALID_ARG, "reserved option fields must be 0");
@@ -147,9 +148,13 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
     if (r > (1 << 30) || c > (1 << 30) || r * c > ((int64_t)1 << 40))
       return fail(MUON_ERR_UNSUPPORTED, "parameter %d is too large", p);
     d->param_E.push_back(E); d->param_rows.push_back(r); d->param_cols.push_back(c);
+    d->param_scale.push_back(scale_of(o.scale, r, c));
     total_members += E;
     if (total_members > INT32_MAX) return fail(MUON_ERR_INVALID_ARG, "too many members");
-    auto key = std::make_pair(r, c);
+    // the bucket key: (rows, cols), or (min, max) when [r, c] and [c, r]
+    // share a group (each member keeps its orientation)
+    auto key = (o.flags & MUON_FLAG_MERGE_TRANSPOSED) ? std::make_pair(std::min(r, c), std::max(r, c))
+                                                      : std::make_pair(r, c);
     auto it = index.find(key);
     int g;
     if (it == index.end()) {
@@ -180,7 +185,9 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
       d->member_param.push_back(pe.first);
       d->member_expert.push_back(pe.second);
     }
-    gp.transposed = gp.rows > gp.cols;
+    int n_t = 0;  // members whose parameter is [n, m]
+    for (auto& pe : members[g]) n_t += d->param_rows[pe.first] > d->param_cols[pe.first] ? 1 : 0;
+    gp.transposed = n_t == 0 ? 0 : (n_t == (int)members[g].size() ? 1 : 2);
     gp.m = std::min(gp.rows, gp.cols);
     gp.n = std::max(gp.rows, gp.cols);
     gp.ns_type = f32 ? NS_F32 : (o.ns_dtype == MUON_NS_BF16 ? NS_BF16 : NS_F16);
@@ -670,6 +677,8 @@ muon_status_t step_impl(muon_plan_t p, void* const* params, const void* const* g
     mp[i].P = static_cast<unsigned char*>(params[pi]) + off * pes;
     mp[i].G = static_cast<const unsigned char*>(grads[pi]) + off * pes;
     mp[i].M = momenta[pi] + off;
+    mp[i].T = p->d.param_rows[pi] > p->d.param_cols[pi] ? 1 : 0;
+    mp[i].scale = p->d.param_scale[pi];
   }
   // The device block keeps the last upload (stream order on `s` makes it
   // visible to the steps after it): a step with the same scalars and buffers

@@ -167,13 +167,16 @@ def _members(shape: Sequence[int]) -> Tuple[int, int, int]:
     raise ValueError(f"parameter must be 2-D or 3-D, got {shape}")
 
 
-def bucket_shapes(shapes: Sequence[Sequence[int]]) -> List[Dict]:
+def bucket_shapes(shapes: Sequence[Sequence[int]], merge_transposed: bool = False) -> List[Dict]:
     """Group parameters by their exact trailing two dims, first-seen order.
 
     «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化
     (Fig. 6): parameters whose trailing two dims agree are stacked into one
     [B, M, N] batch; Muon亲和的专家切分 (Fig. 4): a 3-D [E, M, N] tensor is E
     independent matrices.  Members keep parameter order, experts in E order.
+    With merge_transposed the key is (min, max) of the two dims, so [r, c]
+    and [c, r] share a group (a larger fused batch; each member keeps its
+    orientation); the group's (rows, cols) are its first member's.
     Returns [{'rows', 'cols', 'members': [(param, expert), ...]}, ...].
     """
     groups: Dict[Tuple[int, int], Dict] = {}
@@ -182,7 +185,7 @@ def bucket_shapes(shapes: Sequence[Sequence[int]]) -> List[Dict]:
         E, r, cl = _members(shp)
         if E < 1 or r < 1 or cl < 1:
             raise ValueError(f"parameter {pi} has an empty dim: {tuple(shp)}")
-        key = (r, cl)
+        key = (min(r, cl), max(r, cl)) if merge_transposed else (r, cl)
         if key not in groups:
             groups[key] = {"rows": r, "cols": cl, "members": []}
             order.append(key)

@@ -75,6 +75,26 @@ def test_planner_matches_oracle_bucketing(lib, shapes):
         first += g["batch"]
 
 
+@pytest.mark.parametrize("shapes", [
+    [[4, 8], [3, 8, 4], [4, 8], [2, 3, 8], [8, 4]],
+    [[4096, 16384], [16384, 4096]] * 3 + [[4096, 4096]],
+    [[24, 10240], [10240, 24], [2, 24, 10240], [5, 3], [3, 5], [1, 9], [9, 1]],
+])
+def test_merged_orientation_buckets(lib, shapes):
+    """[r, c] and [c, r] share a group keyed by (min, max) with the merge flag;
+    the member order and group order match the oracle's merged bucketing."""
+    d = pkg.describe(shapes, merge_transposed=True)
+    ref = muon_ref.bucket_shapes(shapes, merge_transposed=True)
+    assert [(g["rows"], g["cols"], g["batch"]) for g in d["groups"]] == \
+        [(g["rows"], g["cols"], len(g["members"])) for g in ref]
+    assert d["members"] == [m for g in ref for m in g["members"]]
+    for g, rg in zip(d["groups"], ref):
+        orient = {shapes[p][-2] > shapes[p][-1] for p, _ in rg["members"]}
+        want = "mixed" if len(orient) == 2 else orient.pop()
+        assert g["transposed"] == want
+    assert len(d["groups"]) == len({(min(s[-2:]), max(s[-2:])) for s in shapes})
+
+
 def test_planner_paths(lib):
     d = pkg.describe([[24, 10240], [64, 7168], [4096, 4096], [10240, 24]])
     paths = [g["path"] for g in d["groups"]]

@@ -123,8 +123,13 @@ def test_gram_space_zero_rows(k, rows):
 
 
 def test_many_steps_direct_iteration():
-    """Step counts beyond the Gram-space range run the direct iteration."""
+    """Step counts beyond the Gram-space range run the direct iteration.  The
+    run ends in the contractive textbook map (see the schedule's last row):
+    under the constant quintic, 70 fp16-rounded steps drift from the fp64
+    oracle (singular values keep moving inside [0.68, 1.13]) for some inputs."""
+    from oracle_pins import SCHEDULE
     w = W.custom([[24, 2048], [2, 16, 512], [64, 1024], [40, 512]], seed=22, ns_steps=70)
+    w.coeffs = SCHEDULE
     run = GpuRun(w)
     check_all(run)
     run.close()
