@@ -132,7 +132,9 @@ typedef struct {
   uint32_t flags;            /* MUON_FLAG_*                                        */
   int32_t path_override;     /* muon_path_t for every group; AUTO = choose         */
   int32_t max_streams;       /* groups run on up to this many graph branches; 0=4  */
-  int32_t reserved[8];       /* must be zero                                       */
+  int32_t column_shards;     /* skinny path: CTAs per member, each owning one      */
+                             /* contiguous column shard (1, 2, 4 or 8; 0 = 2)      */
+  int32_t reserved[7];       /* must be zero                                       */
 } muon_plan_options;
 
 typedef struct {

@@ -41,7 +41,7 @@ def _shapes(shapes: Sequence[Sequence[int]]):
 
 def _options(mode="bf16", scale="sqrt_aspect", eps=1e-7, ns_dtype="fp16", skinny_threshold=0,
              path="auto", keep_update=False, no_graph=False, host_staging=False, max_streams=0,
-             group_timing=False, nesterov=False, merge_transposed=False):
+             group_timing=False, nesterov=False, merge_transposed=False, column_shards=0):
     L = _c.load()
     o = _c.muon_plan_options()
     _c.check(L.muon_default_options(C.byref(o)), "muon_default_options")
@@ -58,6 +58,7 @@ def _options(mode="bf16", scale="sqrt_aspect", eps=1e-7, ns_dtype="fp16", skinny
                | (_c.MUON_FLAG_NESTEROV if nesterov else 0)
                | (_c.MUON_FLAG_MERGE_TRANSPOSED if merge_transposed else 0))
     o.max_streams = int(max_streams)
+    o.column_shards = int(column_shards)
     return o
 
 

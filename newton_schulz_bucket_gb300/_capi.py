@@ -45,7 +45,8 @@ class muon_plan_options(C.Structure):
     _fields_ = [("mode", C.c_int32), ("scale", C.c_int32), ("eps", C.c_float),
                 ("skinny_threshold", C.c_int32), ("ns_dtype", C.c_int32),
                 ("flags", C.c_uint32), ("path_override", C.c_int32),
-                ("max_streams", C.c_int32), ("reserved", C.c_int32 * 8)]
+                ("max_streams", C.c_int32), ("column_shards", C.c_int32),
+                ("reserved", C.c_int32 * 7)]
 
 
 class muon_group_info_t(C.Structure):

@@ -111,14 +111,15 @@ cudaError_t launch_simt_update(const KArgs& a, const void* ysrc, void* ydst, cud
 // then the write, one cluster per member, no workspace); otherwise the
 // momentum kernel, then the direct iteration (iterate in a fragment-ordered
 // workspace a.y0).
-bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg);
+// shards: CTAs (contiguous column shards) per member, 1, 2, 4 or 8; 0 = 2.
+bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg, int32_t shards = 0);
 cudaError_t prepare_skinny(const KArgs& a, const SkinnyCfg& cfg);  // function attributes
 cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, int32_t ns_steps, cudaStream_t s);
 cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare);
-int gs_max_active_clusters(int ns_type, int m);
+int gs_max_active_clusters(int ns_type, int m, int cl);
 // Clusters of the skinny kernel for min dim m that fit on the device at once
 // (after prepare_skinny for that m).
-int skinny_max_active_clusters(int ns_type, int m);
+int skinny_max_active_clusters(int ns_type, int m, int cl);
 
 // Test hook: one bounded mbarrier wait, completed by a second thread
 // (arrive != 0) or by nothing; on giving up it sets bit 16 of *err.

@@ -28,7 +28,7 @@ namespace muon {
 
 namespace {
 
-constexpr int kCL = 2;  // CTAs per member (cluster size), fixed for every shape
+constexpr int kDefaultShards = 2;  // CTAs (column shards) per member unless the plan says otherwise
 
 // Shared memory (bytes): the cp.async stage ring, per-warp Gram partials, the
 // CTA partial (double buffered, read by the peer), A (fp32), Q (operand type).
@@ -53,7 +53,7 @@ struct SkArgs {
   int W;        // columns of the wide iterate per CTA (multiple of 16)
   int NB;       // 16-column blocks per CTA
   int blk;      // bytes of one block in the fragment workspace
-  uint8_t* ws;  // fragment workspace [B][kCL][NB][blk]
+  uint8_t* ws;  // fragment workspace [B][CL][NB][blk]
 };
 
 // Offsets of element (i, j) of the wide iterate in the parameter's memory.
@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank();
-  const int b = blockIdx.x / kCL;
+  const int CL = (int)cluster_size();  // CTAs (column shards) per member
+  const int b = blockIdx.x / CL;
   const int m = a.m;
   const MemberPtrs mp = a.mem[b];
 
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   // iterate is the parameter itself, its rows are even and bases are aligned
   c.pairs = !T && (cols % 2 == 0) &&
             ((reinterpret_cast<uintptr_t>(c.Mp) | reinterpret_cast<uintptr_t>(c.P)) & 7) == 0;
-  c.ws = s.ws + ((int64_t)b * kCL + rank) * s.NB * s.blk;
+  c.ws = s.ws + ((int64_t)b * CL + rank) * s.NB * s.blk;
   c.dbg = a.dbg ? a.dbg + (int64_t)b * m * a.n : nullptr;
 #pragma unroll
   for (int mi = 0; mi < MT; ++mi)
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
       if (i > j) continue;
       float acc = 0.f;
 #pragma unroll
-      for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cp[i * MP + j], (uint32_t)r);
+      for (int r = 0; r < CL; ++r) acc += ld_dsmem_f32(&cp[i * MP + j], (uint32_t)r);
       acc *= inv_a2;
       Af[i * MP + j] = acc;
       Af[j * MP + i] = acc;
@@ -447,13 +448,13 @@ cudaError_t launch_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool
   s.blk = cfg.blk;
   s.ws = static_cast<uint8_t*>(a.y0);
   cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(a.B * kCL);
+  lc.gridDim = dim3(a.B * cfg.cluster);
   lc.blockDim = dim3(NT);
   lc.dynamicSmemBytes = smem;
   lc.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.x = cfg.cluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
@@ -487,16 +488,16 @@ cudaError_t dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool
 }
 
 template <typename TY, int MT, bool HALF>
-int clusters_of() {
+int clusters_of(int cl) {
   constexpr int NT = MT <= 2 ? 512 : 256;
   auto fn = k_skinny_ns<TY, MT, NT, HALF>;
   cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(kCL * 1024);
+  lc.gridDim = dim3(cl * 1024);
   lc.blockDim = dim3(NT);
   lc.dynamicSmemBytes = NsSmem<MT, NT>::kTotal;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.x = cl;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
@@ -506,29 +507,31 @@ int clusters_of() {
 }
 
 template <typename TY, bool HALF>
-int clusters_mt(int mtiles) {
+int clusters_mt(int mtiles, int cl) {
   switch (mtiles) {
-    case 1: return clusters_of<TY, 1, HALF>();
-    case 2: return clusters_of<TY, 2, HALF>();
-    case 3: return clusters_of<TY, 3, HALF>();
-    default: return clusters_of<TY, 4, HALF>();
+    case 1: return clusters_of<TY, 1, HALF>(cl);
+    case 2: return clusters_of<TY, 2, HALF>(cl);
+    case 3: return clusters_of<TY, 3, HALF>(cl);
+    default: return clusters_of<TY, 4, HALF>(cl);
   }
 }
 
 }  // namespace
 
-bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg) {
+bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg, int32_t shards) {
   const int m = rows < cols ? rows : cols, n = rows < cols ? cols : rows;
   if (m < 1 || m > max_m || m > 64) return false;
+  const int cl = shards > 0 ? shards : kDefaultShards;
+  if (cl != 1 && cl != 2 && cl != 4 && cl != 8) return false;
   cfg->mtiles = (m + 15) / 16;
-  cfg->cluster = kCL;
+  cfg->cluster = cl;
   cfg->threads = cfg->mtiles <= 2 ? 512 : 256;
-  const int w = (n + kCL - 1) / kCL;
+  const int w = (n + cl - 1) / cl;
   cfg->width = (w + 31) / 32 * 32;  // whole 32-column superblocks (Gram-space output pass)
   int blk = 0;
   for (int q = 0; q < cfg->mtiles; ++q) blk += (m - 16 * q > 8) ? 512 : 256;
   cfg->blk = blk;
-  cfg->ws_bytes = (int64_t)kCL * (cfg->width / 16) * blk;  // per member (direct kernel)
+  cfg->ws_bytes = (int64_t)cl * (cfg->width / 16) * blk;  // per member (direct kernel)
   cfg->smem = 0;
   cfg->gram_space = 1;  // every skinny m (<= 64); the step count decides at launch
   return true;
@@ -546,13 +549,14 @@ cudaError_t launch_skinny(const KArgs& a, const SkinnyCfg& cfg, int32_t ns_steps
   return e == cudaSuccess ? dispatch(a, cfg, s, false) : e;
 }
 
-int skinny_max_active_clusters(int ns_type, int m) {
+int skinny_max_active_clusters(int ns_type, int m, int cl) {
   const int mt = (m + 15) / 16;
   const bool half = half_last_tile(m, mt);
-  const int direct = ns_type == NS_F16 ? (half ? clusters_mt<__half, true>(mt) : clusters_mt<__half, false>(mt))
-                                       : (half ? clusters_mt<__nv_bfloat16, true>(mt)
-                                               : clusters_mt<__nv_bfloat16, false>(mt));
-  const int gs = gs_max_active_clusters(ns_type, m);  // either kernel may serve a step
+  const int direct = ns_type == NS_F16
+                         ? (half ? clusters_mt<__half, true>(mt, cl) : clusters_mt<__half, false>(mt, cl))
+                         : (half ? clusters_mt<__nv_bfloat16, true>(mt, cl)
+                                 : clusters_mt<__nv_bfloat16, false>(mt, cl));
+  const int gs = gs_max_active_clusters(ns_type, m, cl);  // either kernel may serve a step
   return gs < direct ? gs : direct;
 }
 

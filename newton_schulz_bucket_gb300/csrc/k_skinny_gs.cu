@@ -6,7 +6,7 @@
 namespace muon {
 
 cudaError_t gs_dispatch_nesterov(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare);
-int gs_max_active_clusters_nesterov(int ns_type, int m);
+int gs_max_active_clusters_nesterov(int ns_type, int m, int cl);
 
 cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare) {
   if (prepare) {  // both settings, so that either may run
@@ -16,8 +16,8 @@ cudaError_t gs_dispatch(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bo
   return a.nesterov ? gs_dispatch_nesterov(a, cfg, s, false) : gs::gs_dispatch_t<false>(a, cfg, s, false);
 }
 
-int gs_max_active_clusters(int ns_type, int m) {
-  const int p = gs::gs_clusters_t<false>(ns_type, m), q = gs_max_active_clusters_nesterov(ns_type, m);
+int gs_max_active_clusters(int ns_type, int m, int cl) {
+  const int p = gs::gs_clusters_t<false>(ns_type, m, cl), q = gs_max_active_clusters_nesterov(ns_type, m, cl);
   return p < q ? p : q;
 }
 

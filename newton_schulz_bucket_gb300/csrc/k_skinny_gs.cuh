@@ -30,7 +30,8 @@
 // type once instead of once per step.  All reduction orders depend only on
 // (rows, cols), so a member gives the same bits in any batch.
 //
-// Layout: one cluster of kCL CTAs per member; CTA r owns the wide iterate's
+// Layout: one cluster of CL CTAs per member (the plan's column shards; 2 by
+// default), CTA r owning one contiguous column shard of the wide iterate's
 // columns [r W, (r + 1) W), 16 warps up to m = 32 and 8 beyond (each lane
 // then keeps Pi's fragments for four 16-row tiles, 128 registers).  Both
 // passes walk 32-column superblocks (superblock sb by warp sb % NW).  In the
@@ -48,7 +49,6 @@
 namespace muon {
 namespace gs {
 
-constexpr int kCL = 2;  // CTAs per member (cluster size)
 
 template <int MT, int NT, bool HALF>
 struct GsLayout {
@@ -646,7 +646,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank();
-  const int b = blockIdx.x / kCL;
+  const int CL = (int)cluster_size();  // CTAs (column shards) per member
+  const int b = blockIdx.x / CL;
   const int m = a.m;
   const MemberPtrs mp = a.mem[b];
 
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: CTAs summed in rank order
   float ssum = 0.f;
 #pragma unroll
-  for (int r = 0; r < kCL; ++r) ssum += ld_dsmem_f32(&misc[0], (uint32_t)r);
+  for (int r = 0; r < CL; ++r) ssum += ld_dsmem_f32(&misc[0], (uint32_t)r);
   const float inv_raw = 1.f / (sqrtf(ssum) + a.eps);
   c.inv = a.alpha * inv_raw;
   const float inv2 = inv_raw * inv_raw;
@@ -741,7 +742,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     const int i = tab[e] >> 16, j = tab[e] & 0xffff;
     float acc = 0.f;
 #pragma unroll
-    for (int r = 0; r < kCL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
+    for (int r = 0; r < CL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
     acc *= inv2;
     mats.put(0, i, j, acc);
     mats.put(0, j, i, acc);
@@ -974,13 +975,13 @@ cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, b
   constexpr int smem = GsLayout<MT, NT, HALF>::kTotal;
   if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(a.B * kCL);
+  lc.gridDim = dim3(a.B * cfg.cluster);
   lc.blockDim = dim3(NT);
   lc.dynamicSmemBytes = smem;
   lc.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.x = cfg.cluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
@@ -989,16 +990,16 @@ cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, b
 }
 
 template <typename TY, int MT, bool HALF, bool NEST>
-int gs_clusters_of() {
+int gs_clusters_of(int cl) {
   constexpr int NT = gs_threads<MT>();
   auto fn = k_skinny_gs<TY, MT, NT, HALF, NEST>;
   cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(kCL * 1024);
+  lc.gridDim = dim3(cl * 1024);
   lc.blockDim = dim3(NT);
   lc.dynamicSmemBytes = GsLayout<MT, NT, HALF>::kTotal;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.x = cl;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
@@ -1023,14 +1024,14 @@ cudaError_t gs_launch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, 
 }
 
 template <typename TY, bool NEST>
-int gs_clusters_ty(int m) {
+int gs_clusters_ty(int m, int cl) {
   const int mt = (m + 15) / 16;
   const bool half = m - 16 * (mt - 1) <= 8;
   switch (mt) {
-    case 1: return half ? gs_clusters_of<TY, 1, true, NEST>() : gs_clusters_of<TY, 1, false, NEST>();
-    case 2: return half ? gs_clusters_of<TY, 2, true, NEST>() : gs_clusters_of<TY, 2, false, NEST>();
-    case 3: return gs_clusters_of<TY, 3, false, NEST>();
-    default: return gs_clusters_of<TY, 4, false, NEST>();
+    case 1: return half ? gs_clusters_of<TY, 1, true, NEST>(cl) : gs_clusters_of<TY, 1, false, NEST>(cl);
+    case 2: return half ? gs_clusters_of<TY, 2, true, NEST>(cl) : gs_clusters_of<TY, 2, false, NEST>(cl);
+    case 3: return gs_clusters_of<TY, 3, false, NEST>(cl);
+    default: return gs_clusters_of<TY, 4, false, NEST>(cl);
   }
 }
 
@@ -1044,9 +1045,9 @@ cudaError_t gs_dispatch_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, 
 }
 
 template <bool NEST>
-int gs_clusters_t(int ns_type, int m) {
+int gs_clusters_t(int ns_type, int m, int cl) {
   if (m < 1 || m > 64) return -1;
-  return ns_type == NS_F16 ? gs_clusters_ty<__half, NEST>(m) : gs_clusters_ty<__nv_bfloat16, NEST>(m);
+  return ns_type == NS_F16 ? gs_clusters_ty<__half, NEST>(m, cl) : gs_clusters_ty<__nv_bfloat16, NEST>(m, cl);
 }
 
 }  // namespace gs

@@ -8,6 +8,6 @@ cudaError_t gs_dispatch_nesterov(const KArgs& a, const SkinnyCfg& cfg, cudaStrea
   return gs::gs_dispatch_t<true>(a, cfg, s, prepare);
 }
 
-int gs_max_active_clusters_nesterov(int ns_type, int m) { return gs::gs_clusters_t<true>(ns_type, m); }
+int gs_max_active_clusters_nesterov(int ns_type, int m, int cl) { return gs::gs_clusters_t<true>(ns_type, m, cl); }
 
 }  // namespace muon

@@ -103,7 +103,10 @@ muon_status_t check_options(const muon_plan_options& o) {
   if (o.flags & ~(MUON_FLAG_KEEP_UPDATE | MUON_FLAG_NO_GRAPH | MUON_FLAG_HOST_STAGING |
                   MUON_FLAG_GROUP_TIMING | MUON_FLAG_NESTEROV | MUON_FLAG_MERGE_TRANSPOSED))
     return fail(MUON_ERR_INVALID_ARG, "unknown flag bits 0x%x", o.flags);
-  for (int i = 0; i < 8; ++i)
+  if (o.column_shards != 0 && o.column_shards != 1 && o.column_shards != 2 && o.column_shards != 4 &&
+      o.column_shards != 8)
+    return fail(MUON_ERR_INVALID_ARG, "column_shards must be 0, 1, 2, 4 or 8");
+  for (int i = 0; i < 7; ++i)
     if (o.reserved[i] != 0) return fail(MUON_ERR_INVALID_ARG, "reserved option fields must be 0");
   return MUON_OK;
 }
@@ -203,10 +206,11 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
     if (f32) {
       path = PATH_SIMT;
     } else if (path == PATH_AUTO) {
-      const bool sk = thr > 0 && skinny_config((int32_t)gp.rows, (int32_t)gp.cols, thr, &gp.sk);
+      const bool sk = thr > 0 && skinny_config((int32_t)gp.rows, (int32_t)gp.cols, thr, &gp.sk,
+                                               o.column_shards);
       path = sk ? PATH_SKINNY : PATH_TENSOR;
     } else if (path == PATH_SKINNY) {
-      if (!skinny_config((int32_t)gp.rows, (int32_t)gp.cols, 64, &gp.sk))
+      if (!skinny_config((int32_t)gp.rows, (int32_t)gp.cols, 64, &gp.sk, o.column_shards))
         return fail(MUON_ERR_UNSUPPORTED, "group %zu [%lld,%lld] does not fit the skinny path", g,
                     (long long)gp.rows, (long long)gp.cols);
     }

@@ -64,7 +64,7 @@ extern "C" int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m)
   k.m = (int32_t)m;
   k.ns_type = ns_dtype == MUON_NS_BF16 ? NS_BF16 : NS_F16;
   if (prepare_skinny(k, cfg) != cudaSuccess) return -1;
-  return skinny_max_active_clusters(k.ns_type, (int)m);
+  return skinny_max_active_clusters(k.ns_type, (int)m, cfg.cluster);
 }
 
 extern "C" muon_status_t muon_testing_wait_probe(int32_t arrive, int64_t limit_cycles, void* stream) {

@@ -38,8 +38,10 @@ from .muon_ref import (  # noqa: F401
     muon_update_ref,
     nesterov_input,
     newton_schulz,
+    newton_schulz_sharded,
     ns_polynomial,
     orthogonalize,
     scale_factor,
+    sharded_frobenius_normalize,
     step_coefficients,
 )

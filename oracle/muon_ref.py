@@ -101,6 +101,38 @@ def newton_schulz(X: np.ndarray, k: int, a: float, b: float, c: float,
     return X
 
 
+def newton_schulz_sharded(X: np.ndarray, k: int, a: float, b: float, c: float, shards: int,
+                          schedule=None) -> np.ndarray:
+    """The same k steps with X (rows <= cols) held as `shards` contiguous
+    column blocks, as on ranks that each own a slice of the columns
+    («关于分布式Muon的想法整合及讨论» §6: the Gram matrix is a sum of per-shard
+    partial products, so each round needs one all-reduce of it).  Each step
+    forms every shard's partial Gram, adds them in shard order (the
+    all-reduce), and updates each shard with the same m x m polynomial."""
+    X = np.array(X, dtype=np.float64, copy=True)
+    if X.shape[0] > X.shape[1]:
+        raise ValueError("newton_schulz_sharded expects rows <= cols")
+    parts = [p.copy() for p in np.array_split(X, int(shards), axis=1)]
+    for a_s, b_s, c_s in step_coefficients(k, a, b, c, schedule):
+        A = np.zeros((X.shape[0], X.shape[0]))
+        for p in parts:
+            A = A + p @ p.T
+        B = b_s * A + c_s * (A @ A)
+        parts = [a_s * p + B @ p for p in parts]
+    return np.concatenate(parts, axis=1)
+
+
+def sharded_frobenius_normalize(M: np.ndarray, eps: float, shards: int) -> np.ndarray:
+    """X0 = M / (||M||_F + eps) with ||M||_F^2 summed from per-shard sums of
+    squares in shard order (the sharded normaliser of «关于分布式Muon的想法整合
+    及讨论» §6)."""
+    M = np.asarray(M, np.float64)
+    ss = 0.0
+    for p in np.array_split(M, int(shards), axis=1):
+        ss += float(np.sum(p * p))
+    return M / (math.sqrt(ss) + float(eps))
+
+
 def orthogonalize(Mp: np.ndarray, k: int, a: float, b: float, c: float,
                   eps: float, schedule=None) -> np.ndarray:
     """O = NS_k(M' / (||M'||_F + eps)), iterating on the wide orientation.

@@ -220,3 +220,29 @@ def pin_nesterov(ref):
 
 
 ALL_PINS += [pin_schedule_diagonal, pin_nesterov]
+
+
+def pin_sharded_equals_unsharded(ref, k=5, seed=8):
+    """Column shards change nothing mathematically: the sum of per-shard
+    partial Grams is the Gram matrix, and the per-shard sums of squares add up
+    to ||M||_F^2.  So the sharded normalise + iteration equals the unsharded
+    one (fp64 rounding only), for any shard count, including shards narrower
+    than the matrix is tall."""
+    rng = np.random.default_rng(seed)
+    M = rng.standard_normal((6, 23))
+    X0 = ref.frobenius_normalize(M, 1e-7)
+    want = ref.newton_schulz(X0, k, A_, B_, C_)
+    for t in (1, 2, 3, 8):
+        Xs = ref.sharded_frobenius_normalize(M, 1e-7, t)
+        assert np.max(np.abs(Xs - X0)) <= 1e-15, f"sharded norm t={t}"
+        got = ref.newton_schulz_sharded(Xs, k, A_, B_, C_, t)
+        assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want)), f"sharded NS t={t}"
+    # and against the closed form on a diagonal input split across shards
+    sig = np.array([1.0, 0.6, 0.2])
+    X = np.zeros((3, 7)); X[np.arange(3), np.arange(3)] = sig
+    got = ref.newton_schulz_sharded(X, k, A_, B_, C_, 3)
+    assert np.max(np.abs(np.diag(got[:, :3]) - p_iter(sig, k))) <= 1e-12, "sharded diagonal"
+    assert np.max(np.abs(got[:, 3:])) == 0.0 and np.max(np.abs(got - np.diag(np.diag(got[:, :3])) @ np.eye(3, 7))) <= 1e-12
+
+
+ALL_PINS.append(pin_sharded_equals_unsharded)

@@ -122,7 +122,8 @@ def test_planner_rejects_bad_shapes(lib, bad):
 
 def test_bad_options_are_statuses(lib):
     for kw in [dict(eps=-1.0), dict(eps=float("nan")), dict(skinny_threshold=65),
-               dict(max_streams=17)]:
+               dict(max_streams=17), dict(column_shards=3), dict(column_shards=16),
+               dict(column_shards=-1)]:
         with pytest.raises(pkg.MuonError) as ei:
             pkg.describe([[4, 4]], **kw)
         assert ei.value.status == _capi.MUON_ERR_INVALID_ARG

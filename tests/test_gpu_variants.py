@@ -153,3 +153,37 @@ def test_merged_orientations_fp32_mode():
     errs = check_all(run)
     assert max(errs) <= 1e-4
     run.close()
+
+
+# column shards on the skinny path (plan option column_shards): one CTA per
+# contiguous column shard, partial Grams and sums of squares added in shard
+# order through distributed shared memory
+@pytest.mark.parametrize("t", [1, 4, 8])
+def test_column_shards_match_oracle(t):
+    w = W.custom([[24, 4096], [64, 1000], [2, 40, 3000], [4096, 24], [17, 333]], seed=39)
+    run = GpuRun(w, column_shards=t)
+    assert all(g["path"] == "skinny" for g in run.plan.groups())
+    check_all(run)
+    run.close()
+
+
+def test_column_shards_direct_iteration():
+    w = W.custom([[24, 2048], [48, 1000]], seed=40, ns_steps=70)
+    w.coeffs = SCHEDULE
+    run = GpuRun(w, column_shards=4)
+    check_all(run)
+    run.close()
+
+
+def test_column_shards_batch_invariance_bitwise():
+    """For a fixed shard count a member alone equals the member in a batch."""
+    w = W.custom([[24, 4096]] * 5, seed=41)
+    P, G, M = W.make_tensors(w, "cuda")
+    keep = [[t.clone() for t in ts] for ts in (P, G, M)]
+    full = GpuRun(w, tensors=(P, G, M), column_shards=8)
+    sub = W.custom([w.shapes[3]], seed=0)
+    one = GpuRun(sub, tensors=([keep[0][3]], [keep[1][3]], [keep[2][3]]), column_shards=8)
+    assert np.array_equal(one.p1(0), full.p1(3))
+    assert np.array_equal(one.O(0), full.O(3))
+    one.close()
+    full.close()

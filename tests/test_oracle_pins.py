@@ -50,6 +50,9 @@ MUTANTS = {
                                "return [rows[s] if s < len(rows) else rows[0] for s in range(int(k))]"),
     "nesterov_undamped": ("return np.asarray(G, np.float64) + float(beta) * np.asarray(Mp, np.float64)",
                           "return np.asarray(G, np.float64) + np.asarray(Mp, np.float64)"),
+    "shard_gram_last_only": ("            A = A + p @ p.T", "            A = p @ p.T"),
+    "shard_update_own_gram": ("        parts = [a_s * p + B @ p for p in parts]",
+                              "        parts = [a_s * p + (b_s * (p @ p.T) + c_s * (p @ p.T) @ (p @ p.T)) @ p for p in parts]"),
     "nesterov_on_old_m": ("U = nesterov_input(Mp, G, beta) if nesterov else Mp",
                           "U = nesterov_input(M, G, beta) if nesterov else Mp"),
 }
