@@ -259,6 +259,9 @@ void set_last_error(const char* msg) { g_last_error = msg; }
 
 using namespace muon;
 
+// Chunks of the pipelined host-buffer step (muon_step_host on skinny-only plans).
+constexpr int kHostChunks = 4;
+
 struct muon_plan_s {
   PlanDesc d;
   int device = 0;
@@ -281,6 +284,10 @@ struct muon_plan_s {
   unsigned char* stage_g = nullptr;
   float* stage_m = nullptr;
   std::vector<size_t> stage_off;      // element offset of each parameter
+  // pipelined muon_step_host (skinny-only plans): copy streams and per-chunk events
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t up_ev = nullptr;
+  std::vector<cudaEvent_t> in_ev, run_ev, out_ev;
 };
 
 namespace {
@@ -442,6 +449,12 @@ void destroy_plan(muon_plan_s* p) {
   if (p->cap) cudaStreamDestroy(p->cap);
   if (p->ws) cudaFree(p->ws);
   if (p->pinned) cudaFreeHost(p->pinned);
+  for (auto ev : p->in_ev) cudaEventDestroy(ev);
+  for (auto ev : p->run_ev) cudaEventDestroy(ev);
+  for (auto ev : p->out_ev) cudaEventDestroy(ev);
+  if (p->up_ev) cudaEventDestroy(p->up_ev);
+  if (p->h2d) cudaStreamDestroy(p->h2d);
+  if (p->d2h) cudaStreamDestroy(p->d2h);
   if (p->stage_p) cudaFree(p->stage_p);
   if (p->stage_g) cudaFree(p->stage_g);
   if (p->stage_m) cudaFree(p->stage_m);
@@ -629,6 +642,18 @@ muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
     PLAN_TRY(cudaMalloc(&p->stage_p, tot * p_esize(p)));
     PLAN_TRY(cudaMalloc(&p->stage_g, tot * p_esize(p)));
     PLAN_TRY(cudaMalloc(&p->stage_m, tot * 4));
+    PLAN_TRY(cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking));
+    PLAN_TRY(cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking));
+    PLAN_TRY(cudaEventCreateWithFlags(&p->up_ev, cudaEventDisableTiming));
+    for (int i = 0; i < kHostChunks; ++i) {
+      cudaEvent_t e0, e1, e2;
+      PLAN_TRY(cudaEventCreateWithFlags(&e0, cudaEventDisableTiming));
+      p->in_ev.push_back(e0);
+      PLAN_TRY(cudaEventCreateWithFlags(&e1, cudaEventDisableTiming));
+      p->run_ev.push_back(e1);
+      PLAN_TRY(cudaEventCreateWithFlags(&e2, cudaEventDisableTiming));
+      p->out_ev.push_back(e2);
+    }
   }
   PLAN_TRY(cudaDeviceSynchronize());
 #undef PLAN_TRY
@@ -642,7 +667,7 @@ namespace {
 // (a, b, c) rows (host memory).
 muon_status_t step_impl(muon_plan_t p, void* const* params, const void* const* grads,
                         float* const* momenta, float beta, float lr, float wd, int32_t ns_steps,
-                        const float* coef, int32_t n_coef, void* stream) {
+                        const float* coef, int32_t n_coef, void* stream, bool launch = true) {
   if (!p) return fail(MUON_ERR_INVALID_ARG, "plan is NULL");
   if (!params || !grads || !momenta) return fail(MUON_ERR_INVALID_ARG, "NULL pointer array");
   if (ns_steps < 0 || ns_steps > 1000)
@@ -693,10 +718,121 @@ muon_status_t step_impl(muon_plan_t p, void* const* params, const void* const* g
     CUDA_TRY(cudaMemcpyAsync(p->ws + p->d.off_scalars, host, p->d.pb_bytes, cudaMemcpyHostToDevice, s));
     CUDA_TRY(cudaEventRecord(p->slot_ev[slot], s));
   }
+  if (!launch) return MUON_OK;  // the caller enqueues the kernels itself
   if (p->d.opt.flags & MUON_FLAG_NO_GRAPH) return enqueue_all(p, ns_steps, s, false);
   cudaGraphExec_t exec;
   if (muon_status_t st = get_graph(p, ns_steps, &exec)) return st;
   CUDA_TRY(cudaGraphLaunch(exec, s));
+  return MUON_OK;
+}
+
+// Kernel arguments of members [i0, i0 + cnt) of a skinny group.
+KArgs skinny_sub_args(const KArgs& a, const GroupPlan& g, int64_t i0, int64_t cnt) {
+  KArgs r = a;
+  const int64_t mn = g.m * g.n;
+  r.B = (int32_t)cnt;
+  r.mem = a.mem + i0;
+  r.part = a.part + i0 * a.n_chunks;
+  r.y0 = static_cast<unsigned char*>(a.y0) + i0 * g.sk.ws_bytes;
+  if (a.dbg) r.dbg = a.dbg + i0 * mn;
+  if (a.u) r.u = a.u + i0 * mn;
+  return r;
+}
+
+bool all_skinny(const muon_plan_s* p) {
+  for (const GroupPlan& g : p->d.groups)
+    if (g.path != PATH_SKINNY) return false;
+  return true;
+}
+
+// One cudaMemcpyAsync per run of parameters in [p0, p1) whose host and device
+// buffers are both back to back.
+cudaError_t copy_param_runs(const muon_plan_s* p, int32_t p0, int32_t p1, const void* const* host,
+                            void* const* dev, size_t es, bool to_device, cudaStream_t s) {
+  int32_t i = p0;
+  while (i < p1) {
+    int32_t j = i + 1;
+    size_t bytes = (size_t)param_elems(p->d, i) * es;
+    while (j < p1 && (const unsigned char*)host[j] == (const unsigned char*)host[i] + bytes &&
+           (const unsigned char*)dev[j] == (const unsigned char*)dev[i] + bytes) {
+      bytes += (size_t)param_elems(p->d, j) * es;
+      ++j;
+    }
+    const cudaError_t e =
+        to_device ? cudaMemcpyAsync(dev[i], host[i], bytes, cudaMemcpyHostToDevice, s)
+                  : cudaMemcpyAsync(const_cast<void*>(host[i]), dev[i], bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    i = j;
+  }
+  return cudaSuccess;
+}
+
+// muon_step_host for a plan whose groups all take the skinny path.  The
+// parameters go in up to in_ev.size() chunks of about equal size: a chunk's
+// inputs are copied in on one stream, its members' kernels run on the
+// caller's stream once they have landed, and its results are copied out on
+// a third stream.  So one chunk's copy back overlaps the next chunk's copy
+// in (the host link carries both directions at once), and the kernels hide
+// behind the copies.  Every member gets the same kernels as in a whole-plan
+// step, so its results are the same bits.
+muon_status_t host_step_pipelined(muon_plan_s* p, void* const* hp, const void* const* hg,
+                                  float* const* hm, std::vector<void*>& dp, std::vector<void*>& dg,
+                                  std::vector<float*>& dm, float beta, float lr, float wd,
+                                  int32_t k, float a, float b, float c, cudaStream_t s) {
+  const int32_t np = (int32_t)p->d.param_E.size();
+  const float coef[3] = {a, b, c};
+  // scalars and member pointers (the staging buffers) to the device, on s
+  if (muon_status_t st = step_impl(p, dp.data(), (const void* const*)dg.data(), dm.data(), beta, lr,
+                                   wd, k, coef, 1, s, false))
+    return st;
+  CUDA_TRY(cudaEventRecord(p->up_ev, s));
+  CUDA_TRY(cudaStreamWaitEvent(p->h2d, p->up_ev, 0));
+  // chunk boundaries: parameter ranges of about equal element counts
+  const int nch = std::min<int>((int)p->in_ev.size(), np);
+  int64_t total = 0;
+  for (int32_t i = 0; i < np; ++i) total += param_elems(p->d, i);
+  std::vector<int32_t> cut(nch + 1, np);
+  cut[0] = 0;
+  {
+    int64_t acc = 0;
+    int ci = 1;
+    for (int32_t i = 0; i < np && ci < nch; ++i) {
+      acc += param_elems(p->d, i);
+      if (acc * nch >= total * ci) cut[ci++] = i + 1;
+    }
+  }
+  const size_t pes = p_esize(p);
+  std::vector<const void*> hpc(hp, hp + np), hmc(hm, hm + np);
+  std::vector<void*> dmv(dm.begin(), dm.end());
+  for (int ci = 0; ci < nch; ++ci) {
+    const int32_t p0 = cut[ci], p1 = cut[ci + 1];
+    if (p0 >= p1) continue;
+    CUDA_TRY(copy_param_runs(p, p0, p1, hpc.data(), dp.data(), pes, true, p->h2d));
+    CUDA_TRY(copy_param_runs(p, p0, p1, hg, dg.data(), pes, true, p->h2d));
+    CUDA_TRY(copy_param_runs(p, p0, p1, hmc.data(), dmv.data(), 4, true, p->h2d));
+    CUDA_TRY(cudaEventRecord(p->in_ev[ci], p->h2d));
+    CUDA_TRY(cudaStreamWaitEvent(s, p->in_ev[ci], 0));
+    for (const GroupPlan& g : p->d.groups) {
+      int64_t i0 = -1, cnt = 0;  // the chunk's members of g are contiguous in it
+      for (int64_t i = 0; i < g.batch; ++i) {
+        const int32_t pi = p->d.member_param[g.first_member + i];
+        if (pi >= p0 && pi < p1) {
+          if (i0 < 0) i0 = i;
+          ++cnt;
+        }
+      }
+      if (!cnt) continue;
+      const cudaError_t e = launch_skinny(skinny_sub_args(make_args(p, g), g, i0, cnt), g.sk, k, s);
+      if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    CUDA_TRY(cudaEventRecord(p->run_ev[ci], s));
+    CUDA_TRY(cudaStreamWaitEvent(p->d2h, p->run_ev[ci], 0));
+    CUDA_TRY(copy_param_runs(p, p0, p1, hpc.data(), dp.data(), pes, false, p->d2h));
+    CUDA_TRY(copy_param_runs(p, p0, p1, hmc.data(), dmv.data(), 4, false, p->d2h));
+  }
+  CUDA_TRY(cudaEventRecord(p->out_ev[0], p->d2h));
+  CUDA_TRY(cudaStreamWaitEvent(s, p->out_ev[0], 0));
+  CUDA_TRY(cudaStreamSynchronize(s));
   return MUON_OK;
 }
 
@@ -757,6 +893,8 @@ muon_status_t muon_step_host(muon_plan_t p, void* const* hp, const void* const* 
     return MUON_OK;
   };
   muon_status_t st;
+  if (all_skinny(p) && !p->in_ev.empty() && np > 1)
+    return host_step_pipelined(p, hp, hg, hm, dp, dg, dm, beta, lr, wd, ns_steps, a, b, c, s);
   if ((st = copy_runs([&](int32_t i) { return (const void*)hp[i]; },
                       [&](int32_t i) { return (const void*)dp[i]; }, pes, cudaMemcpyHostToDevice)))
     return st;
