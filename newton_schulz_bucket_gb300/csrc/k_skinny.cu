@@ -1,14 +1,15 @@
 // Skinny path, direct iteration: Newton-Schulz for m = min(rows, cols) <= 64,
-// one pass over the m x n iterate per step.  It serves 32 < m <= 64 and step
-// counts beyond the Gram-space kernel's range (k_skinny_gs.cu); the host
-// functions at the end choose between the two.
+// one pass over the m x n iterate per step.  It serves step counts beyond the
+// Gram-space kernel's range (k_skinny_gs.cuh); the host functions at the end
+// choose between the two.
 //
 // «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: for
 // shapes such as [24, 10240] the per-parameter iteration is dominated by host
 // dispatch, small allocations and synchronisation; batching every member of a
 // shape into one launch removes that (Fig. 7).  After the streaming momentum
-// kernel (k_elementwise.cu), k_skinny_ns runs one cluster of kCL CTAs per
-// member.  CTA r owns columns [r W, (r+1) W) of the wide m x n iterate.  The
+// kernel (k_elementwise.cu), k_skinny_ns runs one cluster of CL CTAs per
+// member (the plan's column shards, 2 by default).  CTA r owns columns
+// [r W, (r+1) W) of the wide m x n iterate.  The
 // iterate is kept in an L2-resident workspace in the exact register order of
 // mma.sync fragments, so each pass is: load fragments -> Y <- Q Y (mma.sync,
 // with movmatrix transposes for the B operand) -> accumulate the next Gram
