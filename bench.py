@@ -417,9 +417,15 @@ def main():
         ent = {"shape": shp, "batch": info["batch"], "path": info["path"], "ms": gms}
         if gms:
             ent["matrices_per_s"] = info["batch"] / (gms / 1e3)
-            if info["path"] == "skinny":
+            # the roofline that bounds the group: HBM when its dense FLOPs per
+            # compulsory byte fall below the ridge (peak FLOP/s / peak bytes/s;
+            # every skinny group and small-m tensor groups such as [128, 4096]),
+            # else the tensor cores
+            ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+            if info["path"] == "skinny" or gf / gb < ridge:
                 ach = gb / (gms / 1e3) / 1e9
-                ent.update({"GB_s": ach, "roofline_frac": ach / peaks["hbm_gbs"], "bound": "hbm"})
+                ent.update({"GB_s": ach, "roofline_frac": ach / peaks["hbm_gbs"], "bound": "hbm",
+                            "flop_per_byte": gf / gb})
             else:
                 # TFLOP/s of the dense count (algorithmic); the executed rate
                 # counts only the tiles the symmetric products compute
@@ -433,14 +439,18 @@ def main():
 
     dom = max(range(len(groups)), key=lambda g: per_group[g]["ms"] or 0)
     dg = per_group[dom]
-    if dg["path"] == "skinny":
-        gram_space = w.ns_steps <= 64
-        kfile = "k_skinny_gs.cuh" if gram_space else "k_skinny.cu"
+    if dg.get("bound") == "hbm":
+        if dg["path"] == "skinny":
+            gram_space = w.ns_steps <= 64
+            kfile = "k_skinny_gs.cuh" if gram_space else "k_skinny.cu"
+            kernel = ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"
+                      if gram_space else "k_momentum_partial + k_skinny_ns")
+            traffic = ncu_traffic(kfile, w.name)
+        else:
+            kernel = f"group {dg['shape']} chain (k_tc_gemm and the elementwise passes)"
+            traffic = None
         roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": dg.get("roofline_frac"),
-                "kernel": ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"
-                           if gram_space else "k_momentum_partial + k_skinny_ns"),
-                "traffic": ncu_traffic(kfile, w.name),
+                "frac": dg.get("roofline_frac"), "kernel": kernel, "traffic": traffic,
                 "peak_source": peaks["source"] + " hbm_gbs (burst copy)"}
     else:
         roof = {"bound": "tensor", "achieved": dg.get("TFLOP_s"), "peak": peaks["bf16_tflops_sustained"],
