@@ -13,6 +13,33 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Eight consecutive elements (16- or 32-byte aligned) to / from fp32.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* f) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = to_f32(h[e]);
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float* f) {
+  if constexpr (sizeof(T) == 4) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  } else {
+    uint4 u;
+    T* h = reinterpret_cast<T*>(&u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] = from_f32<T>(f[e]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+}
+
 // One CTA = one fixed chunk of one member: M' = beta M + G (stored), and the
 // chunk's sum of squares of X = M' (Nesterov: X = U = G + beta M') by a
 // fixed-order tree into part[b][chunk]; with a.u set, U is stored there too.
@@ -133,6 +160,31 @@ __global__ void __launch_bounds__(kThreads) k_normalize_cast(KArgs a, TY* __rest
   const bool T = a.mem[b].T != 0;
   const int rows = T ? a.n : a.m, cols = T ? a.m : a.n;
   const int r0 = (T ? blockIdx.x : blockIdx.y) * 64, c0 = (T ? blockIdx.y : blockIdx.x) * 64;
+  // Untransposed member, whole tile width, 8-element alignment: each thread
+  // moves rows (t / 8) and (t / 8 + 32), columns 8 (t % 8) .. + 7, as vectors.
+  if (!T && c0 + 64 <= cols && cols % 8 == 0 && a.n_pitch % 8 == 0 && aligned16(Mp) && aligned16(Yb) &&
+      (!nest || aligned16(Gp))) {
+    const int cc = (threadIdx.x & 7) * 8, rr0 = threadIdx.x >> 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + rr0 + 32 * h;
+      if (r >= rows) continue;
+      const int64_t o = (int64_t)r * cols + c0 + cc;
+      float x[8];
+      load8(Mp + o, x);
+      if (nest) {
+        float g[8];
+        if (a.mode_f32) load8(static_cast<const float*>(Gp) + o, g);
+        else load8(static_cast<const __nv_bfloat16*>(Gp) + o, g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = fmaf(beta, x[e], g[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= inv;
+      store8(Yb + (int64_t)r * a.n_pitch + c0 + cc, x);
+    }
+    return;
+  }
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
   for (int rr = ty; rr < 64; rr += 4) {
     const int r = r0 + rr, c = c0 + tx;
@@ -179,6 +231,31 @@ __global__ void __launch_bounds__(kThreads) k_write(KArgs a, const TY* __restric
   const bool T = mp.T != 0;
   const int rows = T ? a.n : a.m, cols = T ? a.m : a.n;
   const int r0 = (T ? blockIdx.x : blockIdx.y) * 64, c0 = (T ? blockIdx.y : blockIdx.x) * 64;
+  float* dbg = a.dbg ? a.dbg + (int64_t)b * a.m * a.n : nullptr;
+  // Untransposed member, whole tile width, 8-element alignment: vectors, as in
+  // k_normalize_cast (the same arithmetic per element as below).
+  if (!T && c0 + 64 <= cols && cols % 8 == 0 && a.n_pitch % 8 == 0 && aligned16(P) && aligned16(Yb) &&
+      (!dbg || aligned16(dbg))) {
+    const int cc = (threadIdx.x & 7) * 8, rr0 = threadIdx.x >> 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + rr0 + 32 * h;
+      if (r >= rows) continue;
+      const int64_t idx = (int64_t)r * cols + c0 + cc;
+      float y[8], pv[8], w[8];
+      load8(Yb + (int64_t)r * a.n_pitch + c0 + cc, y);
+      load8(P + idx, pv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = fmaf(-coef, y[e], pv[e] * decay);
+      store8(P + idx, w);
+      if (dbg) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = y[e] * inv_alpha;
+        store8(dbg + idx, w);
+      }
+    }
+    return;
+  }
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
   if (T) {
     // stage the Y tile Y[c0..c0+64)[r0..r0+64) so reads are coalesced along r
@@ -188,7 +265,6 @@ __global__ void __launch_bounds__(kThreads) k_write(KArgs a, const TY* __restric
     }
     __syncthreads();
   }
-  float* dbg = a.dbg ? a.dbg + (int64_t)b * a.m * a.n : nullptr;
   for (int rr = ty; rr < 64; rr += 4) {
     const int r = r0 + rr, c = c0 + tx;
     if (r >= rows || c >= cols) continue;
