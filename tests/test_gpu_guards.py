@@ -99,3 +99,31 @@ def test_resume_through_host_equals_continuous(shapes):
     c.close()
     for x, y in zip(P + M, P3 + M3):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("shapes", [[[24, 4096]] * 6, [[64, 1000]] * 4, [[256, 512]] * 3, [[2, 130, 384]]],
+                         ids=["gram_space", "gram_space_m64", "tensor", "tensor_experts"])
+def test_nonfinite_member_stays_isolated(shapes):
+    """A NaN in one member's gradient propagates into that member only (no
+    special casing, as stated); every other member gives the same bits as in
+    a run without it."""
+    w = W.custom(shapes, seed=53)
+    P, G, M = W.make_tensors(w, "cuda")
+    clean = [[t.clone() for t in ts] for ts in (P, G, M)]
+    bad_param, bad_expert = (1, 0) if len(shapes) > 1 else (0, 1)
+    target = G[bad_param][bad_expert] if len(shapes[bad_param]) == 3 else G[bad_param]
+    target[3, 5] = float("nan")
+    for tensors in ((P, G, M), clean):
+        plan = pkg.MuonPlan(w.shapes)
+        plan.step(*tensors, w.beta, w.lr, w.wd, 5)
+        torch.cuda.synchronize()
+        plan.close()
+    for i, s in enumerate(w.shapes):
+        E = s[0] if len(s) == 3 else 1
+        for e in range(E):
+            sl = (lambda t: t[e]) if len(s) == 3 else (lambda t: t)
+            if (i, e) == (bad_param, bad_expert):
+                assert torch.isnan(sl(M[i])).any() and torch.isnan(sl(P[i]).float()).any()
+            else:
+                assert torch.equal(sl(P[i]), sl(clean[0][i])), (i, e)
+                assert torch.equal(sl(M[i]), sl(clean[2][i])), (i, e)
