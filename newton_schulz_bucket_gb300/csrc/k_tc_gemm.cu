@@ -121,7 +121,11 @@ struct TcSmem {
   static constexpr uint32_t kB = BN * BK * 2;          // 32 KB (BN = 256)
   static constexpr uint32_t kStage = kA + kB;
   static constexpr uint32_t kBars = kStages * kStage;  // barrier area offset
-  static constexpr uint32_t kTotal = kBars + 256 + 1024;  // + barriers + alignment slack
+  // GRAM / POLY: per epilogue warp a 32 x 32 block of 16-bit values as 32 rows
+  // of 17 words (a padded row keeps the column reads free of bank conflicts)
+  static constexpr uint32_t kEpi = kBars + 256;
+  static constexpr uint32_t kEpiBytes = 4 * 32 * 17 * 4;
+  static constexpr uint32_t kTotal = kEpi + kEpiBytes + 1024;  // + alignment slack
 };
 
 __device__ __forceinline__ void decode_tile(int t, const TcArgs& p, int& b, int& tm, int& tn) {
@@ -201,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // bars: full[kStages], empty[kStages], tfull[2], tempty[2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* epi = reinterpret_cast<uint32_t*>(smem + L::kEpi);  // GRAM / POLY mirror staging
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = saddr(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -304,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(tfull(acc), aph, abort_flag, p.err, 8)) break;
       tc_fence_after();
       const int row = tm * BM + row_in_tile;
+      const int row0 = tm * BM + quarter * 32;  // this warp's first row
       TY* crow = static_cast<TY*>(p.C) + (int64_t)b * p.sC + (int64_t)row * p.ldc;
       const TY* arow = OP == TC_POLY ? static_cast<const TY*>(p.aux) + (int64_t)b * p.sC +
                                            (int64_t)row * p.ldc
@@ -315,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (uint32_t)(acc * BN + ch * 32);
         tmem_ld32(taddr, r);
         const int col0 = tn * BN + ch * 32;
-        if (row >= p.M || col0 >= p.N) continue;
+        if (col0 >= p.N) continue;  // the same for the whole warp
+        const bool live = row < p.M;
+        if (OP == TC_UPDATE && !live) continue;
         const int nvalid = min(32, p.N - col0);
         float v[32];
 #pragma unroll
@@ -325,7 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] *= p.scale;
         } else if (OP == TC_POLY) {
           float av[32];
-          if (nvalid == 32) {
+          if (!live) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) av[i] = 0.f;
+          } else if (nvalid == 32) {
             const uint4* src = reinterpret_cast<const uint4*>(arow + col0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -347,19 +358,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (OP == TC_UPDATE) {
           store_row32<TY>(crow + col0, v, nvalid);
         } else {
-          // on and above the diagonal in place, strictly above also at (j, i);
-          // for a fixed i the warp's lanes (rows) write one contiguous run
-          if (col0 >= row) {
-            store_row32<TY>(crow + col0, v, nvalid);
-          } else if (col0 + 31 >= row) {
+          // on and above the diagonal in place
+          if (live) {
+            if (col0 >= row) {
+              store_row32<TY>(crow + col0, v, nvalid);
+            } else if (col0 + 31 >= row) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid && col0 + i >= row) crow[col0 + i] = from_f32<TY>(v[i]);
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid && col0 + i >= row) crow[col0 + i] = from_f32<TY>(v[i]);
+            }
           }
-          TY* cbase = static_cast<TY*>(p.C) + (int64_t)b * p.sC;
+          // strictly above also at (j, i): the warp's 32 x 32 block goes
+          // through shared memory, so that lane j then writes row col0 + j of
+          // the mirror, 32 values from column row0, as 16-byte stores
+          uint32_t* sw = epi + quarter * (32 * 17);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nvalid && col0 + i > row) cbase[(int64_t)(col0 + i) * p.ldc + row] = from_f32<TY>(v[i]);
+          for (int q = 0; q < 16; ++q) {
+            const TY lo = from_f32<TY>(v[2 * q]), hi = from_f32<TY>(v[2 * q + 1]);
+            sw[lane * 17 + q] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
+                                ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+          }
+          __syncwarp();
+          const int orow = col0 + lane;
+          if (lane < nvalid && orow > row0) {
+            uint32_t w[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const uint32_t a0 = sw[(2 * q) * 17 + (lane >> 1)], a1 = sw[(2 * q + 1) * 17 + (lane >> 1)];
+              const uint32_t h0 = (lane & 1) ? (a0 >> 16) : (a0 & 0xffffu);
+              const uint32_t h1 = (lane & 1) ? (a1 >> 16) : (a1 & 0xffffu);
+              w[q] = h0 | (h1 << 16);
+            }
+            TY* dst = static_cast<TY*>(p.C) + (int64_t)b * p.sC + (int64_t)orow * p.ldc + row0;
+            if (col0 >= row0 + 32 && row0 + 32 <= p.M) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            } else {
+              const TY* h = reinterpret_cast<const TY*>(w);
+#pragma unroll
+              for (int r2 = 0; r2 < 32; ++r2)
+                if (orow > row0 + r2 && row0 + r2 < p.M) dst[r2] = h[r2];
+            }
+          }
+          __syncwarp();  // the block is overwritten by the next chunk
         }
       }
       tc_fence_before();
