@@ -79,20 +79,6 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
   return u;
 }
 
-// 16-byte global accesses.  Plain (non-volatile) so the compiler may batch
-// independent loads; in-place updates stay ordered through data dependences.
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {  // read-only data
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ uint4 ld_cs(const void* p) {   // read once, then overwritten
-  return __ldcs(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ void st_cs(void* p, const uint4& v) {
-  __stcs(reinterpret_cast<uint4*>(p), v);
-}
-__device__ __forceinline__ void st_u4(void* p, const uint4& v) {  // re-read soon: keep in L2
-  *reinterpret_cast<uint4*>(p) = v;
-}
 // L2 eviction priorities.  A policy from createpolicy rides on each access;
 // evict_last lines outlive evict_normal / evict_first ones under pressure.
 __device__ __forceinline__ uint64_t l2_evict_first() {

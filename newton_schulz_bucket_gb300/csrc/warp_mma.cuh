@@ -63,11 +63,6 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, i
                "r"(src_bytes), "l"(pol)
                : "memory");
 }
-__device__ __forceinline__ void cp_async8_hint(uint32_t dst, const void* src, int src_bytes, uint64_t pol) {
-  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2, %3;" ::"r"(dst), "l"(src),
-               "r"(src_bytes), "l"(pol)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
