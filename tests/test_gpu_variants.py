@@ -187,3 +187,16 @@ def test_column_shards_batch_invariance_bitwise():
     assert np.array_equal(one.O(0), full.O(3))
     one.close()
     full.close()
+
+
+@pytest.mark.parametrize("k", [5, 70])
+def test_all_options_together(k):
+    """Nesterov, a per-step schedule, merged orientations and 4 column shards
+    at once, on skinny (Gram-space or direct) and tensor groups."""
+    w = W.custom([[24, 4096], [4096, 24], [2, 64, 1000], [256, 512], [512, 256]], seed=42, ns_steps=k)
+    w.nesterov = True
+    w.coeffs = SCHEDULE
+    run = GpuRun(w, merge_transposed=True, column_shards=4)
+    assert len(run.plan.groups()) == 3
+    check_all(run)
+    run.close()
