@@ -1,0 +1,67 @@
+"""Host-side helpers of bench.py and the workload module (CPU only): the
+algorithmic work counts, the executed share of the symmetric GEMMs, the
+roofline ridge, and the per-group mixed-bag workloads."""
+import math
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from newton_schulz_bucket_gb300 import workloads as W  # noqa: E402
+
+
+def test_algorithmic_work_counts():
+    # c2: 14 B per element, dense k (4 m^2 n + 2 m^3) per matrix
+    w = W.get("c2_skinny_74x24x10240")
+    b, f = bench.algorithmic_work(w.shapes, w.mode, w.ns_steps)
+    assert b == 74 * 24 * 10240 * 14
+    assert f == 74 * 5 * (4 * 24 * 24 * 10240 + 2 * 24 ** 3)
+    # an expert tensor counts E matrices; a tall matrix iterates on its transpose
+    b, f = bench.algorithmic_work([[3, 512, 2048], [2048, 512]], "bf16", 2)
+    assert b == 4 * 512 * 2048 * 14
+    assert f == 4 * 2 * (4 * 512 * 512 * 2048 + 2 * 512 ** 3)
+
+
+def test_executed_flop_fraction():
+    # m = 4096, BN = 256: 272 of the 512 tiles of each symmetric product
+    m, n = 4096, 12288
+    sym = 272 / 512
+    want = (sym * (2 * m * m * n + 2 * m ** 3) + 2 * m * m * n) / (4 * m * m * n + 2 * m ** 3)
+    assert bench.executed_flop_fraction(m, n) == pytest.approx(want, rel=1e-12)
+    assert bench.executed_flop_fraction(n, m) == pytest.approx(want, rel=1e-12)
+    # one tile per product: nothing to skip
+    assert bench.executed_flop_fraction(128, 4096) == 1.0
+    # square: between 2/3 and 1
+    f = bench.executed_flop_fraction(7168, 7168)
+    assert 2 / 3 < f < 0.7
+
+
+def test_roofline_ridge_splits_the_mixed_bag():
+    """Groups whose dense FLOPs per compulsory byte fall below the ridge
+    (measured bf16 rate / copy rate) are HBM-bound: the skinny shapes and
+    [128, 4096]; [512, 2048] and larger are tensor-bound."""
+    peaks = bench.load_peaks()
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    intensity = {}
+    for s in W.C5_SHAPES:
+        b, f = bench.algorithmic_work([s], "bf16", 5)
+        intensity[tuple(s)] = f / b
+    for s in ([24, 10240], [64, 7168], [128, 4096]):
+        assert intensity[tuple(s)] < ridge, s
+    for s in ([512, 2048], [1024, 1024], [4096, 4096], [7168, 7168]):
+        assert intensity[tuple(s)] > ridge, s
+
+
+def test_mixed_bag_group_workloads():
+    full = W.get("c5_mixed_1000")
+    counts = W.c5_counts(5)
+    for s, n in zip(W.C5_SHAPES, counts):
+        g = W.get(f"c5_group_{s[0]}x{s[1]}")
+        assert g.shapes == [s] * n and len(g.g_std) == n
+    assert sum(counts) == 1000 == len(full.shapes)
+    with pytest.raises(KeyError):
+        W.get("c5_group_3x3")
