@@ -20,20 +20,25 @@ def _transpose(X):
     return [list(col) for col in zip(*X)]
 
 
-def naive_update(P, G, M, beta, lr, wd, k, a, b, c, eps, s):
-    """Returns (P', M', O) as nested lists; s is the shape scale."""
+def naive_update(P, G, M, beta, lr, wd, k, a, b, c, eps, s, nesterov=False, rows_abc=None):
+    """Returns (P', M', O) as nested lists; s is the shape scale.  With
+    nesterov the iteration starts from U = G + beta M' (M' is still returned);
+    rows_abc, if given, holds per-step (a, b, c) rows, the last repeating."""
     rows, cols = len(P), len(P[0])
     Mp = [[beta * M[i][j] + G[i][j] for j in range(cols)] for i in range(rows)]
+    U = [[G[i][j] + beta * Mp[i][j] for j in range(cols)] for i in range(rows)] if nesterov else Mp
     sq = 0.0
     for i in range(rows):
         for j in range(cols):
-            sq += Mp[i][j] * Mp[i][j]
+            sq += U[i][j] * U[i][j]
     inv = 1.0 / (math.sqrt(sq) + eps)
-    X = [[Mp[i][j] * inv for j in range(cols)] for i in range(rows)]
+    X = [[U[i][j] * inv for j in range(cols)] for i in range(rows)]
     tr = rows > cols
     if tr:
         X = _transpose(X)
-    for _ in range(k):
+    for step in range(k):
+        if rows_abc:
+            a, b, c = rows_abc[min(step, len(rows_abc) - 1)]
         A = _matmul_nt(X, X)                      # A = X X^T
         AA = _matmul_nt(A, _transpose(A))         # A A
         m = len(A)

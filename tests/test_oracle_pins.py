@@ -153,3 +153,20 @@ def test_ns_band_for_normalised_inputs():
 def test_package_exports():
     assert oracle.NS_COEFFS_QUINTIC == (A_, B_, C_)
     assert set(oracle.SCALE_MODES) == {"sqrt_aspect", "rms_0_2", "none"}
+
+
+def test_naive_loops_match_nesterov_and_schedule():
+    """The pure-Python loops and the NumPy oracle agree on the Nesterov input
+    and on a per-step schedule (tall matrix: the transposed iteration)."""
+    from oracle_pins import SCHEDULE
+    rng = np.random.default_rng(9)
+    P, G, M = (rng.standard_normal((12, 5)) for _ in range(3))
+    s = muon_ref.scale_factor(12, 5)
+    for nest, sched in ((True, None), (False, SCHEDULE), (True, SCHEDULE)):
+        rP, rM, rO = muon_ref.muon_update_ref(P, G, M, 0.9, 0.05, 0.1, 6, A_, B_, C_, 1e-7, "sqrt_aspect",
+                                              nest, sched)
+        nP, nM, nO = naive_update(P.tolist(), G.tolist(), M.tolist(), 0.9, 0.05, 0.1, 6, A_, B_, C_, 1e-7, s,
+                                  nesterov=nest, rows_abc=sched)
+        assert np.max(np.abs(np.array(nO) - rO)) <= 1e-12
+        assert np.max(np.abs(np.array(nP) - rP)) <= 1e-12
+        assert np.max(np.abs(np.array(nM) - rM)) == 0.0
