@@ -132,8 +132,12 @@ typedef struct {
   uint32_t flags;            /* MUON_FLAG_*                                        */
   int32_t path_override;     /* muon_path_t for every group; AUTO = choose         */
   int32_t max_streams;       /* groups run on up to this many graph branches; 0=4  */
-  int32_t column_shards;     /* skinny path: CTAs per member, each owning one      */
-                             /* contiguous column shard (1, 2, 4 or 8; 0 = 2)      */
+  int32_t column_shards;     /* skinny path: CTAs per member (1, 2, 4 or 8; 0 = 2), */
+                             /* each owning one contiguous column shard; their     */
+                             /* partial Grams and sums of squares are added in     */
+                             /* shard order («关于分布式Muon的想法整合及讨论» §6). */
+                             /* Bits depend on it (summation order), never on the  */
+                             /* batch; more shards help small batches fill the GPU */
   int32_t reserved[7];       /* must be zero                                       */
 } muon_plan_options;
 
