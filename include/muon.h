@@ -59,7 +59,7 @@ typedef struct muon_plan_s* muon_plan_t;
 typedef enum {
   MUON_OK = 0,
   MUON_ERR_INVALID_ARG = 1,  /* bad shape, null pointer, bad option        */
-  MUON_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run        */
+  MUON_ERR_UNSUPPORTED = 2,  /* valid request the library cannot run      */
   MUON_ERR_OOM = 3,          /* device or pinned-host allocation failed    */
   MUON_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed          */
   MUON_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out (see check) */

@@ -13,7 +13,7 @@ from typing import Dict, List, Sequence, Tuple
 
 import numpy as np
 
-# Quintic coefficients (a, b, c) used by every workload of this build.  The
+# Quintic coefficients (a, b, c) used by every seeded workload.  The
 # pages print no coefficients (the formula block of «关于分布式Muon的想法整合及
 # 讨论» §2 was lost in extraction); these are the values the workloads fix and
 # every call takes them as arguments anyway.
