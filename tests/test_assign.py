@@ -6,7 +6,8 @@ rank; the list-scheduling bound (busiest rank <= total/R + (1 - 1/R) * largest
 member); on small cases the optimum found by brute force over every
 assignment, with Graham's longest-processing-time-first bound (<= (4/3 -
 1/(3R)) times that optimum); equal members spread evenly; experts of a 3-D
-parameter assigned one by one; the result is a function of its inputs only.
+parameter assigned one by one; the result is a function of its inputs only,
+so two gloo ranks that run it on their own agree and partition the members.
 """
 import itertools
 import math
@@ -81,3 +82,54 @@ def test_bad_arguments_are_statuses():
     sh = pkg._shapes(MIXED)
     o = pkg._options()
     assert L.muon_plan_assign(sh, len(MIXED), o, 5, 4, None, 0, None, None) == _capi.MUON_ERR_INVALID_ARG
+
+
+def _assign_rank(rank, port, q):
+    import os
+    import sys
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch
+    import torch.distributed as dist
+    import newton_schulz_bucket_gb300 as p
+    from newton_schulz_bucket_gb300 import workloads as W
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    r = p.assign_owners(W.get("c5_mixed_1000").shapes, 2)
+    mine = torch.tensor([i for i, o in enumerate(r["owner"]) if o == rank], dtype=torch.int64)
+    owners = torch.tensor(r["owner"], dtype=torch.int64)
+    got = [torch.zeros_like(owners) for _ in range(2)]
+    dist.all_gather(got, owners)
+    n = torch.tensor([mine.numel()], dtype=torch.int64)
+    counts = [torch.zeros_like(n) for _ in range(2)]
+    dist.all_gather(counts, n)
+    dist.destroy_process_group()
+    q.put((rank, bool(torch.equal(got[0], got[1])), mine.tolist(), [int(c) for c in counts],
+           len(r["owner"])))
+
+
+def test_two_gloo_ranks_agree_on_owners():
+    """Each replica runs the planner on its own; with no exchange of the
+    result they must agree, and their owned sets must partition the members."""
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_assign_rank, args=(r, port, q)) for r in range(2)]
+    for pr in procs:
+        pr.start()
+    for pr in procs:
+        pr.join(timeout=120)
+    for pr in procs:
+        if pr.is_alive():
+            pr.kill()
+    assert all(pr.exitcode == 0 for pr in procs)
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert all(agree for _, agree, _, _, _ in res)
+    n = res[0][4]
+    assert n == 1000
+    owned = res[0][2] + res[1][2]
+    assert sorted(owned) == list(range(n))
+    assert res[0][3] == [len(res[0][2]), len(res[1][2])]
