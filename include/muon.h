@@ -73,7 +73,11 @@ typedef enum { MUON_MODE_BF16 = 0, MUON_MODE_FP32 = 1 } muon_mode_t;
 
 /* Operand type of the Newton-Schulz products in MUON_MODE_BF16.  FP16 (the
  * default) keeps 3 more mantissa bits at the same tensor-core rate; BF16
- * rounds X, A and the polynomial matrix to bf16 (larger error, grows with k). */
+ * rounds X, A and the polynomial matrix to bf16, an error that grows with k.
+ * With the roundings emulated against the fp64 oracle on Gaussian momenta,
+ * the relative Frobenius error of O is about 2e-3 for FP16 up to k = 10 and
+ * for BF16 on the skinny path (the data is rounded once); BF16 on the tensor
+ * path is about 1.2e-2 at k = 5 and 2.5e-2 to 3e-2 at k = 10. */
 typedef enum { MUON_NS_FP16 = 0, MUON_NS_BF16 = 1 } muon_ns_dtype_t;
 
 /* Shape-dependent scale s(rows, cols) of the update (a reading; the pages
