@@ -160,16 +160,24 @@ def allmax(world, v):
 
 
 def oracle_time(w, members, host_inputs):
-    """Seconds the CPU oracle needs for `members` (list of (param, expert))."""
+    """(wall seconds, process CPU seconds) the CPU oracle needs for `members`
+    (list of (param, expert)); CPU over wall is the number of host threads
+    it kept busy on average (NumPy's BLAS may use several)."""
     import numpy as np
     from oracle import muon_ref
     f32 = lambda v: float(np.float32(v))
     a, b, c = (f32(v) for v in w.coeffs)
-    t0 = time.perf_counter()
-    for (i, e) in members:
-        P, G, M = host_inputs(i, e)
+    inputs = [host_inputs(i, e) for (i, e) in members]
+    t0, c0 = time.perf_counter(), time.process_time()
+    for P, G, M in inputs:
         muon_ref.muon_update_ref(P, G, M, f32(w.beta), f32(w.lr), f32(w.wd), w.ns_steps, a, b, c)
-    return time.perf_counter() - t0
+    return time.perf_counter() - t0, time.process_time() - c0
+
+
+def busy_cores(wall, cpu):
+    """Host threads the oracle used: its CPU time over its wall time, rounded
+    up (at least 1)."""
+    return max(1, math.ceil(cpu / wall - 0.05)) if wall > 0 else 1
 
 
 def sample_members(w, budget_s=12.0):
@@ -256,16 +264,17 @@ def run_reference(args, w, world, rank):
     get = host_member_inputs(w)
     for _ in range(args.warmup):
         oracle_time(w, members[:1], get)
-    times = [oracle_time(w, members, get) for _ in range(args.steps)]
-    per_step = statistics.mean(times) / frac  # extrapolated to the whole workload
+    runs = [oracle_time(w, members, get) for _ in range(args.steps)]
+    per_step = statistics.mean(t for t, _ in runs) / frac  # extrapolated to the whole workload
     value, unit = headline(w, byts, flops, per_step)
-    cores = os.cpu_count()
+    cores = busy_cores(sum(t for t, _ in runs), sum(c for _, c in runs))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "ns_steps": w.ns_steps},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores,
+                             "host_cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{len(members)} of {round(len(members) / frac)} matrices "
                                        "per step, extrapolated linearly by matrix count"},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -472,9 +481,11 @@ def main():
         members = sample_members(w, budget_s=12.0)
         frac = len(members) / sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
         get = host_member_inputs(w)
-        t = oracle_time(w, members, get) / frac
+        wall, cpu_s = oracle_time(w, members, get)
+        t = wall / frac
         cv, cu = headline(w, byts, flops, t)
-        cpu = {"value": cv, "unit": cu, "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": cv, "unit": cu, "cores": busy_cores(wall, cpu_s),
+               "host_cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{len(members)} matrices of the workload, extrapolated by matrix count",
                "ms_per_step": t * 1e3}
 
