@@ -206,8 +206,12 @@ class MuonPlan:
 
     def step_host(self, params, grads, momenta, beta, lr, wd, ns_steps=5, coeffs=QUINTIC,
                   stream=None) -> None:
-        """The same step on host tensors (copied in and out by the library)."""
+        """The same step on host tensors (copied in and out by the library),
+        for one (a, b, c) triple."""
         import torch
+        if len(coeffs) != 3 or isinstance(coeffs[0], (tuple, list)):
+            raise ValueError("step_host takes one (a, b, c) triple; per-step schedules go "
+                             "through step()")
         pd = self._pdtype()
         P = self._ptrs(params, "params", pd, "cpu")
         G = self._ptrs(grads, "grads", pd, "cpu")
