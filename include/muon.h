@@ -217,7 +217,13 @@ MUON_API muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_pa
  * parameter i, updated in place; grads[i]: same type, read only; momenta[i]:
  * fp32, updated in place to M'.  beta, lr, wd: momentum, learning rate,
  * decoupled weight decay.  ns_steps >= 0 (0 = no iteration: O = X0);
- * (a, b, c): quintic coefficients.  Never allocates.  The first call with a
+ * (a, b, c): quintic coefficients.  Each buffer holds its parameter
+ * contiguously, row-major with experts outermost ([E, rows, cols]); buffers
+ * must not overlap.  Any alignment of the element type is accepted: a member
+ * whose buffers start on 16 bytes, with rows <= cols and cols % 8 == 0,
+ * takes the vector paths, and other members take element-wise accesses (the
+ * kernels test this per member, so no access leaves the buffers).
+ * Never allocates.  The first call with a
  * given ns_steps captures and instantiates a CUDA graph (host work only);
  * later calls copy the scalars and pointers into the plan's device table
  * (one async H2D copy from pinned memory, skipped when they equal those of
