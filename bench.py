@@ -174,6 +174,16 @@ def oracle_time(w, members, host_inputs):
     return time.perf_counter() - t0, time.process_time() - c0
 
 
+def blas_name():
+    """NumPy's BLAS library and version, as its build config reports them."""
+    import numpy as np
+    try:
+        d = np.show_config(mode="dicts")["Build Dependencies"]["blas"]
+        return f"{d.get('name', '?')} {d.get('version', '')}".strip()
+    except Exception:  # older NumPy: no dict form of the build config
+        return "unknown"
+
+
 def busy_cores(wall, cpu):
     """Host threads the oracle used: its CPU time over its wall time, rounded
     up (at least 1)."""
@@ -274,7 +284,7 @@ def run_reference(args, w, world, rank):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "ns_steps": w.ns_steps},
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores,
-                             "host_cores": os.cpu_count(), "kind": "oracle",
+                             "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
                              "sample": f"{len(members)} of {round(len(members) / frac)} matrices "
                                        "per step, extrapolated linearly by matrix count"},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -485,7 +495,7 @@ def main():
         t = wall / frac
         cv, cu = headline(w, byts, flops, t)
         cpu = {"value": cv, "unit": cu, "cores": busy_cores(wall, cpu_s),
-               "host_cores": os.cpu_count(), "kind": "oracle",
+               "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
                "sample": f"{len(members)} matrices of the workload, extrapolated by matrix count",
                "ms_per_step": t * 1e3}
 

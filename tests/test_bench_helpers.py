@@ -65,3 +65,14 @@ def test_mixed_bag_group_workloads():
     assert sum(counts) == 1000 == len(full.shapes)
     with pytest.raises(KeyError):
         W.get("c5_group_3x3")
+
+
+def test_cpu_baseline_thread_count_and_blas():
+    """cores = CPU time over wall time, rounded up, at least 1; the BLAS name
+    is a string whatever NumPy reports."""
+    assert bench.busy_cores(2.0, 2.0) == 1
+    assert bench.busy_cores(1.0, 7.2) == 8
+    assert bench.busy_cores(1.0, 7.96) == 8
+    assert bench.busy_cores(1.0, 0.3) == 1
+    assert bench.busy_cores(0.0, 0.0) == 1
+    assert isinstance(bench.blas_name(), str) and bench.blas_name()
