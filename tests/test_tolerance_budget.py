@@ -15,7 +15,9 @@ Gaussian momenta:
 * bf16 operands on the tensor path land inside at k = 5 but outgrow the
   tolerance by k = 10, which is why fp16 is the default operand type;
 * a dropped A^2 term, a flipped sign of b, the Gram of the wrong side, one
-  Newton-Schulz step too few, and a missing normalisation each land outside.
+  Newton-Schulz step too few, and a missing normalisation each land outside;
+* momenta whose singular values spread over several decades use up most of
+  the margin, because the iteration stretches their small directions.
 """
 import numpy as np
 import pytest
@@ -140,3 +142,46 @@ def test_bf16_rounding_helper():
                  np.float32)
     np.testing.assert_array_equal(round_bf16(x),
                                   np.array([1.0, 1.0, 1.0 + 2 * ulp, 1.0, -1.0], np.float32))
+
+
+def _spread_momentum(m, n, decades, seed):
+    """A momentum whose singular values fall log-evenly over `decades`."""
+    rng = np.random.default_rng(seed)
+    U, _ = np.linalg.qr(rng.standard_normal((m, m)))
+    V, _ = np.linalg.qr(rng.standard_normal((n, m)))
+    X = (U * np.logspace(0, -decades, m)) @ V.T * 1e-2
+    return X.astype(np.float32).astype(np.float64)
+
+
+def _hi_lo_f16(x):
+    hi = round_f16(x)
+    return hi + round_f16(x - hi)
+
+
+def test_spread_spectra_use_up_the_headroom():
+    """Five steps stretch directions with small singular values by up to
+    a^5 (about 486), so the one rounding of X0 dominates the error.  With the
+    spectrum over four decades, fp16 operands come within a factor 2 of the
+    tolerance and bf16 operands exceed it several times over.  Rounding X0
+    as an fp16 pair (high part plus residual) for the final product
+    O = Pi X0 brings the Gram-space error back to about 1e-3."""
+    Mp = _spread_momentum(24, 10240, 4, seed=0)
+    want = _want(Mp, 5)
+    e16 = _rel(emulated_gram_space(Mp, 5, round_f16), want)
+    ebf = _rel(emulated_gram_space(Mp, 5, round_bf16), want)
+    assert TOL_BF16_MODE / 2 <= e16 <= TOL_BF16_MODE, e16
+    assert ebf > 4 * TOL_BF16_MODE, ebf
+    # the same iteration with only the last product's operand split
+    X = np.asarray(Mp, np.float32)
+    X = X / (np.sqrt(np.sum(X.astype(np.float64) ** 2)).astype(np.float32) + np.float32(1e-7))
+    Xr = round_f16(X)
+    I = np.eye(24, dtype=np.float32)
+    A, Pi = Xr @ Xr.T, I.copy()
+    for _ in range(5):
+        Q = np.float32(A_) * I + np.float32(B_) * A + np.float32(C_) * (A @ A)
+        Pi, A = Q @ Pi, (Q @ Q) @ A
+    e_split = _rel((Pi @ _hi_lo_f16(X)).astype(np.float64), want)
+    assert e_split <= TOL_BF16_MODE / 10, e_split
+    # concentrated spectra, like the seeded Gaussian workloads, keep a wide margin
+    Mp = _spread_momentum(24, 10240, 0.3, seed=0)
+    assert _rel(emulated_gram_space(Mp, 5, round_f16), _want(Mp, 5)) <= TOL_BF16_MODE / 20
