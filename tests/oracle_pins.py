@@ -246,3 +246,17 @@ def pin_sharded_equals_unsharded(ref, k=5, seed=8):
 
 
 ALL_PINS.append(pin_sharded_equals_unsharded)
+
+
+def pin_eps_placement(ref):
+    """eps is added to the norm, not to its square (the reading taken; the
+    pages give no eps): a matrix whose Frobenius norm equals eps normalises
+    to norm exactly 1/2, sharded or not, and with eps = 0 to norm 1."""
+    M = np.zeros((3, 5)); M[1, 2] = 1e-7
+    for X in (ref.frobenius_normalize(M, 1e-7), ref.sharded_frobenius_normalize(M, 1e-7, 2)):
+        assert abs(np.linalg.norm(X) - 0.5) <= 1e-15, "eps on the norm"
+    M = np.full((2, 4), 0.5)
+    assert abs(np.linalg.norm(ref.frobenius_normalize(M, 0.0)) - 1.0) <= 1e-15, "eps = 0"
+
+
+ALL_PINS.append(pin_eps_placement)

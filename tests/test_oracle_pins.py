@@ -55,6 +55,15 @@ MUTANTS = {
                               "        parts = [a_s * p + (b_s * (p @ p.T) + c_s * (p @ p.T) @ (p @ p.T)) @ p for p in parts]"),
     "nesterov_on_old_m": ("U = nesterov_input(Mp, G, beta) if nesterov else Mp",
                           "U = nesterov_input(M, G, beta) if nesterov else Mp"),
+    "eps_in_square": ("math.sqrt(float(np.sum(M * M))) + float(eps)",
+                      "math.sqrt(float(np.sum(M * M)) + float(eps))"),
+    "sharded_eps_in_square": ("return M / (math.sqrt(ss) + float(eps))",
+                              "return M / math.sqrt(ss + float(eps))"),
+    "sharded_norm_last_shard": ("        ss += float(np.sum(p * p))", "        ss = float(np.sum(p * p))"),
+    "transpose_wrong_way": ("transposed = X.shape[0] > X.shape[1]",
+                            "transposed = X.shape[0] < X.shape[1]"),
+    "decay_after_update": ("Pn = P * (1.0 - float(lr) * float(wd)) - float(lr) * s * O",
+                           "Pn = (P - float(lr) * s * O) * (1.0 - float(lr) * float(wd))"),
 }
 
 
