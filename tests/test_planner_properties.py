@@ -37,6 +37,23 @@ def test_planner_equals_oracle_bucketing(shapes, merge):
         assert g["path"] == ("skinny" if m <= 64 else "tensor")
         assert g["workspace_bytes"] > 0
     assert first == sum(s[0] if len(s) == 3 else 1 for s in shapes)
+    # one workspace holds every group's scratch plus the per-member pointer
+    # table (three pointers, the orientation and the scale: 32 bytes each)
+    assert d["workspace_bytes"] >= sum(g["workspace_bytes"] for g in d["groups"]) + \
+        32 * len(d["members"])
+
+
+def test_options_add_their_buffers():
+    """Nesterov on the skinny path keeps U = G + beta M' (fp32) for the
+    direct kernel, and keep_update keeps O (fp32): each adds one fp32 copy of
+    the group's data."""
+    shapes = [[24, 10240]] * 3 + [[2, 40, 1000]]
+    base = pkg.describe(shapes)["groups"]
+    for opt in ("nesterov", "keep_update"):
+        more = pkg.describe(shapes, **{opt: True})["groups"]
+        for g0, g1 in zip(base, more):
+            assert g1["workspace_bytes"] - g0["workspace_bytes"] >= \
+                4 * g0["batch"] * g0["rows"] * g0["cols"], (opt, g0)
 
 
 @hypothesis.settings(max_examples=60, deadline=None, derandomize=True)
