@@ -291,7 +291,7 @@ MUON_API muon_status_t muon_plan_check_error(muon_plan_t plan);
 /* The skinny-path step (min(rows, cols) <= 64) for callers that cannot
  * allocate device memory -- for example code inside a framework whose caching
  * allocator forbids outside cudaMalloc calls, latency-critical loops that must
- * not enter the driver's allocator, or embedded deployments that fix every
+ * not enter the CUDA allocator, or embedded deployments that fix every
  * device buffer at start-up.  The pages have no counterpart to this call; it
  * exists for those callers.  It applies the update at the top of this file to
  * the `batch` matrices of one [batch, rows, cols] parameter in BF16 mode with

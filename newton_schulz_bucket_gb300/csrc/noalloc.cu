@@ -3,7 +3,7 @@
 //
 // Some callers cannot call cudaMalloc at step time or at all: code running
 // inside a framework's pooled or capped allocator that forbids foreign
-// allocations, real-time loops that must not block on the driver's allocator,
+// allocations, real-time loops that must not block on the CUDA allocator,
 // and embedded hosts that fix all device memory up front.  For them this entry
 // point runs the same momentum and Newton-Schulz kernels as the SKINNY path
 // of muon_step, but keeps every byte of scratch (the scalar/pointer table, the

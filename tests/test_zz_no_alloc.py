@@ -1,6 +1,6 @@
 """GPU test of muon_step_skinny_static, the entry point for callers that
 cannot allocate device memory (a framework allocator that forbids outside
-cudaMalloc calls, a latency-critical loop that must stay out of the driver's
+cudaMalloc calls, a latency-critical loop that must stay out of the CUDA
 allocator, or a deployment that fixes all device buffers at start-up).
 
 It must give the same update as the plan-based muon_step on the same inputs:
