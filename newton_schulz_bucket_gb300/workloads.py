@@ -38,6 +38,7 @@ class Workload:
     m_zero: bool = False
     seed: int = 0
     describe: str = ""
+    spectrum_decades: float = 0.0  # > 0: M and G share singular values log-spaced over this many decades
 
     @property
     def n_params(self) -> int:
@@ -118,11 +119,26 @@ def get(name: str, ns_steps: Optional[int] = None) -> Workload:
 
 def custom(shapes: Sequence[Sequence[int]], mode: str = "bf16", seed: int = 0,
            g_std: float = 1e-3, p_std: float = 0.02, beta: float = 0.95, lr: float = 0.02,
-           wd: float = 0.1, ns_steps: int = 5, m_zero: bool = False) -> Workload:
+           wd: float = 0.1, ns_steps: int = 5, m_zero: bool = False,
+           spectrum_decades: float = 0.0) -> Workload:
     shapes = [list(map(int, s)) for s in shapes]
     return Workload("custom", shapes, mode, beta, lr, wd, ns_steps,
                     p_std=[p_std] * len(shapes), g_std=[g_std] * len(shapes),
-                    m_zero=m_zero, seed=seed, describe=f"custom {shapes}")
+                    m_zero=m_zero, seed=seed, describe=f"custom {shapes}",
+                    spectrum_decades=float(spectrum_decades))
+
+
+def spread_matrix(rows: int, cols: int, decades: float, std: float,
+                  g: torch.Generator) -> torch.Tensor:
+    """A seeded fp64 [rows, cols] matrix U diag(s) V^T with random orthonormal
+    U, V (QR of Gaussian draws) and s log-spaced from 1 down to 10^-decades,
+    scaled so that its entries have root-mean-square `std`."""
+    r = min(rows, cols)
+    U = torch.linalg.qr(torch.randn(rows, r, generator=g, dtype=torch.float64))[0]
+    V = torch.linalg.qr(torch.randn(cols, r, generator=g, dtype=torch.float64))[0]
+    s = torch.logspace(0, -float(decades), r, dtype=torch.float64)
+    X = (U * s) @ V.T
+    return X * (std * math.sqrt(rows * cols) / float(torch.linalg.norm(X)))
 
 
 def make_tensors(w: Workload, device="cpu"):
@@ -130,12 +146,29 @@ def make_tensors(w: Workload, device="cpu"):
 
     bf16 mode: P, G bf16 (fp32 draw, round-to-nearest-even cast), M fp32.
     fp32 mode: all fp32.  M0 follows the same law as G (so beta matters)
-    unless ``m_zero``.  Per-expert stds scale each expert slice.
+    unless ``m_zero``.  Per-expert stds scale each expert slice.  With
+    ``spectrum_decades`` > 0, G and M0 are one spread_matrix per member (the
+    same draw), so their singular values fall log-evenly over that many
+    decades, unlike the concentrated spectra of Gaussian draws.
     """
     dev = torch.device(device)
     g = torch.Generator(device=dev).manual_seed(w.seed)
     pdt = torch.bfloat16 if w.mode == "bf16" else torch.float32
     params, grads, moms = [], [], []
+    if w.spectrum_decades > 0:
+        # M0 and G share their singular vectors, so M' = beta M0 + G keeps
+        # the log-spaced spectrum (up to the rounding of G); drawn on the host
+        hg = torch.Generator().manual_seed(w.seed)
+        for i, shp in enumerate(w.shapes):
+            E = shp[0] if len(shp) == 3 else 1
+            X = torch.stack([spread_matrix(shp[-2], shp[-1], w.spectrum_decades,
+                                           float(w.g_std[i]), hg) for _ in range(E)])
+            X = X.reshape(shp).float()
+            P = (torch.randn(shp, generator=hg, dtype=torch.float32) * w.p_std[i]).to(pdt)
+            params.append(P.to(dev).contiguous())
+            grads.append(X.to(pdt).to(dev).contiguous())
+            moms.append((torch.zeros_like(X) if w.m_zero else X).to(dev).contiguous())
+        return params, grads, moms
     for i, shp in enumerate(w.shapes):
         gs = w.g_std[i]
         if isinstance(gs, (list, tuple)):

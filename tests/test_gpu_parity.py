@@ -92,6 +92,21 @@ def test_ns_steps_zero_and_ten():
         run.close()
 
 
+def test_spread_spectrum_inputs():
+    """Momenta whose singular values fall log-evenly over several decades,
+    unlike the concentrated spectra of Gaussian draws: two decades in bf16
+    mode (Gram-space wide and transposed members, m = 64 experts, tensor
+    path), four in fp32 mode."""
+    run = GpuRun(W.custom([[24, 4096], [4096, 24], [2, 64, 2048], [256, 1024], [200, 600]],
+                          seed=31, spectrum_decades=2))
+    check_all(run)
+    run.close()
+    run = GpuRun(W.custom([[64, 128], [24, 4096], [128, 512]], mode="fp32", seed=31,
+                          spectrum_decades=4))
+    check_all(run)
+    run.close()
+
+
 def test_zero_gradient_and_momentum():
     w = W.custom([[24, 2048]], seed=13, g_std=0.0, m_zero=True)
     run = GpuRun(w)

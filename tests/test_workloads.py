@@ -91,3 +91,26 @@ def test_per_expert_stds_scale_each_slice():
 def test_zero_momentum_option():
     _, _, M = W.make_tensors(W.custom([[8, 64]], m_zero=True))
     assert not M[0].any()
+
+
+def test_spread_spectrum_draws():
+    """spectrum_decades: M0 and G are one draw U diag(s) V^T per member, s
+    log-spaced over the stated decades, entries of the stated rms; G is that
+    draw rounded to bf16 and P follows its usual law."""
+    w = W.custom([[24, 512], [300, 40], [2, 16, 64]], seed=5, spectrum_decades=3)
+    P, G, M = W.make_tensors(w)
+    for i, shp in enumerate(w.shapes):
+        ms = M[i].reshape(-1, *shp[-2:])
+        gs = G[i].reshape(-1, *shp[-2:])
+        assert ms.dtype == torch.float32 and gs.dtype == torch.bfloat16
+        for m, g in zip(ms, gs):
+            s = torch.linalg.svdvals(m.double())
+            want = torch.logspace(0, -3, s.numel(), dtype=torch.float64)
+            assert torch.allclose(s / s[0], want, rtol=1e-3)
+            assert abs(float(m.double().pow(2).mean().sqrt()) / 1e-3 - 1) < 1e-5
+            assert torch.equal(g, m.to(torch.bfloat16))
+        assert abs(float(P[i].double().std()) / 0.02 - 1) < 0.2
+    again = W.make_tensors(w)
+    assert all(torch.equal(a, b) for a, b in zip(M + G + P, again[2] + again[1] + again[0]))
+    _, _, Mz = W.make_tensors(W.custom([[8, 64]], spectrum_decades=2, m_zero=True))
+    assert not Mz[0].any()
