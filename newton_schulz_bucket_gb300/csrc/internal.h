@@ -140,5 +140,9 @@ cudaError_t launch_tc_gram(const KArgs& a, const TcMaps& t, int src, cudaStream_
 cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, int step, cudaStream_t s);  // step: schedule row
 // Y[1 - src] = Q Y[src]
 cudaError_t launch_tc_update(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
+// The (tile row, tile column) of each tile the Gram and polynomial GEMMs
+// compute for one m x m output with bn-wide tiles, in launch order; returns
+// the tile count (entries past cap are not written), -1 on bad arguments.
+int32_t tc_sym_tile_walk(int64_t m, int32_t bn, int32_t* tm, int32_t* tn, int32_t cap);
 
 }  // namespace muon

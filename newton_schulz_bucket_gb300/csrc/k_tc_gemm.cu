@@ -155,21 +155,26 @@ __host__ __device__ inline int sym_tiles_per_batch(int tiles_m, int tiles_n) {
   }
   return u;
 }
-// Tile t of a symmetric output: batch-major, then tile rows, then the tile
-// columns from first_tn(tm).
+// Tile r of one batch's symmetric output: tile rows in order, each from its
+// first tile column that reaches the upper triangle.
+template <int BN>
+__host__ __device__ __forceinline__ void decode_sym(int r, int tiles_m, int tiles_n, int& tm,
+                                                    int& tn) {
+  tm = 0;
+  while (tm + 1 < tiles_m && r >= tiles_n - first_tn<BN>(tm)) {
+    r -= tiles_n - first_tn<BN>(tm);
+    ++tm;
+  }
+  tn = first_tn<BN>(tm) + r;
+}
+// Tile t of an output: for the symmetric ones batch-major, then decode_sym.
 template <int OP, int BN>
 __device__ __forceinline__ void decode(int t, const TcArgs& p, int& b, int& tm, int& tn) {
   if constexpr (OP == TC_UPDATE) {
     decode_tile(t, p, b, tm, tn);
   } else {
     b = t / p.tiles_sym;
-    int r = t - b * p.tiles_sym;
-    tm = 0;
-    while (tm + 1 < p.tiles_m && r >= p.tiles_n - first_tn<BN>(tm)) {
-      r -= p.tiles_n - first_tn<BN>(tm);
-      ++tm;
-    }
-    tn = first_tn<BN>(tm) + r;
+    decode_sym<BN>(t - b * p.tiles_sym, p.tiles_m, p.tiles_n, tm, tn);
   }
 }
 
@@ -461,6 +466,19 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int ns_type, int64_t inne
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+template <int BN>
+static int32_t sym_walk(int64_t m, int32_t* tm, int32_t* tn, int32_t cap) {
+  const int tiles_m = (int)((m + BM - 1) / BM), tiles_n = (int)((m + BN - 1) / BN);
+  const int n = sym_tiles_per_batch<BN>(tiles_m, tiles_n);
+  for (int t = 0; t < n && t < cap; ++t) {
+    int a = 0, b = 0;
+    decode_sym<BN>(t, tiles_m, tiles_n, a, b);
+    tm[t] = a;
+    tn[t] = b;
+  }
+  return n;
+}
+
 int num_sms() {
   static int n = 0;
   if (!n) {
@@ -513,6 +531,12 @@ int tc_bn_square(int64_t m) { return m >= 256 ? 256 : 128; }
 int tc_bn_update(int64_t n) { return n >= 256 ? 256 : 128; }
 
 }  // namespace
+
+int32_t tc_sym_tile_walk(int64_t m, int32_t bn, int32_t* tm, int32_t* tn, int32_t cap) {
+  if (m < 1 || m > (1ll << 20) || (bn != 128 && bn != 256) || cap < 0 || (cap && (!tm || !tn)))
+    return -1;
+  return bn == 256 ? sym_walk<256>(m, tm, tn, cap) : sym_walk<128>(m, tm, tn, cap);
+}
 
 cudaError_t tc_make_maps(const KArgs& a, TcMaps* t) {
   const int bs = tc_bn_square(a.m), bu = tc_bn_update(a.n);
