@@ -1,10 +1,11 @@
 /* Host-only checks of the C ABI from plain C99 (no device is touched): the
- * header compiles as C, the library links, and the planning calls and error
+ * headers compile as C, the library links, and the planning calls and error
  * statuses behave as include/muon.h states.  Exit status 0 = all passed. */
 #include <stdio.h>
 #include <string.h>
 
 #include "muon.h"
+#include "muon_testing.h"
 
 static int failures = 0;
 #define CHECK(cond, what)                                          \
@@ -96,6 +97,15 @@ int main(void) {
   CHECK(muon_step_schedule(NULL, NULL, NULL, NULL, 0.9f, 0.02f, 0.1f, 5, rows, 1, NULL) == MUON_ERR_INVALID_ARG,
         "NULL plan (schedule)");
   CHECK(muon_plan_num_groups(NULL) == 0, "groups of a NULL plan");
+
+  /* the symmetric GEMMs' tile walk (host only): m = 300 with 128 x 128
+   * tiles is the upper triangle of a 3 x 3 tile grid, row by row */
+  int32_t tm[8], tn[8];
+  CHECK(muon_testing_sym_tiles(300, 128, tm, tn, 8) == 6, "sym tile count");
+  CHECK(tm[0] == 0 && tn[0] == 0 && tm[2] == 0 && tn[2] == 2 && tm[3] == 1 && tn[3] == 1 &&
+            tm[5] == 2 && tn[5] == 2,
+        "sym tile order");
+  CHECK(muon_testing_sym_tiles(300, 96, NULL, NULL, 0) == -1, "sym tiles: bad width");
 
   if (failures) {
     fprintf(stderr, "%d check(s) failed\n", failures);
