@@ -185,3 +185,11 @@ def test_spread_spectra_use_up_the_headroom():
     # concentrated spectra, like the seeded Gaussian workloads, keep a wide margin
     Mp = _spread_momentum(24, 10240, 0.3, seed=0)
     assert _rel(emulated_gram_space(Mp, 5, round_f16), _want(Mp, 5)) <= TOL_BF16_MODE / 20
+
+
+def test_fp32_mode_keeps_its_margin_on_spread_spectra():
+    """fp32 mode (every product an fp32 FMA) against its 1e-4 tolerance, on a
+    spectrum over four decades: about 5e-6."""
+    Mp = _spread_momentum(64, 512, 4, seed=2)
+    err = _rel(emulated_ns(Mp, 5, lambda x: np.asarray(x, np.float32)), _want(Mp, 5))
+    assert err <= TOL_O["fp32"] / 10, err
