@@ -159,19 +159,29 @@ def allmax(world, v):
     return v
 
 
-def oracle_time(w, members, host_inputs):
-    """(wall seconds, process CPU seconds) the CPU oracle needs for `members`
-    (list of (param, expert)); CPU over wall is the number of host threads
-    it kept busy on average (NumPy's BLAS may use several)."""
+def oracle_time(w, sample, host_inputs):
+    """Times the CPU oracle on a per-group sample [(members, group size), ...]
+    (members: list of (param, expert)).  Returns (seconds for the whole
+    workload, each group's time scaled by its size over its sample; wall
+    seconds timed; process CPU seconds timed).  CPU over wall is the number
+    of host threads the oracle kept busy (NumPy's BLAS may use several).
+    Each group's inputs are drawn before its timed region."""
     import numpy as np
     from oracle import muon_ref
     f32 = lambda v: float(np.float32(v))
     a, b, c = (f32(v) for v in w.coeffs)
-    inputs = [host_inputs(i, e) for (i, e) in members]
-    t0, c0 = time.perf_counter(), time.process_time()
-    for P, G, M in inputs:
-        muon_ref.muon_update_ref(P, G, M, f32(w.beta), f32(w.lr), f32(w.wd), w.ns_steps, a, b, c)
-    return time.perf_counter() - t0, time.process_time() - c0
+    total = wall = cpu = 0.0
+    for members, size in sample:
+        inputs = [host_inputs(i, e) for (i, e) in members]
+        t0, c0 = time.perf_counter(), time.process_time()
+        for P, G, M in inputs:
+            muon_ref.muon_update_ref(P, G, M, f32(w.beta), f32(w.lr), f32(w.wd), w.ns_steps,
+                                     a, b, c)
+        dt, dc = time.perf_counter() - t0, time.process_time() - c0
+        wall += dt
+        cpu += dc
+        total += dt * size / len(members)
+    return total, wall, cpu
 
 
 def blas_name():
@@ -191,41 +201,47 @@ def busy_cores(wall, cpu):
 
 
 def sample_members(w, budget_s=12.0):
-    """Seeded sample of members sized so the oracle runs for about budget_s."""
+    """Seeded per-group sample for timing the oracle: every shape group gets
+    at least one member, and as many more as its share of budget_s allows at
+    the estimated cost of one member.  Returns [(members, group size), ...].
+    A group whose single member costs more than its share still gets one, so
+    workloads of large matrices run past the budget."""
     import random
-    mem = [(i, e) for i, s in enumerate(w.shapes) for e in range(s[0] if len(s) == 3 else 1)]
+    groups = {}
+    for i, s in enumerate(w.shapes):
+        for e in range(s[0] if len(s) == 3 else 1):
+            groups.setdefault((s[-2], s[-1]), []).append((i, e))
     rng = random.Random(1234)
-    order = mem[:]
-    rng.shuffle(order)
-    tot = 0.0
+    share = budget_s / len(groups)
     out = []
-    for (i, e) in order:
-        r, c = w.shapes[i][-2:]
+    for (r, c), mem in groups.items():
         m, n = min(r, c), max(r, c)
         cost = w.ns_steps * (4 * m * m * n + 2 * m ** 3) / 2.5e10 + r * c * 1e-8
-        if out and tot + cost > budget_s:
-            break
-        out.append((i, e))
-        tot += cost
+        order = mem[:]
+        rng.shuffle(order)
+        out.append((order[:max(1, min(len(order), int(share / cost)))], len(mem)))
     return out
 
 
+def sample_note(sample):
+    n = sum(len(m) for m, _ in sample)
+    return (f"{n} of {sum(s for _, s in sample)} matrices per step, at least one of each of the "
+            f"{len(sample)} shape groups; each group extrapolated by its member count")
+
+
 def host_member_inputs(w):
-    """Host fp64 inputs of single members drawn from the same laws (for timing
-    the oracle; the values need not match the GPU draw)."""
+    """Host fp64 inputs of single members, each drawn alone from its own
+    parameter's (or expert's) law, for timing the oracle: the values need not
+    match the GPU draw, and an expert tensor is never drawn whole."""
     from newton_schulz_bucket_gb300 import workloads as W
-    cache = {}
 
     def get(i, e):
-        if i not in cache:
-            sub = W.custom([w.shapes[i]], mode=w.mode, seed=w.seed + i)
-            P, G, M = W.make_tensors(sub, "cpu")
-            cache.clear()
-            cache[i] = [t.float().double().numpy() for t in (P[0], G[0], M[0])]
-        P, G, M = cache[i]
-        if P.ndim == 3:
-            return P[e], G[e], M[e]
-        return P, G, M
+        gs = w.g_std[i]
+        std = float(gs[e]) if isinstance(gs, (list, tuple)) else float(gs)
+        sub = W.custom([w.shapes[i][-2:]], mode=w.mode, seed=w.seed * 100003 + i * 1009 + e,
+                       g_std=std, p_std=float(w.p_std[i]))
+        P, G, M = W.make_tensors(sub, "cpu")
+        return tuple(t[0].float().double().numpy() for t in (P, G, M))
     return get
 
 
@@ -269,15 +285,14 @@ def run_reference(args, w, world, rank):
     if rank != 0:
         return
     byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
-    members = sample_members(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
-    frac = len(members) / sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
+    sample = sample_members(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
     get = host_member_inputs(w)
     for _ in range(args.warmup):
-        oracle_time(w, members[:1], get)
-    runs = [oracle_time(w, members, get) for _ in range(args.steps)]
-    per_step = statistics.mean(t for t, _ in runs) / frac  # extrapolated to the whole workload
+        oracle_time(w, [(sample[0][0][:1], 1)], get)
+    runs = [oracle_time(w, sample, get) for _ in range(args.steps)]
+    per_step = statistics.mean(r[0] for r in runs)  # extrapolated to the whole workload
     value, unit = headline(w, byts, flops, per_step)
-    cores = busy_cores(sum(t for t, _ in runs), sum(c for _, c in runs))
+    cores = busy_cores(sum(r[1] for r in runs), sum(r[2] for r in runs))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -285,8 +300,7 @@ def run_reference(args, w, world, rank):
             "config": {"workload": w.name, "ns_steps": w.ns_steps},
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores,
                              "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
-                             "sample": f"{len(members)} of {round(len(members) / frac)} matrices "
-                                       "per step, extrapolated linearly by matrix count"},
+                             "sample": sample_note(sample)},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -488,16 +502,12 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        members = sample_members(w, budget_s=12.0)
-        frac = len(members) / sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
-        get = host_member_inputs(w)
-        wall, cpu_s = oracle_time(w, members, get)
-        t = wall / frac
+        sample = sample_members(w, budget_s=12.0)
+        t, wall, cpu_s = oracle_time(w, sample, host_member_inputs(w))
         cv, cu = headline(w, byts, flops, t)
         cpu = {"value": cv, "unit": cu, "cores": busy_cores(wall, cpu_s),
                "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
-               "sample": f"{len(members)} matrices of the workload, extrapolated by matrix count",
-               "ms_per_step": t * 1e3}
+               "sample": sample_note(sample), "ms_per_step": t * 1e3}
 
     launches = plan.kernels_per_step(w.ns_steps) * args.steps
     if rank == 0:

@@ -76,3 +76,37 @@ def test_cpu_baseline_thread_count_and_blas():
     assert bench.busy_cores(1.0, 0.3) == 1
     assert bench.busy_cores(0.0, 0.0) == 1
     assert isinstance(bench.blas_name(), str) and bench.blas_name()
+
+
+def test_host_member_inputs_draw_single_members():
+    """The oracle's timing inputs: one [rows, cols] member at a time, with
+    the member's own law (per-expert stds of a 3-D parameter included)."""
+    w = W.custom([[3, 40, 96], [24, 64]], seed=4)
+    w.g_std = [[1e-4, 1e-3, 1e-2], 1e-3]
+    get = bench.host_member_inputs(w)
+    for (i, e), std in [((0, 0), 1e-4), ((0, 2), 1e-2), ((1, 0), 1e-3)]:
+        P, G, M = get(i, e)
+        assert P.shape == G.shape == M.shape == tuple(w.shapes[i][-2:])
+        assert P.dtype == G.dtype == M.dtype
+        assert abs(float(G.std()) / std - 1) < 0.1 and abs(float(M.std()) / std - 1) < 0.1
+        assert abs(float(P.std()) / 0.02 - 1) < 0.1
+    a, b = get(0, 1), get(0, 1)
+    assert all((x == y).all() for x, y in zip(a, b))
+
+
+def test_oracle_sample_covers_every_shape_group():
+    """The CPU baseline's sample holds at least one member of every shape
+    group, no member twice, and the group sizes add up to the workload."""
+    for name in ["c2_skinny_74x24x10240", "c3_moe_64x2048x7168_32x24x10240", "c5_mixed_1000"]:
+        w = W.get(name)
+        sample = bench.sample_members(w, budget_s=12.0)
+        keys = {tuple(s[-2:]) for s in w.shapes}
+        assert len(sample) == len(keys)
+        assert sum(size for _, size in sample) == sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
+        seen = set()
+        for members, size in sample:
+            assert 1 <= len(members) <= size
+            assert len({tuple(w.shapes[i][-2:]) for i, _ in members}) == 1
+            assert not (seen & set(members))
+            seen |= set(members)
+    assert len(bench.sample_members(W.get("c2_skinny_74x24x10240"), 12.0)[0][0]) == 74
