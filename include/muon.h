@@ -189,9 +189,9 @@ MUON_API muon_status_t muon_plan_describe(const muon_shape_t* shapes, int32_t n_
  * balance; «关于分布式Muon的想法整合及讨论» §3: whole matrices per owner,
  * balanced by compute cost, not size).  A member's cost is its estimated
  * seconds on this library's path for its group (memory traffic over HBM
- * bandwidth, Newton-Schulz FLOPs over the tensor rate; nominal rates).  The
- * result is deterministic: a function of the shapes, options, ns_steps and
- * n_ranks only.  owner: member_cap >= member count entries, receives ranks in
+ * bandwidth, Newton-Schulz FLOPs over the tensor rate; rates measured on a
+ * GB300).  The result is deterministic: a function of the shapes, options,
+ * ns_steps and n_ranks only.  owner: member_cap >= member count entries, receives ranks in
  * [0, n_ranks); member_cost (nullable, member_cap entries) and rank_cost
  * (nullable, n_ranks entries) receive seconds.  No communication and no
  * device.  Errors: INVALID_ARG (as muon_plan_describe; n_ranks not in

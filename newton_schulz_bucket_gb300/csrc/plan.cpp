@@ -514,7 +514,9 @@ namespace {
 // Estimated seconds of one member's step on this library's path for its
 // group: the larger of its compulsory memory traffic over the HBM rate and
 // its Newton-Schulz work over the tensor (or fp32 FMA) rate.  Only ratios
-// matter to the planner, so nominal rates are used.
+// matter to the planner.  The HBM and tensor rates are a GB300's measured
+// copy bandwidth and sustained bf16 GEMM rate; the fp32 rate is a nominal
+// FFMA figure.
 double member_seconds(const GroupPlan& g, int32_t ns_steps, bool f32) {
   constexpr double kHbm = 6.8e12, kTensor = 1.7e15, kFp32 = 6.0e13;
   const double m = (double)g.m, n = (double)g.n;
