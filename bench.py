@@ -424,7 +424,8 @@ def main():
             evs[j][1].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
-        ms_total = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+        step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+        ms_total = sum(step_ms)
         # per-group kernel times from events recorded inside the step graph
         for j in range(min(args.steps, 6) + 1):
             flush(j)
@@ -513,6 +514,8 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "step_ms_this_rank": {"median": statistics.median(step_ms), "min": min(step_ms),
+                                      "max": max(step_ms)},
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.mode == "bf16" else "f32",
                 "data": "synthetic: seeded Gaussian G, M0 (std 1e-3), P (std 0.02)",
