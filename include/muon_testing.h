@@ -27,15 +27,18 @@ MUON_API muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int32_
                                             const void* q, void* out, float alpha, float pa,
                                             float pb, float pc, void* stream);
 
-/* The tiles the Gram and polynomial GEMMs compute for one m x m output (both
- * are symmetric, so only 128-row x bn-column tiles that reach the upper
- * triangle run; each writes its elements with col >= row in place and
- * mirrors those with col > row).  For t = 0 .. count-1, in launch order,
- * tm[t] and tn[t] receive tile t's row and column; entries past cap are not
- * written.  Returns count, or -1 for m outside [1, 2^20], bn other than 128
- * or 256, cap < 0, or a NULL array with cap > 0.  Host only: no device. */
-MUON_API int32_t muon_testing_sym_tiles(int64_t m, int32_t bn, int32_t* tm, int32_t* tn,
-                                        int32_t cap);
+/* The 128-row x bn-column tiles one batch item of a tcgen05 product (op as
+ * in muon_testing_tc_gemm) computes, in launch order.  op 0 / 1: the Gram and
+ * polynomial outputs are symmetric m x m (n is ignored), so only tiles that
+ * reach the upper triangle run; each writes its elements with col >= row in
+ * place and mirrors those with col > row.  op 2: every tile of the m x n
+ * update, in groups of 8 tile rows that sweep the tile columns together.
+ * For t = 0 .. count-1, tm[t] and tn[t] receive tile t's row and column;
+ * entries past cap are not written.  Returns count, or -1 for another op,
+ * m (or, for op 2, n) outside [1, 2^20], bn other than 128 or 256, cap < 0,
+ * or a NULL array with cap > 0.  Host only: no device. */
+MUON_API int32_t muon_testing_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn,
+                                        int32_t* tm, int32_t* tn, int32_t cap);
 
 /* Number of skinny-path clusters (one per member of min dim m, 1..64) that the
  * current device can hold at once for the given operand type; -1 on error. */

@@ -140,9 +140,12 @@ cudaError_t launch_tc_gram(const KArgs& a, const TcMaps& t, int src, cudaStream_
 cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, int step, cudaStream_t s);  // step: schedule row
 // Y[1 - src] = Q Y[src]
 cudaError_t launch_tc_update(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
-// The (tile row, tile column) of each tile the Gram and polynomial GEMMs
-// compute for one m x m output with bn-wide tiles, in launch order; returns
-// the tile count (entries past cap are not written), -1 on bad arguments.
-int32_t tc_sym_tile_walk(int64_t m, int32_t bn, int32_t* tm, int32_t* tn, int32_t cap);
+// The (tile row, tile column) of each tile one batch item of a GEMM computes
+// with 128 x bn tiles, in launch order: op 0 / 1 (Gram, polynomial) the
+// symmetric walk over the m x m output, op 2 (update) the grouped raster over
+// the m x n output.  Returns the tile count (entries past cap are not
+// written), -1 on bad arguments.
+int32_t tc_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn, int32_t* tm, int32_t* tn,
+                     int32_t cap);
 
 }  // namespace muon

@@ -128,19 +128,23 @@ struct TcSmem {
   static constexpr uint32_t kTotal = kEpi + kEpiBytes + 1024;  // + alignment slack
 };
 
-__device__ __forceinline__ void decode_tile(int t, const TcArgs& p, int& b, int& tm, int& tn) {
-  // grouped order: 8 tile-rows share a sweep over the tile-columns, so the
-  // tiles in flight reuse a compact set of operand panels through L2
+// Tile r of one batch's full output in grouped order: 8 tile-rows share a
+// sweep over the tile-columns, so the tiles in flight reuse a compact set of
+// operand panels through L2.
+__host__ __device__ __forceinline__ void decode_raster(int r, int tiles_m, int tiles_n, int& tm,
+                                                       int& tn) {
   constexpr int GM = 8;
-  const int per_b = p.tiles_m * p.tiles_n;
-  b = t / per_b;
-  int r = t - b * per_b;
-  const int group = r / (GM * p.tiles_n);
+  const int group = r / (GM * tiles_n);
   const int first = group * GM;
-  const int gsz = min(p.tiles_m - first, GM);
-  r -= group * GM * p.tiles_n;
+  const int gsz = tiles_m - first < GM ? tiles_m - first : GM;
+  r -= group * GM * tiles_n;
   tm = first + r % gsz;
   tn = r / gsz;
+}
+__device__ __forceinline__ void decode_tile(int t, const TcArgs& p, int& b, int& tm, int& tn) {
+  const int per_b = p.tiles_m * p.tiles_n;
+  b = t / per_b;
+  decode_raster(t - b * per_b, p.tiles_m, p.tiles_n, tm, tn);
 }
 
 // First tile column of tile row tm that reaches the upper triangle.
@@ -467,16 +471,18 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int ns_type, int64_t inne
 }
 
 template <int BN>
-static int32_t sym_walk(int64_t m, int32_t* tm, int32_t* tn, int32_t cap) {
-  const int tiles_m = (int)((m + BM - 1) / BM), tiles_n = (int)((m + BN - 1) / BN);
-  const int n = sym_tiles_per_batch<BN>(tiles_m, tiles_n);
-  for (int t = 0; t < n && t < cap; ++t) {
+static int32_t tile_walk(bool sym, int64_t m, int64_t n, int32_t* tm, int32_t* tn, int32_t cap) {
+  const int tiles_m = (int)((m + BM - 1) / BM);
+  const int tiles_n = (int)(((sym ? m : n) + BN - 1) / BN);
+  const int count = sym ? sym_tiles_per_batch<BN>(tiles_m, tiles_n) : tiles_m * tiles_n;
+  for (int t = 0; t < count && t < cap; ++t) {
     int a = 0, b = 0;
-    decode_sym<BN>(t, tiles_m, tiles_n, a, b);
+    if (sym) decode_sym<BN>(t, tiles_m, tiles_n, a, b);
+    else decode_raster(t, tiles_m, tiles_n, a, b);
     tm[t] = a;
     tn[t] = b;
   }
-  return n;
+  return count;
 }
 
 int num_sms() {
@@ -532,10 +538,13 @@ int tc_bn_update(int64_t n) { return n >= 256 ? 256 : 128; }
 
 }  // namespace
 
-int32_t tc_sym_tile_walk(int64_t m, int32_t bn, int32_t* tm, int32_t* tn, int32_t cap) {
-  if (m < 1 || m > (1ll << 20) || (bn != 128 && bn != 256) || cap < 0 || (cap && (!tm || !tn)))
+int32_t tc_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn, int32_t* tm, int32_t* tn,
+                     int32_t cap) {
+  const bool sym = op == TC_GRAM || op == TC_POLY;
+  if ((!sym && op != TC_UPDATE) || m < 1 || m > (1ll << 20) || (!sym && (n < 1 || n > (1ll << 20))) ||
+      (bn != 128 && bn != 256) || cap < 0 || (cap && (!tm || !tn)))
     return -1;
-  return bn == 256 ? sym_walk<256>(m, tm, tn, cap) : sym_walk<128>(m, tm, tn, cap);
+  return bn == 256 ? tile_walk<256>(sym, m, n, tm, tn, cap) : tile_walk<128>(sym, m, n, tm, tn, cap);
 }
 
 cudaError_t tc_make_maps(const KArgs& a, TcMaps* t) {

@@ -1,5 +1,5 @@
 // Test hooks (include/muon_testing.h): one tcgen05 product on caller buffers,
-// the symmetric GEMMs' tile walk, the skinny kernel's cluster occupancy, and a
+// the GEMMs' tile walks, the skinny kernel's cluster occupancy, and a
 // bounded wait that times out.
 #include <cstring>
 
@@ -57,9 +57,9 @@ extern "C" muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int3
   return st;
 }
 
-extern "C" int32_t muon_testing_sym_tiles(int64_t m, int32_t bn, int32_t* tm, int32_t* tn,
-                                          int32_t cap) {
-  return tc_sym_tile_walk(m, bn, tm, tn, cap);
+extern "C" int32_t muon_testing_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn,
+                                          int32_t* tm, int32_t* tn, int32_t cap) {
+  return tc_tile_walk(op, m, n, bn, tm, tn, cap);
 }
 
 extern "C" int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m) {

@@ -98,14 +98,19 @@ int main(void) {
         "NULL plan (schedule)");
   CHECK(muon_plan_num_groups(NULL) == 0, "groups of a NULL plan");
 
-  /* the symmetric GEMMs' tile walk (host only): m = 300 with 128 x 128
-   * tiles is the upper triangle of a 3 x 3 tile grid, row by row */
-  int32_t tm[8], tn[8];
-  CHECK(muon_testing_sym_tiles(300, 128, tm, tn, 8) == 6, "sym tile count");
+  /* the GEMMs' tile walks (host only): m = 300 with 128 x 128 tiles is the
+   * upper triangle of a 3 x 3 tile grid, row by row, for the Gram; the
+   * update of a 300 x 400 output sweeps 3 tile rows together */
+  int32_t tm[16], tn[16];
+  CHECK(muon_testing_tile_walk(0, 300, 0, 128, tm, tn, 16) == 6, "sym tile count");
   CHECK(tm[0] == 0 && tn[0] == 0 && tm[2] == 0 && tn[2] == 2 && tm[3] == 1 && tn[3] == 1 &&
             tm[5] == 2 && tn[5] == 2,
         "sym tile order");
-  CHECK(muon_testing_sym_tiles(300, 96, NULL, NULL, 0) == -1, "sym tiles: bad width");
+  CHECK(muon_testing_tile_walk(2, 300, 400, 128, tm, tn, 16) == 12, "update tile count");
+  CHECK(tm[0] == 0 && tn[0] == 0 && tm[1] == 1 && tn[1] == 0 && tm[3] == 0 && tn[3] == 1,
+        "update tile order");
+  CHECK(muon_testing_tile_walk(0, 300, 0, 96, NULL, NULL, 0) == -1, "tile walk: bad width");
+  CHECK(muon_testing_tile_walk(3, 300, 300, 128, NULL, NULL, 0) == -1, "tile walk: bad op");
 
   if (failures) {
     fprintf(stderr, "%d check(s) failed\n", failures);
