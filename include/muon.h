@@ -76,8 +76,11 @@ typedef enum { MUON_MODE_BF16 = 0, MUON_MODE_FP32 = 1 } muon_mode_t;
  * rounds X, A and the polynomial matrix to bf16, an error that grows with k.
  * With the roundings emulated against the fp64 oracle on Gaussian momenta,
  * the relative Frobenius error of O is about 2e-3 for FP16 up to k = 10 and
- * for BF16 on the skinny path (the data is rounded once); BF16 on the tensor
- * path is about 1.2e-2 at k = 5 and 2.5e-2 to 3e-2 at k = 10. */
+ * for BF16 on the skinny path up to k = 64 (the data is rounded once); BF16
+ * where the iterate is rounded on every step (tensor and SIMT paths, skinny
+ * path beyond 64 steps) is about 1.2e-2 at k = 5, 1.7e-2 at k = 6 and 2.5e-2
+ * to 3e-2 at k = 10.  So a step with BF16 operands and more than 5
+ * Newton-Schulz steps on such a group fails with MUON_ERR_UNSUPPORTED. */
 typedef enum { MUON_NS_FP16 = 0, MUON_NS_BF16 = 1 } muon_ns_dtype_t;
 
 /* Shape-dependent scale s(rows, cols) of the update (a reading; the pages
@@ -88,10 +91,14 @@ typedef enum {
   MUON_SCALE_NONE = 2
 } muon_scale_t;
 
-/* Kernel path of a shape group.  AUTO picks SKINNY for small min(rows, cols)
- * (mma.sync fragments streamed through an L2-resident workspace, one
- * two-CTA cluster per matrix), TENSOR (tcgen05 GEMMs) otherwise; FP32 mode
- * always uses SIMT. */
+/* Kernel path of a shape group.  AUTO picks SKINNY when min(rows, cols) <= 64
+ * (the skinny_threshold option): up to 64 Newton-Schulz steps that is one
+ * kernel per group, a cluster of column_shards CTAs per matrix that streams
+ * the data twice (momentum with the Gram matrix and the norm, then the
+ * output) and iterates in m x m Gram space on chip; beyond 64 steps, a
+ * momentum kernel and the direct iteration on a fragment-ordered, L2-resident
+ * workspace.  TENSOR otherwise (tcgen05 GEMMs on TMEM accumulators, fed by
+ * TMA).  FP32 mode always uses SIMT (fp32 FMA). */
 typedef enum {
   MUON_PATH_AUTO = 0,
   MUON_PATH_SKINNY = 1,
@@ -230,7 +237,9 @@ MUON_API muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_pa
  * the previous call) and replay the graph on `stream`.  Successive calls on
  * different streams must be ordered by the caller (the table is shared).
  * Errors (nothing is launched): INVALID_ARG for a null plan/array/pointer,
- * ns_steps < 0 or > 1000, or non-finite scalars; CUDA on a launch failure. */
+ * ns_steps < 0 or > 1000, or non-finite scalars; UNSUPPORTED for ns_steps > 5
+ * on a group that iterates on BF16 operands (see muon_ns_dtype_t); CUDA on a
+ * launch failure. */
 MUON_API muon_status_t muon_step(muon_plan_t plan, void* const* params,
                                  const void* const* grads, float* const* momenta,
                                  float beta, float lr, float wd, int32_t ns_steps,
@@ -300,19 +309,27 @@ MUON_API muon_status_t muon_plan_check_error(muon_plan_t plan);
  * device buffer at start-up.  The pages have no counterpart to this call; it
  * exists for those callers.  It applies the update at the top of this file to
  * the `batch` matrices of one [batch, rows, cols] parameter in BF16 mode with
- * fp16 Newton-Schulz operands, and gives the same results as muon_step on a
- * plan made of that one parameter (same kernels, same reduction orders).
- * params (bf16), grads (bf16) and momenta (fp32) are the caller's device
- * buffers, updated in place as in muon_step.  All scratch lives in one static
- * device array of 8 MiB inside the library: every GPU that loads the library
- * keeps it until the process exits, it is shared by every call (calls whose
- * work overlaps on a GPU race -- issue them on one stream), and a request
- * needing more (about 8 members of [24, 10240]) fails with
- * MUON_ERR_INVALID_ARG and a message giving both sizes.  It calls no
- * allocator.  The first call on each device looks up the array's device
- * address and sets kernel attributes (host work): make that first call before
- * any stream capture.  Errors: INVALID_ARG (NULL pointer, bad size, scalar or
- * scale_mode, too much scratch), UNSUPPORTED (min(rows, cols) > 64), CUDA. */
+ * fp16 Newton-Schulz operands, and gives bit for bit the results of muon_step
+ * on a plan made of that one parameter with default options (same kernels,
+ * same arguments, same reduction orders).  params (bf16), grads (bf16) and
+ * momenta (fp32) are the caller's device buffers, updated in place as in
+ * muon_step.  All scratch lives in one static device array of 8 MiB inside
+ * the library: every GPU that loads the library keeps it until the process
+ * exits, and it is shared by every call (calls whose work overlaps on a GPU
+ * race -- issue them on one stream).  Up to 64 Newton-Schulz steps a call
+ * needs 256 + 32 * batch bytes of it (step scalars and member pointers; e.g.
+ * any batch, up to 65535, of [24, 10240]); beyond 64 steps the direct
+ * iteration also keeps its iterate there (about 2 * rows * cols bytes per
+ * member, so about 8 members of [24, 10240]).  A request needing more fails
+ * with MUON_ERR_INVALID_ARG and a message giving both sizes.  It calls no
+ * allocator.  The current device must be the device of `stream` (checked:
+ * INVALID_ARG otherwise).  The first call on each device looks up the array's
+ * device address, and the first call for each kernel variant (number of
+ * 16-row tiles of min(rows, cols)) sets that kernel's attributes; both are
+ * host work: make those calls before any stream capture.  Errors:
+ * INVALID_ARG (NULL pointer, batch not in [1, 65535], bad size, scalar or
+ * scale_mode, too much scratch, stream of another device), UNSUPPORTED (min(rows, cols) > 64),
+ * CUDA. */
 MUON_API muon_status_t muon_step_skinny_static(void* params, const void* grads, float* momenta,
                                                int32_t batch, int64_t rows, int64_t cols,
                                                float beta, float lr, float wd, int32_t ns_steps,

@@ -89,6 +89,14 @@ struct SkinnyCfg {
 // X_0 its m x m product Pi_k grows like a^k (3.4445^64 < 2^115 stays in fp32).
 constexpr int32_t kGramSpaceMaxSteps = 64;
 
+// Newton-Schulz steps allowed on bf16 operands where the iterate itself is
+// rounded on every step (tensor and SIMT paths, and the skinny direct
+// iteration): with those roundings emulated against the fp64 oracle on
+// Gaussian momenta, the relative error of O is 1.1e-2 to 1.2e-2 at 5 steps,
+// 1.5e-2 to 1.7e-2 at 6 and 2.1e-2 to 2.4e-2 at 8, against the bf16-mode
+// tolerance of 2e-2.
+constexpr int32_t kBf16OperandMaxSteps = 5;
+
 // Sets the thread-local message muon_last_error() returns.
 void set_last_error(const char* msg);
 

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) k_write(KArgs a, const TY* __restric
   TP* P = static_cast<TP*>(a.mem[b].P);
   const TY* Yb = Y + (int64_t)b * a.m * a.n_pitch;
   const float lr = a.sc->lr, wd = a.sc->wd;
-  const float decay = 1.f - lr * wd;
+  const float decay = __fmaf_rn(-lr, wd, 1.f);  // one rounding of 1 - lr wd
   const MemberPtrs mp = a.mem[b];
   const float coef = lr * mp.scale / a.alpha;  // alpha is a power of two
   const float inv_alpha = 1.f / a.alpha;

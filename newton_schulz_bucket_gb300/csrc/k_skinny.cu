@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_ns(KArgs a, SkArgs s) {
   const int ns = a.sc->ns_steps;
   const float inv_a2 = 1.f / (a.alpha * a.alpha);
   const float lr = a.sc->lr, wdk = a.sc->wd;
-  c.decay = 1.f - lr * wdk;
+  c.decay = __fmaf_rn(-lr, wdk, 1.f);  // one rounding of 1 - lr wd
   c.inv_alpha = 1.f / a.alpha;
   c.coef = lr * mp.scale * c.inv_alpha;
   uint8_t* stage_warp = smem + L::kStage + warp * 32 * L::LB;

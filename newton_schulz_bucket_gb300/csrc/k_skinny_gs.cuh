@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   const int ns = a.sc->ns_steps;
   c.beta = a.sc->beta;
   const float lr = a.sc->lr;
-  c.decay = 1.f - lr * a.sc->wd;
+  c.decay = __fmaf_rn(-lr, a.sc->wd, 1.f);  // one rounding of 1 - lr wd
   c.inv_alpha = 1.f / a.alpha;
   c.coef = lr * mp.scale * c.inv_alpha;
 

@@ -5,14 +5,17 @@
 // inside a framework's pooled or capped allocator that forbids foreign
 // allocations, real-time loops that must not block on the CUDA allocator,
 // and embedded hosts that fix all device memory up front.  For them this entry
-// point runs the same momentum and Newton-Schulz kernels as the SKINNY path
-// of muon_step, but keeps every byte of scratch (the scalar/pointer table, the
-// momentum kernel's partial sums and the fragment-ordered iterate) in one
-// file-scope device array of kStaticScratchBytes.  The array is part of the
-// library image: every GPU that loads the library holds it until the process
-// exits.  Every call uses the same array, so two calls whose kernels overlap
-// on a GPU race (serialise them on one stream).  No byte of the array needs to
-// start at zero: each call writes every location it later reads.
+// point runs the same kernels as the SKINNY path of muon_step, with the same
+// arguments, and keeps every byte of scratch in one file-scope device array of
+// kStaticScratchBytes.  Up to kGramSpaceMaxSteps Newton-Schulz steps that
+// scratch is only the step scalars and the member pointer table (the
+// Gram-space kernel keeps everything else on chip); beyond, the direct
+// iteration also needs the momentum kernel's partial sums and the
+// fragment-ordered iterate.  The array is part of the library image: every
+// GPU that loads the library holds it until the process exits.  Every call
+// uses the same array, so two calls whose kernels overlap on a GPU race
+// (serialise them on one stream).  No byte of the array needs to start at
+// zero: each call writes every location it later reads.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
@@ -33,8 +36,11 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // Device address of g_static_scratch per device, looked up once with that
-// device current (the array's host-side name is not a device address).
+// device current (the array's host-side name is not a device address), and
+// whether the kernel attributes of one (m16 tiles, half last tile) variant
+// have been set on that device.
 unsigned char* g_scratch_addr[kMaxDevices] = {};
+bool g_prepared[kMaxDevices][5][2] = {};
 std::mutex g_setup_mu;
 
 // Errors are reported through muon_last_error(), like every other entry point.
@@ -76,8 +82,10 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
                                                  int32_t scale_mode, void* stream) {
   if (!params || !grads || !momenta)
     return static_fail(MUON_ERR_INVALID_ARG, "params, grads and momenta must be non-NULL");
-  if (batch < 1 || rows < 1 || cols < 1 || rows > (1 << 30) || cols > (1 << 30))
-    return static_fail(MUON_ERR_INVALID_ARG, "batch, rows and cols must be >= 1");
+  if (batch < 1 || batch > 65535)
+    return static_fail(MUON_ERR_INVALID_ARG, "batch must be in [1, 65535]");
+  if (rows < 1 || cols < 1 || rows > (1 << 30) || cols > (1 << 30))
+    return static_fail(MUON_ERR_INVALID_ARG, "rows and cols must be in [1, 2^30]");
   if (ns_steps < 0 || ns_steps > 1000)
     return static_fail(MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 1000]");
   const float sv[7] = {beta, lr, wd, a, b, c, eps};
@@ -92,23 +100,37 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
 
   const int64_t m = rows < cols ? rows : cols, n = rows < cols ? cols : rows;
   const int64_t n_chunks = (rows * cols + kMomentumChunk - 1) / kMomentumChunk;
-  // scratch layout: scalars | member table | partial sums | fragment iterate
+  // scratch layout: scalars | member table [| partial sums | fragment
+  // iterate, for the direct iteration beyond kGramSpaceMaxSteps only]
+  const bool gram_space = cfg.gram_space && ns_steps <= kGramSpaceMaxSteps;
   const size_t off_mem = align256(sizeof(StepScalars));
   const size_t off_part = align256(off_mem + (size_t)batch * sizeof(MemberPtrs));
   const size_t off_ws = align256(off_part + (size_t)batch * n_chunks * sizeof(float));
-  const size_t total = off_ws + (size_t)batch * cfg.ws_bytes;
+  const size_t total = gram_space ? off_part : off_ws + (size_t)batch * cfg.ws_bytes;
   if (total > kStaticScratchBytes) {
     char msg[200];
     std::snprintf(msg, sizeof msg,
-                  "needs %zu bytes of scratch for batch %d of [%lld, %lld]; the static array "
-                  "holds %zu",
-                  total, batch, (long long)rows, (long long)cols, kStaticScratchBytes);
+                  "needs %zu bytes of scratch for batch %d of [%lld, %lld] at %d steps; the "
+                  "static array holds %zu",
+                  total, batch, (long long)rows, (long long)cols, ns_steps, kStaticScratchBytes);
     return static_fail(MUON_ERR_INVALID_ARG, msg);
   }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return static_fail(MUON_ERR_CUDA, "cudaGetDevice failed");
+  {
+    // the launches and the array address belong to the current device, so
+    // the stream must be one of that device's (the default streams always are)
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int sdev = dev;
+    if (cs != nullptr && cs != cudaStreamLegacy && cs != cudaStreamPerThread &&
+        cudaStreamGetDevice(cs, &sdev) != cudaSuccess)
+      return static_fail(MUON_ERR_INVALID_ARG, "stream is not a valid CUDA stream");
+    if (sdev != dev)
+      return static_fail(MUON_ERR_INVALID_ARG,
+                         "stream belongs to another device than the current one");
+  }
   KArgs k{};
   k.B = batch;
   k.rows = (int32_t)rows;
@@ -126,8 +148,10 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
   k.alpha = (float)std::ldexp(1.0, (int)std::round(0.5 * std::log2((double)n)));
   k.l2_keep_m = 1;
   {
-    // once per device, with that device current: the array's device address
-    // and the kernel attributes (host work only; do it before stream capture)
+    // once per device, with that device current: the array's device address;
+    // once per device and kernel variant: the kernel attributes (host work
+    // only; do the first call before any stream capture)
+    const int mt = cfg.mtiles, half = (int)(m - 16 * (mt - 1) <= 8);
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (!g_scratch_addr[dev]) {
       void* ptr = nullptr;
@@ -136,16 +160,19 @@ extern "C" muon_status_t muon_step_skinny_static(void* params, const void* grads
         return static_fail(MUON_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
       g_scratch_addr[dev] = static_cast<unsigned char*>(ptr);
     }
-    if (prepare_skinny(k, cfg) != cudaSuccess)
-      return static_fail(MUON_ERR_CUDA, "setting the skinny kernel's attributes failed");
+    if (!g_prepared[dev][mt][half]) {
+      if (prepare_skinny(k, cfg) != cudaSuccess)
+        return static_fail(MUON_ERR_CUDA, "setting the skinny kernel's attributes failed");
+      g_prepared[dev][mt][half] = true;
+    }
   }
   unsigned char* base = g_scratch_addr[dev];
   StepScalars* sc = reinterpret_cast<StepScalars*>(base);
   MemberPtrs* mem = reinterpret_cast<MemberPtrs*>(base + off_mem);
   k.sc = sc;
   k.mem = mem;
-  k.part = reinterpret_cast<float*>(base + off_part);
-  k.y0 = base + off_ws;
+  k.part = gram_space ? nullptr : reinterpret_cast<float*>(base + off_part);
+  k.y0 = gram_space ? nullptr : base + off_ws;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StepScalars hs{};

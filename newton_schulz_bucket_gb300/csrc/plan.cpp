@@ -686,6 +686,15 @@ muon_status_t step_impl(muon_plan_t p, void* const* params, const void* const* g
   for (int32_t i = 0; i < np; ++i)
     if (!params[i] || !grads[i] || !momenta[i])
       return fail(MUON_ERR_INVALID_ARG, "parameter %d has a NULL pointer", i);
+  // bf16 operands rounded on every step (every group but a Gram-space skinny
+  // one) drift past the bf16-mode tolerance beyond kBf16OperandMaxSteps
+  if (ns_steps > kBf16OperandMaxSteps)
+    for (const GroupPlan& g : p->d.groups)
+      if (g.ns_type == NS_BF16 && !(g.path == PATH_SKINNY && ns_steps <= kGramSpaceMaxSteps))
+        return fail(MUON_ERR_UNSUPPORTED,
+                    "group [%lld,%lld] iterates on bf16 operands, which is limited to %d "
+                    "Newton-Schulz steps (asked for %d); use fp16 operands",
+                    (long long)g.rows, (long long)g.cols, kBf16OperandMaxSteps, ns_steps);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUDA_TRY(cudaSetDevice(p->device));
   // fill the next pinned slot once its previous copy has been consumed

@@ -107,15 +107,21 @@ def test_spread_spectrum_inputs():
     run.close()
 
 
-def test_zero_gradient_and_momentum():
-    w = W.custom([[24, 2048]], seed=13, g_std=0.0, m_zero=True)
-    run = GpuRun(w)
-    O = run.O(0)
-    assert np.all(O == 0)
-    want = (torch.tensor(run.p0(0), dtype=torch.float32) * F32(1 - F32(w.lr) * F32(w.wd)))
+@pytest.mark.parametrize("shape,k,path", [([24, 2048], 5, "auto"), ([2048, 40], 5, "auto"),
+                                          ([24, 2048], 70, "auto"), ([256, 768], 5, "tensor")],
+                         ids=["gram_space", "gram_space_transposed", "direct_k70", "tensor"])
+def test_zero_gradient_and_momentum(shape, k, path):
+    """M' = 0 gives X = 0, O = 0 and P' = P (1 - lr wd) exactly: one fp32
+    rounding of 1 - lr wd, one of the product, then round-to-nearest-even to
+    bf16 -- on every kernel that writes P."""
+    w = W.custom([shape], seed=13, g_std=0.0, m_zero=True, ns_steps=k, lr=0.3, wd=0.7)
+    run = GpuRun(w, path=path)
+    assert np.all(run.O(0) == 0)
+    decay = np.float32(1.0 - np.float64(np.float32(w.lr)) * np.float64(np.float32(w.wd)))
+    want = torch.tensor(run.p0(0).astype(np.float32) * decay, dtype=torch.float32)
     want = want.to(torch.bfloat16).double().numpy()
-    assert np.array_equal(run.p1(0), want) or np.max(np.abs(run.p1(0) - want)) <= \
-        np.max(np.abs(want)) * 2 ** -8
+    assert np.array_equal(run.p1(0), want)
+    assert np.all(run.m1(0) == 0)
     run.close()
 
 

@@ -8,6 +8,8 @@ import numpy as np
 import pytest
 import torch
 
+import newton_schulz_bucket_gb300 as pkg
+
 from newton_schulz_bucket_gb300 import _capi
 from newton_schulz_bucket_gb300 import workloads as W
 
@@ -100,6 +102,30 @@ def test_tensor_path_parity(shapes):
 
 def test_tensor_path_bf16_operands_and_k10():
     run = GpuRun(W.custom([[256, 768]], seed=22), path="tensor", ns_dtype="bf16")
+    check_all(run)
+    run.close()
+    # bf16 operands rounded on every step are limited to 5 steps (the emulated
+    # error reaches 1.7e-2 at 6 steps and 2.5e-2 at 10, against 2e-2); the
+    # Gram-space skinny kernel rounds the data once and takes up to 64
+    w = W.custom([[256, 768]], seed=22, ns_steps=6)
+    P, G, M = W.make_tensors(w, "cuda")
+    before = P[0].clone()
+    plan = pkg.MuonPlan(w.shapes, path="tensor", ns_dtype="bf16")
+    with pytest.raises(pkg.MuonError) as ei:
+        plan.step(P, G, M, w.beta, w.lr, w.wd, 6)
+    assert ei.value.status == 2  # UNSUPPORTED, nothing launched
+    torch.cuda.synchronize()
+    assert torch.equal(P[0], before)
+    plan.close()
+    sk = pkg.MuonPlan([[24, 1024]], ns_dtype="bf16")
+    ws = W.custom([[24, 1024]], seed=22)
+    P, G, M = W.make_tensors(ws, "cuda")
+    sk.step(P, G, M, 0.95, 0.02, 0.1, 10)
+    with pytest.raises(pkg.MuonError) as ei:
+        sk.step(P, G, M, 0.95, 0.02, 0.1, 70)  # the direct iteration rounds every step
+    assert ei.value.status == 2
+    sk.close()
+    run = GpuRun(W.custom([[24, 4096], [4096, 24]], seed=22, ns_steps=10), ns_dtype="bf16")
     check_all(run)
     run.close()
     run = GpuRun(W.custom([[256, 768], [512, 512]], seed=23, ns_steps=10), path="tensor")
