@@ -1,24 +1,30 @@
 #!/usr/bin/env python3
 """Benchmark of the shape-fused Muon step on GB300 (one JSON line on rank 0).
 
-Default workload: 74 parameters of shape [24, 10240] (bf16 params/grads, fp32
-momentum), 5 quintic Newton-Schulz steps -- the fused batch the pages profile
-(«MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化, Fig. 7).
+Headline workload: the dense h=4096 transformer (32 layers x 4 shape buckets
+of 32 matrices: [4096,12288], [4096,4096], [4096,16384], [16384,4096]; bf16
+params/grads, fp32 momentum, 5 quintic Newton-Schulz steps), the largest of
+the benchmark configurations.  The line also carries a `per_config` block that
+times every configuration the same way: the fp32 64x128 case, the pages' fused
+skinny batch 74 x [24, 10240] («MindSpore HyperParallel X 盘古,Muon优化器实现6倍
+性能跃升», 矩阵融合优化, Fig. 7), the MoE expert tensor with its skinny group,
+the dense model, and the 1000-matrix mixed bag at 5 and 10 steps.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl reference] [--no-per-config] [--no-cpu-baseline] [--no-e2e]
 
 `value` is whole-job algorithmic throughput (GB/s of the compulsory G, M, M',
-P, P' traffic for workloads of memory-bound skinny groups; TFLOP/s of
-4 m^2 n + 2 m^3 per matrix per NS step otherwise) with inputs resident in HBM.
-Timing: CUDA events on the launching stream, W untimed warm-up steps, K timed
-steps, barrier + synchronize on both sides, max over ranks.  As in a training
-loop, every step updates the same buffers; before each step an untimed write
-of twice the L2 size flushes it (as the forward and backward passes would),
-and each step is timed alone by its own event pair (an untimed read of as
-much again drains the flush's write-backs before the step starts).  `e2e` times the same step through
-muon_step_host (host buffers in pinned memory, host->device and device->host
-copies inside the timed region).  `--impl reference` times the CPU oracle on
-the host cores instead.
+P, P' traffic for workloads made only of memory-bound skinny groups; TFLOP/s
+of the dense count 4 m^2 n + 2 m^3 per matrix per NS step otherwise) with
+inputs resident in HBM.  Timing: CUDA events on the launching stream, W
+untimed warm-up steps, K timed steps, barrier + synchronize on both sides, max
+over ranks.  As in a training loop, every step updates the same buffers;
+before each step an untimed write of twice the L2 size flushes it, an untimed
+read of as much drains the flush's write-backs, and each step is timed alone
+by its own event pair.  `e2e` times the same step through muon_step_host
+(host buffers in pinned memory, host->device and device->host copies inside
+the timed region).  `--impl reference` times the CPU oracle on the host cores
+instead (it never loads the CUDA library).
 """
 from __future__ import annotations
 
@@ -36,8 +42,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused Muon step ms & TFLOP/s (or GB/s) per shape group, % roofline, 1×GB300"
-DEFAULT_CONFIG = "c2_skinny_74x24x10240"
+DEFAULT_CONFIG = "c4_dense_h4096"
+PER_CONFIG = [("c1_fp32_64x128", None), ("c2_skinny_74x24x10240", None),
+              ("c3_moe_64x2048x7168_32x24x10240", None), ("c4_dense_h4096", None),
+              ("c5_mixed_1000", 5), ("c5_mixed_1000", 10)]
 L2_BYTES = 129 * 2 ** 20
+SKINNY_MAX_M = 64  # the planner's default skinny threshold (min(rows, cols) <= 64)
 
 
 def algorithmic_work(shapes, mode, k):
@@ -52,6 +62,24 @@ def algorithmic_work(shapes, mode, k):
         byts += E * r * c * (pb + 4 + 4 + pb + pb)
         flops += E * k * (4 * m * m * n + 2 * m ** 3)
     return byts, flops
+
+
+def shape_groups(shapes, mode):
+    """The planner's default bucketing restated for the report: exact
+    (rows, cols) keys in first-seen order, 3-D parameters contributing E
+    members, and the path each group takes by default (skinny for
+    min(rows, cols) <= 64 in bf16 mode, tensor above, SIMT in fp32 mode).
+    Pure Python, so the reference arm never loads the CUDA library."""
+    groups = {}
+    for s in shapes:
+        E = s[0] if len(s) == 3 else 1
+        key = (s[-2], s[-1])
+        groups[key] = groups.get(key, 0) + E
+    out = []
+    for (r, c), b in groups.items():
+        path = "simt" if mode == "fp32" else ("skinny" if min(r, c) <= SKINNY_MAX_M else "tensor")
+        out.append({"rows": r, "cols": c, "batch": b, "path": path})
+    return out
 
 
 def load_peaks():
@@ -71,15 +99,16 @@ def kernel_source_hash(name):
 
 
 def ncu_traffic(kernel_file, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel; else None."""
+    """DRAM bytes (read + write) per launch of the dominant kernel, from the
+    committed ncu summary, if it was taken on the current source of that
+    kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(workload)
     if not d or d.get("source_sha256_16") != kernel_source_hash(kernel_file):
         return None
-    return d.get("dram_bytes_per_launch")
+    return d
 
 
 class ClockSampler:
@@ -88,7 +117,7 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join("/tmp", f"muon_clocks_{os.getpid()}.csv")
+        self.path = os.path.join("/tmp", f"muon_clocks_{os.getpid()}_{time.monotonic_ns()}.csv")
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -126,7 +155,7 @@ class ClockSampler:
             except ValueError:
                 continue
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl) if v == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
@@ -159,29 +188,7 @@ def allmax(world, v):
     return v
 
 
-def oracle_time(w, sample, host_inputs):
-    """Times the CPU oracle on a per-group sample [(members, group size), ...]
-    (members: list of (param, expert)).  Returns (seconds for the whole
-    workload, each group's time scaled by its size over its sample; wall
-    seconds timed; process CPU seconds timed).  CPU over wall is the number
-    of host threads the oracle kept busy (NumPy's BLAS may use several).
-    Each group's inputs are drawn before its timed region."""
-    import numpy as np
-    from oracle import muon_ref
-    f32 = lambda v: float(np.float32(v))
-    a, b, c = (f32(v) for v in w.coeffs)
-    total = wall = cpu = 0.0
-    for members, size in sample:
-        inputs = [host_inputs(i, e) for (i, e) in members]
-        t0, c0 = time.perf_counter(), time.process_time()
-        for P, G, M in inputs:
-            muon_ref.muon_update_ref(P, G, M, f32(w.beta), f32(w.lr), f32(w.wd), w.ns_steps,
-                                     a, b, c)
-        dt, dc = time.perf_counter() - t0, time.process_time() - c0
-        wall += dt
-        cpu += dc
-        total += dt * size / len(members)
-    return total, wall, cpu
+# ---------------------------------------------------------------- CPU oracle
 
 
 def blas_name():
@@ -200,35 +207,6 @@ def busy_cores(wall, cpu):
     return max(1, math.ceil(cpu / wall - 0.05)) if wall > 0 else 1
 
 
-def sample_members(w, budget_s=12.0):
-    """Seeded per-group sample for timing the oracle: every shape group gets
-    at least one member, and as many more as its share of budget_s allows at
-    the estimated cost of one member.  Returns [(members, group size), ...].
-    A group whose single member costs more than its share still gets one, so
-    workloads of large matrices run past the budget."""
-    import random
-    groups = {}
-    for i, s in enumerate(w.shapes):
-        for e in range(s[0] if len(s) == 3 else 1):
-            groups.setdefault((s[-2], s[-1]), []).append((i, e))
-    rng = random.Random(1234)
-    share = budget_s / len(groups)
-    out = []
-    for (r, c), mem in groups.items():
-        m, n = min(r, c), max(r, c)
-        cost = w.ns_steps * (4 * m * m * n + 2 * m ** 3) / 2.5e10 + r * c * 1e-8
-        order = mem[:]
-        rng.shuffle(order)
-        out.append((order[:max(1, min(len(order), int(share / cost)))], len(mem)))
-    return out
-
-
-def sample_note(sample):
-    n = sum(len(m) for m, _ in sample)
-    return (f"{n} of {sum(s for _, s in sample)} matrices per step, at least one of each of the "
-            f"{len(sample)} shape groups; each group extrapolated by its member count")
-
-
 def host_member_inputs(w):
     """Host fp64 inputs of single members, each drawn alone from its own
     parameter's (or expert's) law, for timing the oracle: the values need not
@@ -245,6 +223,145 @@ def host_member_inputs(w):
     return get
 
 
+def member_flops(rows, cols, k):
+    m, n = min(rows, cols), max(rows, cols)
+    return k * (4 * m * m * n + 2 * m ** 3)
+
+
+def workload_groups(w):
+    """{(rows, cols): [(param, expert), ...]} in first-seen order."""
+    groups = {}
+    for i, s in enumerate(w.shapes):
+        for e in range(s[0] if len(s) == 3 else 1):
+            groups.setdefault((s[-2], s[-1]), []).append((i, e))
+    return groups
+
+
+def time_members(w, members, get):
+    """Wall and process-CPU seconds of the oracle on `members` (inputs drawn
+    before the timed region)."""
+    import numpy as np
+    from oracle import muon_ref
+    f32 = lambda v: float(np.float32(v))
+    a, b, c = (f32(v) for v in w.coeffs)
+    inputs = [get(i, e) for (i, e) in members]
+    t0, c0 = time.perf_counter(), time.process_time()
+    for P, G, M in inputs:
+        muon_ref.muon_update_ref(P, G, M, f32(w.beta), f32(w.lr), f32(w.wd), w.ns_steps, a, b, c)
+    return time.perf_counter() - t0, time.process_time() - c0
+
+
+def oracle_estimate(w, budget_s, get):
+    """The oracle's time for one whole step of w, from a bounded sample.
+
+    Groups are taken cheapest member first.  Each taken group gets as many
+    members as its share of the budget allows (at least one) and is
+    extrapolated by its member count.  Once the budget is spent, the groups
+    left (whose single member would overrun it) are extrapolated by their
+    dense Newton-Schulz FLOPs at the FLOP rate the oracle reached on the
+    largest sampled tensor-size group (or by bytes for skinny-size groups).
+    Returns (seconds per step, wall, cpu, sample note)."""
+    import random
+    rng = random.Random(1234)
+    groups = workload_groups(w)
+    keys = sorted(groups, key=lambda k: member_flops(k[0], k[1], w.ns_steps) + k[0] * k[1])
+    total = wall = cpu = 0.0
+    rate_flops = None   # oracle FLOP/s on the largest timed tensor-size group
+    rate_elem = None    # oracle seconds per element on the largest timed skinny-size group
+    timed, left = [], []
+    spent = 0.0
+    for key in keys:
+        mem = groups[key][:]
+        rng.shuffle(mem)
+        r, c = key
+        fl = member_flops(r, c, w.ns_steps)
+        # projected seconds of one member from what has been measured so far
+        guess = (fl / rate_flops if rate_flops else fl / 2.5e11) + r * c * 2e-8
+        if timed and spent + guess > budget_s:
+            left.append(key)
+            continue
+        n = 1
+        if guess > 0:
+            n = max(1, min(len(mem), int(max(budget_s - spent, 0.0) / max(guess, 1e-6) / 4)))
+        dt, dc = time_members(w, mem[:n], get)
+        spent += dt
+        wall += dt
+        cpu += dc
+        total += dt * len(mem) / n
+        timed.append(f"{n} of {len(mem)} x {list(key)}")
+        if min(r, c) > SKINNY_MAX_M:
+            rate_flops = fl * n / dt
+        else:
+            rate_elem = dt / (n * r * c)
+    for (r, c) in left:
+        cnt = len(groups[(r, c)])
+        if min(r, c) > SKINNY_MAX_M and rate_flops:
+            total += cnt * member_flops(r, c, w.ns_steps) / rate_flops
+        else:
+            total += cnt * r * c * (rate_elem or 2e-8)
+    note = "timed: " + "; ".join(timed)
+    if left:
+        note += ("; extrapolated by dense NS FLOPs at the oracle's measured rate: " +
+                 "; ".join(f"{len(groups[k])} x {list(k)}" for k in left))
+    return total, wall, cpu, note
+
+
+def headline(w, byts, flops, seconds):
+    """GB/s for workloads made only of skinny groups, else TFLOP/s."""
+    if all(g["path"] == "skinny" for g in shape_groups(w.shapes, w.mode)):
+        return byts / seconds / 1e9, "GB/s"
+    return flops / seconds / 1e12, "TFLOP/s"
+
+
+def config_dict(w, world, in_bytes=None):
+    """The `config` of the JSON line (the same for both arms)."""
+    d = {"workload": w.name, "shapes": describe_shapes(w.shapes), "ns_steps": w.ns_steps,
+         "coeffs": list(w.coeffs), "mode": w.mode,
+         "ns_operands": "fp32 (FFMA)" if w.mode == "fp32" else "fp16 (fp32 accumulate)",
+         "l2": "same buffers every step; L2 flushed before each step by an untimed "
+               f"{2 * L2_BYTES / 1e6:.0f} MB write, then drained by an untimed read of as much; "
+               "each step timed alone",
+         "parallelism": f"replicas x{world}"}
+    return d
+
+
+def run_reference(args, w, world, rank):
+    """--impl reference: the CPU oracle as it stands, on the host cores.  Each
+    step times a bounded sample of the workload and extrapolates it to the
+    whole step; nothing here loads the CUDA library."""
+    if rank != 0:
+        return
+    byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
+    get = host_member_inputs(w)
+    budget = max(1.0, 90.0 / max(1, args.steps))
+    smallest = min(workload_groups(w).items(), key=lambda kv: kv[0][0] * kv[0][1])
+    for _ in range(args.warmup):   # warms NumPy's BLAS on one member of the smallest group
+        time_members(w, smallest[1][:1], get)
+    runs = [oracle_estimate(w, budget, get) for _ in range(args.steps)]
+    per_step = statistics.mean(r[0] for r in runs)  # extrapolated to the whole workload
+    value, unit = headline(w, byts, flops, per_step)
+    cores = busy_cores(sum(r[1] for r in runs), sum(r[2] for r in runs))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, world),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores,
+                             "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
+                             "sample": runs[0][3] + " (per step; members drawn before timing)"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def describe_shapes(shapes):
+    from collections import Counter
+    c = Counter(tuple(s) for s in shapes)
+    return ", ".join(f"{n}x{list(s)}" for s, n in c.items())
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
 def executed_flop_fraction(rows, cols):
     """Share of the dense count k (4 m^2 n + 2 m^3) the tensor path executes.
     The Gram matrix (2 m^2 n) and A^2 (2 m^3) are symmetric, so their GEMMs
@@ -258,68 +375,167 @@ def executed_flop_fraction(rows, cols):
     return (sym * (2 * m * m * n + 2 * m ** 3) + 2 * m * m * n) / dense
 
 
-def executed_flops(w):
+def executed_flops(w, groups):
     """Newton-Schulz FLOPs the step executes (the dense count, with the
     symmetric products of tensor-path groups reduced to their computed tiles;
     skinny groups are counted dense)."""
-    pkg = __import__("newton_schulz_bucket_gb300")
     tot = 0.0
-    for g in pkg.describe(w.shapes, mode=w.mode)["groups"]:
-        m, n = min(g["rows"], g["cols"]), max(g["rows"], g["cols"])
-        f = w.ns_steps * (4 * m * m * n + 2 * m ** 3) * g["batch"]
+    for g in groups:
+        f = member_flops(g["rows"], g["cols"], w.ns_steps) * g["batch"]
         tot += f * (executed_flop_fraction(g["rows"], g["cols"]) if g["path"] == "tensor" else 1.0)
     return tot
 
 
-def headline(w, byts, flops, seconds):
-    """GB/s for workloads of skinny groups only, else TFLOP/s."""
-    from newton_schulz_bucket_gb300 import describe
-    paths = {g["path"] for g in describe(w.shapes, mode=w.mode)["groups"]}
-    if paths <= {"skinny"}:
-        return byts / seconds / 1e9, "GB/s"
-    return flops / seconds / 1e12, "TFLOP/s"
+def group_entry(info, gms, w, peaks):
+    """One group's row: ms, matrices/s and its roofline (HBM when its dense
+    FLOPs per compulsory byte fall below the ridge -- every skinny group and
+    small-m tensor groups such as [128, 4096] -- else the tensor cores)."""
+    shp = [info["rows"], info["cols"]]
+    gb, gf = algorithmic_work([[info["batch"]] + shp], w.mode, w.ns_steps)
+    ent = {"shape": shp, "batch": info["batch"], "path": info["path"], "ms": gms}
+    if not gms:
+        return ent
+    ent["matrices_per_s"] = info["batch"] / (gms / 1e3)
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if info["path"] == "skinny" or gf / gb < ridge:
+        ach = gb / (gms / 1e3) / 1e9
+        ent.update({"GB_s": ach, "roofline_frac": ach / peaks["hbm_gbs"], "bound": "hbm",
+                    "flop_per_byte": gf / gb})
+    else:
+        # TFLOP/s of the dense count (algorithmic); the executed rate counts
+        # only the tiles the symmetric products compute
+        ach = gf / (gms / 1e3) / 1e12
+        xf = executed_flop_fraction(*shp) if info["path"] == "tensor" else 1.0
+        ent.update({"TFLOP_s": ach, "roofline_frac": ach / peaks["bf16_tflops_sustained"],
+                    "bound": "tensor", "executed_flop_fraction": xf, "TFLOP_s_executed": ach * xf,
+                    "roofline_frac_executed": ach * xf / peaks["bf16_tflops_sustained"]})
+    return ent
 
 
-def run_reference(args, w, world, rank):
-    """--impl reference: the CPU oracle as it stands, on the host cores."""
-    if rank != 0:
-        return
+def roofline_of(w, dg, peaks):
+    """The `roofline` object for the dominant group `dg`."""
+    if dg.get("bound") == "hbm":
+        if dg["path"] == "skinny":
+            gram_space = w.ns_steps <= 64
+            kfile = "k_skinny_gs.cuh" if gram_space else "k_skinny.cu"
+            kernel = ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"
+                      if gram_space else "k_momentum_partial + k_skinny_ns")
+        else:
+            kfile = None
+            kernel = f"group {dg['shape']} x {dg['batch']}: k_tc_gemm chain and the elementwise passes"
+        tr = ncu_traffic(kfile, w.name) if kfile else None
+        roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dg.get("roofline_frac"), "kernel": kernel,
+                "peak_source": peaks["source"] + " hbm_gbs (burst copy)"}
+    else:
+        tr = ncu_traffic("k_tc_gemm.cu", w.name)
+        roof = {"bound": "tensor", "achieved": dg.get("TFLOP_s"), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": dg.get("roofline_frac"),
+                "kernel": f"group {dg['shape']} x {dg['batch']}: its k_tc_gemm launches "
+                          "(Gram, polynomial, update per step) and elementwise passes",
+                "peak_source": peaks["source"] + " bf16_tflops_sustained",
+                "flops_counted": "dense k (4 m^2 n + 2 m^3); the symmetric Gram and A^2 compute "
+                                 "only upper-triangle tiles",
+                "executed_flop_fraction": dg.get("executed_flop_fraction"),
+                "achieved_executed": dg.get("TFLOP_s_executed"),
+                "frac_executed": dg.get("roofline_frac_executed")}
+    # DRAM bytes of the dominant kernel from one ncu capture, per launch; null
+    # once the kernel source changed since the capture
+    roof["traffic"] = tr.get("dram_bytes_per_launch") if tr else None
+    if tr:
+        roof["traffic_detail"] = {k: tr[k] for k in ("dram_read_bytes", "dram_write_bytes",
+                                                     "compulsory_read_bytes", "compulsory_write_bytes",
+                                                     "note") if k in tr}
+    return roof
+
+
+def measure(w, args, pkg, torch, dev, local, world, peaks, stream, flush, sample_clocks):
+    """Times workload w on this GPU: K timed steps (the whole step, every
+    group), then per-group times from a second plan that runs the groups one
+    after another.  Returns (summary dict, kernel launches per step)."""
+    from newton_schulz_bucket_gb300 import workloads as W
     byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
-    sample = sample_members(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
-    get = host_member_inputs(w)
-    for _ in range(args.warmup):
-        oracle_time(w, [(sample[0][0][:1], 1)], get)
-    runs = [oracle_time(w, sample, get) for _ in range(args.steps)]
-    per_step = statistics.mean(r[0] for r in runs)  # extrapolated to the whole workload
-    value, unit = headline(w, byts, flops, per_step)
-    cores = busy_cores(sum(r[1] for r in runs), sum(r[2] for r in runs))
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "ns_steps": w.ns_steps},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": cores,
-                             "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
-                             "sample": sample_note(sample)},
-            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    tensors = W.make_tensors(w, dev)
+    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode)
+    groups = plan.groups()
+    bound = plan.bind(*tensors)
+    sp = stream.cuda_stream
 
+    def step():
+        plan.step_bound(bound, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs, stream=sp)
 
-def describe_shapes(shapes):
-    from collections import Counter
-    c = Counter(tuple(s) for s in shapes)
-    return ", ".join(f"{n}x{list(s)}" for s, n in c.items())
+    for j in range(args.warmup):
+        flush(j)
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clk = ClockSampler(local) if sample_clocks else None
+    if clk:
+        clk.__enter__()
+    t_wall = time.perf_counter()
+    for j in range(args.steps):
+        flush(j)
+        evs[j][0].record(stream)
+        step()
+        evs[j][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if clk:
+        clk.__exit__(None, None, None)
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    barrier(world)
+    launches = plan.kernels_per_step(w.ns_steps)
+    plan.close()
+    # per-group kernel times from events recorded inside the step graph of a
+    # plan that runs the groups one after another
+    tplan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, group_timing=True, max_streams=1)
+    tbound = tplan.bind(*tensors)
+    gtimes = [[] for _ in groups]
+    for j in range(min(args.steps, 6) + 1):
+        flush(j)
+        tplan.step_bound(tbound, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs, stream=sp)
+        if j == 0:
+            continue  # graph capture
+        for g in range(len(groups)):
+            gtimes[g].append(tplan.group_elapsed_ms(g))
+    torch.cuda.synchronize()
+    tplan.close()
+    del tensors, bound, tbound
+    torch.cuda.empty_cache()
+
+    ms_step = allmax(world, sum(step_ms)) / args.steps
+    sec = ms_step / 1e3
+    value_1, unit = headline(w, byts, flops, sec)
+    per_group = [group_entry(info, statistics.mean(gtimes[g]) if gtimes[g] else None, w, peaks)
+                 for g, info in enumerate(groups)]
+    dom = max(range(len(groups)), key=lambda g: per_group[g]["ms"] or 0)
+    out = {"workload": w.name, "shapes": describe_shapes(w.shapes), "ns_steps": w.ns_steps,
+           "value": value_1 * world, "unit": unit, "ms_per_step": ms_step,
+           "step_ms_this_rank": {"median": statistics.median(step_ms), "min": min(step_ms),
+                                 "max": max(step_ms)},
+           "matrices_per_s": sum(g["batch"] for g in groups) * world / sec,
+           "tflops": flops * world / sec / 1e12, "gbs": byts * world / sec / 1e9,
+           "tflops_executed": executed_flops(w, groups) * world / sec / 1e12,
+           "per_group": per_group, "roofline": roofline_of(w, per_group[dom], peaks),
+           "wall_s_timed": t_wall}
+    if clk:
+        out["clocks"] = clk.summary()
+    return out, launches
 
 
 def run_e2e(args, w, pkg, torch, dev, local, byts, flops, world):
     """Same step through muon_step_host: H2D of P, G, M and D2H of P', M'
-    inside the timed region."""
+    inside the timed region.  The pinned host buffers are filled on the host
+    from the device draw, one parameter at a time."""
     from newton_schulz_bucket_gb300 import workloads as W
-    P, G, M = W.make_tensors(w, dev)
-    hP = torch.cat([t.reshape(-1) for t in P]).cpu().pin_memory()
-    hG = torch.cat([t.reshape(-1) for t in G]).cpu().pin_memory()
-    hM = torch.cat([t.reshape(-1) for t in M]).cpu().pin_memory()
-    del P, G, M
+    pdt = torch.bfloat16 if w.mode == "bf16" else torch.float32
+    el = sum(math.prod(s) for s in w.shapes)
+    hP = torch.empty(el, dtype=pdt, pin_memory=True)
+    hG = torch.empty(el, dtype=pdt, pin_memory=True)
+    hM = torch.empty(el, dtype=torch.float32, pin_memory=True)
 
     def views(flat):
         out, o = [], 0
@@ -329,13 +545,18 @@ def run_e2e(args, w, pkg, torch, dev, local, byts, flops, world):
             o += n
         return out
     vP, vG, vM = views(hP), views(hG), views(hM)
+    P, G, M = W.make_tensors(w, dev)
+    for i in range(len(w.shapes)):
+        vP[i].copy_(P[i]); vG[i].copy_(G[i]); vM[i].copy_(M[i])
+    del P, G, M
+    torch.cuda.empty_cache()
     plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, host_staging=True)
     stream = torch.cuda.Stream(dev)
     for _ in range(max(2, args.warmup // 2)):
         plan.step_host(vP, vG, vM, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs, stream=stream)
     torch.cuda.synchronize()
     barrier(world)
-    n = max(3, args.steps // 2)
+    n = max(3, args.steps // 4)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -345,10 +566,11 @@ def run_e2e(args, w, pkg, torch, dev, local, byts, flops, world):
     torch.cuda.synchronize()
     ms = allmax(world, ev0.elapsed_time(ev1)) / n
     plan.close()
+    del hP, hG, hM, vP, vG, vM
+    torch.cuda.empty_cache()
     v, u = headline(w, byts, flops, ms / 1e3)
     pb = 2 if w.mode == "bf16" else 4
-    el = sum(math.prod(s) for s in w.shapes)
-    return {"value": v * world, "unit": u, "ms_per_step": ms,
+    return {"value": v * world, "unit": u, "ms_per_step": ms, "steps": n,
             "h2d_bytes_per_step": el * (pb + pb + 4), "d2h_bytes_per_step": el * (pb + 4)}
 
 
@@ -362,6 +584,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -377,20 +600,8 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
-    in_bytes = sum(math.prod(s) for s in w.shapes) * (8 if w.mode == "bf16" else 12)
-    tensors = W.make_tensors(w, dev)
-    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode)
-    groups = plan.groups()
-    # per-group times come from a second plan that runs the groups one after
-    # another (the timed plan overlaps them on several streams)
-    tplan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, group_timing=True, max_streams=1)
+    peaks = load_peaks()
     stream = torch.cuda.Stream(dev)
-    coeffs = w.coeffs
-    # pointer arrays marshalled once, as a C caller would hold them
-    bound = plan.bind(*tensors)
-    tbound = tplan.bind(*tensors)
-    sp = stream.cuda_stream
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     drain_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -403,99 +614,20 @@ def main():
             flush_buf.fill_(float(j))
             torch.sum(drain_buf, dim=0, out=sink)
 
-    def step():
-        plan.step_bound(bound, w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=sp)
+    head, launches = measure(w, args, pkg, torch, dev, local, world, peaks, stream, flush, True)
+    byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
 
-    for j in range(args.warmup):
-        flush(j)
-        step()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    gtimes = [[] for _ in groups]
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        for j in range(args.steps):
-            flush(j)
-            evs[j][0].record(stream)
-            step()
-            evs[j][1].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-        step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-        ms_total = sum(step_ms)
-        # per-group kernel times from events recorded inside the step graph
-        for j in range(min(args.steps, 6) + 1):
-            flush(j)
-            tplan.step_bound(tbound, w.beta, w.lr, w.wd, w.ns_steps, coeffs, stream=sp)
-            if j == 0:
-                continue  # graph capture
-            for g in range(len(groups)):
-                gtimes[g].append(tplan.group_elapsed_ms(g))
-    torch.cuda.synchronize()
-    barrier(world)
-    ms_total = allmax(world, ms_total)
-    ms_step = ms_total / args.steps
-    sec = ms_step / 1e3
-    value_1, unit = headline(w, byts, flops, sec)
-    value = value_1 * world  # every rank ran the same-sized workload (weak scaling)
-
-    peaks = load_peaks()
-    per_group = []
-    for g, info in enumerate(groups):
-        shp = [info["rows"], info["cols"]]
-        gb, gf = algorithmic_work([[info["batch"]] + shp], w.mode, w.ns_steps)
-        gms = statistics.mean(gtimes[g]) if gtimes[g] else None
-        ent = {"shape": shp, "batch": info["batch"], "path": info["path"], "ms": gms}
-        if gms:
-            ent["matrices_per_s"] = info["batch"] / (gms / 1e3)
-            # the roofline that bounds the group: HBM when its dense FLOPs per
-            # compulsory byte fall below the ridge (peak FLOP/s / peak bytes/s;
-            # every skinny group and small-m tensor groups such as [128, 4096]),
-            # else the tensor cores
-            ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-            if info["path"] == "skinny" or gf / gb < ridge:
-                ach = gb / (gms / 1e3) / 1e9
-                ent.update({"GB_s": ach, "roofline_frac": ach / peaks["hbm_gbs"], "bound": "hbm",
-                            "flop_per_byte": gf / gb})
+    per_config = None
+    if not args.no_per_config:
+        per_config = []
+        for name, k in PER_CONFIG:
+            wc = W.get(name, k)
+            if wc.name == w.name and wc.ns_steps == w.ns_steps:
+                ent = {kk: vv for kk, vv in head.items() if kk != "wall_s_timed"}
             else:
-                # TFLOP/s of the dense count (algorithmic); the executed rate
-                # counts only the tiles the symmetric products compute
-                ach = gf / (gms / 1e3) / 1e12
-                xf = executed_flop_fraction(*shp) if info["path"] == "tensor" else 1.0
-                ent.update({"TFLOP_s": ach, "roofline_frac": ach / peaks["bf16_tflops_sustained"],
-                            "bound": "tensor", "executed_flop_fraction": xf,
-                            "TFLOP_s_executed": ach * xf,
-                            "roofline_frac_executed": ach * xf / peaks["bf16_tflops_sustained"]})
-        per_group.append(ent)
-
-    dom = max(range(len(groups)), key=lambda g: per_group[g]["ms"] or 0)
-    dg = per_group[dom]
-    if dg.get("bound") == "hbm":
-        if dg["path"] == "skinny":
-            gram_space = w.ns_steps <= 64
-            kfile = "k_skinny_gs.cuh" if gram_space else "k_skinny.cu"
-            kernel = ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"
-                      if gram_space else "k_momentum_partial + k_skinny_ns")
-            traffic = ncu_traffic(kfile, w.name)
-        else:
-            kernel = f"group {dg['shape']} chain (k_tc_gemm and the elementwise passes)"
-            traffic = None
-        roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": dg.get("roofline_frac"), "kernel": kernel, "traffic": traffic,
-                "peak_source": peaks["source"] + " hbm_gbs (burst copy)"}
-    else:
-        roof = {"bound": "tensor", "achieved": dg.get("TFLOP_s"), "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": dg.get("roofline_frac"),
-                "kernel": f"group {dg['shape']} chain (k_tc_gemm)",
-                "traffic": None, "peak_source": peaks["source"] + " bf16_tflops_sustained",
-                "flops_counted": "dense k (4 m^2 n + 2 m^3); the symmetric Gram and A^2 compute "
-                                 "only upper-triangle tiles",
-                "executed_flop_fraction": dg.get("executed_flop_fraction"),
-                "achieved_executed": dg.get("TFLOP_s_executed"),
-                "frac_executed": dg.get("roofline_frac_executed")}
+                ent, _ = measure(wc, args, pkg, torch, dev, local, world, peaks, stream, flush, True)
+                ent.pop("wall_s_timed", None)
+            per_config.append(ent)
 
     e2e = None
     if not args.no_e2e:
@@ -503,38 +635,28 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = sample_members(w, budget_s=12.0)
-        t, wall, cpu_s = oracle_time(w, sample, host_member_inputs(w))
+        t, wall, cpu_s, note = oracle_estimate(w, 20.0, host_member_inputs(w))
         cv, cu = headline(w, byts, flops, t)
         cpu = {"value": cv, "unit": cu, "cores": busy_cores(wall, cpu_s),
                "host_cores": os.cpu_count(), "blas": blas_name(), "kind": "oracle",
-               "sample": sample_note(sample), "ms_per_step": t * 1e3}
+               "sample": note + " (members drawn before timing)", "ms_per_step": t * 1e3,
+               "wall_s": wall}
 
-    launches = plan.kernels_per_step(w.ns_steps) * args.steps
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-                "step_ms_this_rank": {"median": statistics.median(step_ms), "min": min(step_ms),
-                                      "max": max(step_ms)},
+        line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "step_ms_this_rank": head["step_ms_this_rank"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.mode == "bf16" else "f32",
-                "data": "synthetic: seeded Gaussian G, M0 (std 1e-3), P (std 0.02)",
-                "config": {"workload": w.name, "shapes": describe_shapes(w.shapes),
-                           "ns_steps": w.ns_steps, "coeffs": list(w.coeffs),
-                           "ns_operands": "fp16 (fp32 accumulate)",
-                           "l2": f"same buffers every step ({in_bytes / 1e6:.0f} MB of P, G, M); "
-                                 f"L2 flushed before each step by an untimed {2 * L2_BYTES / 1e6:.0f} MB "
-                                 "write, then drained by an untimed read of as much; each step timed alone",
-                           "parallelism": f"replicas x{world}"},
-                "matrices_per_s": sum(g["batch"] for g in groups) * world / sec,
-                "tflops": flops * world / sec / 1e12, "gbs": byts * world / sec / 1e9,
-                "tflops_executed": executed_flops(w) * world / sec / 1e12,
-                "per_group": per_group, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clk.summary(),
-                "wall_s_timed": t_wall}
+                "data": "synthetic: seeded Gaussian G, M0, P (per-config stds); no dataset",
+                "config": config_dict(w, world),
+                "matrices_per_s": head["matrices_per_s"], "tflops": head["tflops"],
+                "gbs": head["gbs"], "tflops_executed": head["tflops_executed"],
+                "per_group": head["per_group"], "roofline": head["roofline"],
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches * args.steps, "clocks": head.get("clocks"),
+                "wall_s_timed": head["wall_s_timed"], "per_config": per_config}
         print(json.dumps(line), flush=True)
-    plan.close()
-    tplan.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -94,19 +94,28 @@ def test_host_member_inputs_draw_single_members():
     assert all((x == y).all() for x, y in zip(a, b))
 
 
-def test_oracle_sample_covers_every_shape_group():
-    """The CPU baseline's sample holds at least one member of every shape
-    group, no member twice, and the group sizes add up to the workload."""
-    for name in ["c2_skinny_74x24x10240", "c3_moe_64x2048x7168_32x24x10240", "c5_mixed_1000"]:
+def test_oracle_estimate_samples_and_extrapolates():
+    """The CPU baseline's estimate: with a generous budget every group is
+    timed (members of the cheapest first); with a tiny one only the cheapest
+    group is, and the others are extrapolated by FLOPs at the measured rate."""
+    w = W.custom([[24, 512]] * 3 + [[96, 256]] * 2 + [[160, 320]], seed=5)
+    get = bench.host_member_inputs(w)
+    t, wall, cpu, note = bench.oracle_estimate(w, 30.0, get)
+    assert t > 0 and wall > 0 and cpu >= 0
+    assert "extrapolated" not in note
+    assert note.count(" of ") == 3
+    t2, _, _, note2 = bench.oracle_estimate(w, 1e-9, get)
+    assert t2 > 0 and note2.count(" of ") == 1 and "extrapolated" in note2
+    assert "[24, 512]" in note2.split("extrapolated")[0]
+
+
+def test_report_groups_match_the_planner():
+    """bench.py restates the planner's default bucketing and path choice in
+    Python (so its reference arm never loads the library); it must agree
+    with muon_plan_describe on every configuration."""
+    import newton_schulz_bucket_gb300 as pkg
+    for name in W.ALL:
         w = W.get(name)
-        sample = bench.sample_members(w, budget_s=12.0)
-        keys = {tuple(s[-2:]) for s in w.shapes}
-        assert len(sample) == len(keys)
-        assert sum(size for _, size in sample) == sum(s[0] if len(s) == 3 else 1 for s in w.shapes)
-        seen = set()
-        for members, size in sample:
-            assert 1 <= len(members) <= size
-            assert len({tuple(w.shapes[i][-2:]) for i, _ in members}) == 1
-            assert not (seen & set(members))
-            seen |= set(members)
-    assert len(bench.sample_members(W.get("c2_skinny_74x24x10240"), 12.0)[0][0]) == 74
+        want = [{k: g[k] for k in ("rows", "cols", "batch", "path")}
+                for g in pkg.describe(w.shapes, mode=w.mode)["groups"]]
+        assert bench.shape_groups(w.shapes, w.mode) == want, name
