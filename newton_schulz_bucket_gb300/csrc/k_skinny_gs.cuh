@@ -372,10 +372,10 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
     const int sb = r * NW + c.warp;
     if (r >= rounds || sb >= nsb) return;
     const int J = c.c0 + sb * 32, jm = J + 4 * c.g, jp = J + 8 * c.t4;
-    // B fragments: b[kk][q] = rows (2 t4, 2 t4 + 1) and (2 t4 + 8, 2 t4 + 9) of column jm + q
-    uint32_t b[MT][4][2];
-#pragma unroll
-    for (int kk = 0; kk < MT; ++kk) {
+    // B fragments of k-tile kk: bh[q] / bl[q] = rows (2 t4, 2 t4 + 1) and
+    // (2 t4 + 8, 2 t4 + 9) of column jm + q of Y_0, as an operand-type high
+    // part and the operand-type residual of Y_0 - high.
+    auto make_b = [&](int kk, uint32_t (&bh)[4][2], uint32_t (&bl)[4][2]) {
       const bool half = HALF && kk == MT - 1;
       float v[4][4];
 #pragma unroll
@@ -410,18 +410,72 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
           }
         }
       }
+      // Y_0 = alpha M' / (||M'|| + eps) in fp32, split as high + residual
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float2 lo = __fmul2_rn(make_float2(v[0][q], v[1][q]), inv2);
-        b[kk][q][0] = Mma<TY>::pack(lo.x, lo.y);
-        if (half) {
-          b[kk][q][1] = 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (half && h == 1) {
+            bh[q][1] = bl[q][1] = 0u;
+            continue;
+          }
+          const float2 y = __fmul2_rn(make_float2(v[2 * h][q], v[2 * h + 1][q]), inv2);
+          bh[q][h] = Mma<TY>::pack(y.x, y.y);
+          const float2 yh = Mma<TY>::unpack(bh[q][h]);
+          bl[q][h] = Mma<TY>::pack(y.x - yh.x, y.y - yh.y);
+        }
+      }
+    };
+    // With several 16-row output tiles, each k-tile's fragments are needed
+    // once per output tile, and holding both parts of every k-tile in
+    // registers would not fit: on the vector path they are formed once and
+    // written over this lane's own fp32 rows of the ring slot (the same 64
+    // bytes per k-tile: chunk 4 kk + h holds bh[.][h], chunk 4 kk + 2 + h
+    // holds bl[.][h]; a half k-tile has chunks 4 kk + {0, 1} only), then
+    // read back per output tile.  The scalar path rebuilds them.
+    constexpr bool kStage = MT > 1;
+    if (kStage && c.vec) {
+#pragma unroll
+      for (int kk = 0; kk < MT; ++kk) {
+        uint32_t bh[4][2], bl[4][2];
+        make_b(kk, bh, bl);
+        uint8_t* base = const_cast<uint8_t*>(st) + (4 * kk) * 512 + lane * 16;
+        if (HALF && kk == MT - 1) {
+          *reinterpret_cast<uint4*>(base) = make_uint4(bh[0][0], bh[1][0], bh[2][0], bh[3][0]);
+          *reinterpret_cast<uint4*>(base + 512) = make_uint4(bl[0][0], bl[1][0], bl[2][0], bl[3][0]);
         } else {
-          const float2 hi = __fmul2_rn(make_float2(v[2][q], v[3][q]), inv2);
-          b[kk][q][1] = Mma<TY>::pack(hi.x, hi.y);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            *reinterpret_cast<uint4*>(base + h * 512) = make_uint4(bh[0][h], bh[1][h], bh[2][h], bh[3][h]);
+            *reinterpret_cast<uint4*>(base + (2 + h) * 512) =
+                make_uint4(bl[0][h], bl[1][h], bl[2][h], bl[3][h]);
+          }
         }
       }
     }
+    auto load_b = [&](int kk, uint32_t (&bh)[4][2], uint32_t (&bl)[4][2]) {
+      if (kStage && c.vec) {
+        const uint8_t* base = st + (4 * kk) * 512 + lane * 16;
+        if (HALF && kk == MT - 1) {
+          const uint4 h0 = *reinterpret_cast<const uint4*>(base);
+          const uint4 l0 = *reinterpret_cast<const uint4*>(base + 512);
+          bh[0][0] = h0.x; bh[1][0] = h0.y; bh[2][0] = h0.z; bh[3][0] = h0.w;
+          bl[0][0] = l0.x; bl[1][0] = l0.y; bl[2][0] = l0.z; bl[3][0] = l0.w;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) bh[q][1] = bl[q][1] = 0u;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 hv = *reinterpret_cast<const uint4*>(base + h * 512);
+            const uint4 lv = *reinterpret_cast<const uint4*>(base + (2 + h) * 512);
+            bh[0][h] = hv.x; bh[1][h] = hv.y; bh[2][h] = hv.z; bh[3][h] = hv.w;
+            bl[0][h] = lv.x; bl[1][h] = lv.y; bl[2][h] = lv.z; bl[3][h] = lv.w;
+          }
+        }
+      } else {
+        make_b(kk, bh, bl);
+      }
+    };
 #pragma unroll
     for (int mi = 0; mi < MT; ++mi) {
       float d[4][4];
@@ -429,14 +483,19 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
       for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
+        uint32_t bh[4][2], bl[4][2];
+        load_b(kk, bh, bl);
+        // O += Pi_hi Y_hi + Pi_lo Y_hi + Pi_hi Y_lo (Pi_lo Y_lo is below fp32's resolution)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           if (HALF && kk == MT - 1) {  // rows 8..15 of this k-tile are padding
-            Mma<TY>::run8(d[q], ph[mi][kk], b[kk][q][0]);
-            Mma<TY>::run8(d[q], pl[mi][kk], b[kk][q][0]);
+            Mma<TY>::run8(d[q], ph[mi][kk], bh[q][0]);
+            Mma<TY>::run8(d[q], pl[mi][kk], bh[q][0]);
+            Mma<TY>::run8(d[q], ph[mi][kk], bl[q][0]);
           } else {
-            Mma<TY>::run(d[q], ph[mi][kk], b[kk][q][0], b[kk][q][1]);
-            Mma<TY>::run(d[q], pl[mi][kk], b[kk][q][0], b[kk][q][1]);
+            Mma<TY>::run(d[q], ph[mi][kk], bh[q][0], bh[q][1]);
+            Mma<TY>::run(d[q], pl[mi][kk], bh[q][0], bh[q][1]);
+            Mma<TY>::run(d[q], ph[mi][kk], bl[q][0], bl[q][1]);
           }
         }
       }

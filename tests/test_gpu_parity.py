@@ -95,8 +95,8 @@ def test_ns_steps_zero_and_ten():
 def test_spread_spectrum_inputs():
     """Momenta whose singular values fall log-evenly over several decades,
     unlike the concentrated spectra of Gaussian draws: two decades in bf16
-    mode (Gram-space wide and transposed members, m = 64 experts, tensor
-    path), four in fp32 mode."""
+    mode on every path (Gram-space wide and transposed members, m = 64
+    experts, tensor path), four in fp32 mode."""
     run = GpuRun(W.custom([[24, 4096], [4096, 24], [2, 64, 2048], [256, 1024], [200, 600]],
                           seed=31, spectrum_decades=2))
     check_all(run)
@@ -104,6 +104,24 @@ def test_spread_spectrum_inputs():
     run = GpuRun(W.custom([[64, 128], [24, 4096], [128, 512]], mode="fp32", seed=31,
                           spectrum_decades=4))
     check_all(run)
+    run.close()
+
+
+@pytest.mark.parametrize("ns_dtype,margin", [("fp16", 5e-3), ("bf16", 1e-2)])
+def test_four_decade_spectra_on_the_skinny_path(ns_dtype, margin):
+    """Four decades in bf16 mode on the skinny shapes of the pages' batch and
+    the mixed bag, wide and transposed.  Five steps stretch the small
+    directions by up to a^5 (about 486), so a single 16-bit rounding of X0
+    would use most of the 2e-2 budget with fp16 operands (emulated 1.6e-2)
+    and exceed it with bf16 (1.3e-1).  The Gram-space kernel reads X0 as a
+    16-bit high part plus residual in its final product O = Pi X0, which keeps
+    the error well inside: each member must land within `margin`."""
+    w = W.custom([[24, 10240], [64, 7168], [10240, 24], [7168, 64]], seed=33,
+                 spectrum_decades=4)
+    run = GpuRun(w, ns_dtype=ns_dtype)
+    assert {g["path"] for g in run.plan.groups()} == {"skinny"}
+    errs = check_all(run)
+    assert max(errs) <= margin, errs
     run.close()
 
 
