@@ -27,8 +27,9 @@ MUON_API muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int32_
                                             const void* q, void* out, float alpha, float pa,
                                             float pb, float pc, void* stream);
 
-/* The 128-row x bn-column tiles one batch item of a tcgen05 product (op as
- * in muon_testing_tc_gemm) computes, in launch order.  op 0 / 1: the Gram and
+/* The 128-row x bn-column tiles one batch item of the one-CTA form of a
+ * tcgen05 product (op as in muon_testing_tc_gemm; groups with
+ * min(rows, cols) < 256) computes, in launch order.  op 0 / 1: the Gram and
  * polynomial outputs are symmetric m x m (n is ignored), so only tiles that
  * reach the upper triangle run; each writes its elements with col >= row in
  * place and mirrors those with col > row.  op 2: every tile of the m x n
@@ -39,6 +40,18 @@ MUON_API muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int32_
  * or a NULL array with cap > 0.  Host only: no device. */
 MUON_API int32_t muon_testing_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn,
                                         int32_t* tm, int32_t* tn, int32_t cap);
+
+/* The same walk for the CTA-pair form of the products (a cluster of two CTAs
+ * per 256 x 256 tile, tcgen05.mma.cta_group::2), which groups with
+ * min(rows, cols) >= 256 use: tm[t] / tn[t] count 256-row / 256-column
+ * tiles.  Same return values and errors as muon_testing_tile_walk.  Host
+ * only. */
+MUON_API int32_t muon_testing_tile_walk_pair(int32_t op, int64_t m, int64_t n, int32_t* tm,
+                                             int32_t* tn, int32_t cap);
+
+/* 1 when a group of min dim m runs its products in the CTA-pair form, else 0.
+ * Host only. */
+MUON_API int32_t muon_testing_tc_pair_form(int64_t m);
 
 /* Number of skinny-path clusters (one per member of min dim m, 1..64) that the
  * current device can hold at once for the given operand type; -1 on error. */

@@ -57,7 +57,8 @@ class muon_group_info_t(C.Structure):
 
 # test hooks declared in include/muon_testing.h
 EXPORTED_TESTING = ["muon_testing_tc_gemm", "muon_testing_skinny_max_clusters",
-                    "muon_testing_tile_walk", "muon_testing_wait_probe"]
+                    "muon_testing_tile_walk", "muon_testing_tile_walk_pair",
+                    "muon_testing_tc_pair_form", "muon_testing_wait_probe"]
 
 # every symbol include/muon.h declares, for the export check
 EXPORTED = ["muon_default_options", "muon_plan_describe", "muon_plan_create", "muon_step",
@@ -120,6 +121,10 @@ def load() -> C.CDLL:
     L.muon_testing_skinny_max_clusters.restype = i32
     L.muon_testing_tile_walk.argtypes = [i32, i64, i64, i32, C.POINTER(i32), C.POINTER(i32), i32]
     L.muon_testing_tile_walk.restype = i32
+    L.muon_testing_tile_walk_pair.argtypes = [i32, i64, i64, C.POINTER(i32), C.POINTER(i32), i32]
+    L.muon_testing_tile_walk_pair.restype = i32
+    L.muon_testing_tc_pair_form.argtypes = [i64]
+    L.muon_testing_tc_pair_form.restype = i32
     L.muon_testing_wait_probe.argtypes = [i32, i64, vp]
     L.muon_testing_wait_probe.restype = C.c_int
     L.muon_status_string.argtypes = [C.c_int]

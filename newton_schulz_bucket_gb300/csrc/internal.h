@@ -149,11 +149,14 @@ cudaError_t launch_tc_poly(const KArgs& a, const TcMaps& t, int step, cudaStream
 // Y[1 - src] = Q Y[src]
 cudaError_t launch_tc_update(const KArgs& a, const TcMaps& t, int src, cudaStream_t s);
 // The (tile row, tile column) of each tile one batch item of a GEMM computes
-// with 128 x bn tiles, in launch order: op 0 / 1 (Gram, polynomial) the
+// with bm x bn tiles (bm 128: one CTA per tile, bn 128 or 256; bm 256: the
+// CTA-pair form, bn 256), in launch order: op 0 / 1 (Gram, polynomial) the
 // symmetric walk over the m x m output, op 2 (update) the grouped raster over
 // the m x n output.  Returns the tile count (entries past cap are not
 // written), -1 on bad arguments.
-int32_t tc_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn, int32_t* tm, int32_t* tn,
-                     int32_t cap);
+int32_t tc_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bm, int32_t bn, int32_t* tm,
+                     int32_t* tn, int32_t cap);
+// True when a group of min dim m runs its products in the CTA-pair form.
+bool tc_pair_form(int64_t m);
 
 }  // namespace muon

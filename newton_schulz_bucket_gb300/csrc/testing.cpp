@@ -59,8 +59,15 @@ extern "C" muon_status_t muon_testing_tc_gemm(int32_t op, int32_t ns_dtype, int3
 
 extern "C" int32_t muon_testing_tile_walk(int32_t op, int64_t m, int64_t n, int32_t bn,
                                           int32_t* tm, int32_t* tn, int32_t cap) {
-  return tc_tile_walk(op, m, n, bn, tm, tn, cap);
+  return tc_tile_walk(op, m, n, 128, bn, tm, tn, cap);
 }
+
+extern "C" int32_t muon_testing_tile_walk_pair(int32_t op, int64_t m, int64_t n, int32_t* tm,
+                                               int32_t* tn, int32_t cap) {
+  return tc_tile_walk(op, m, n, 256, 256, tm, tn, cap);
+}
+
+extern "C" int32_t muon_testing_tc_pair_form(int64_t m) { return tc_pair_form(m) ? 1 : 0; }
 
 extern "C" int32_t muon_testing_skinny_max_clusters(int32_t ns_dtype, int64_t m) {
   if (m < 1 || m > 64) return -1;

@@ -70,8 +70,9 @@ def _log_uniform(g: torch.Generator, lo: float, hi: float, n: int) -> List[float
 def get(name: str, ns_steps: Optional[int] = None) -> Workload:
     """The named workload.  Names: 'c1_fp32_64x128', 'c2_skinny_74x24x10240',
     'c3_moe_64x2048x7168_32x24x10240', 'c4_dense_h4096', 'c5_mixed_1000',
-    'c5_group_<rows>x<cols>' (one shape group of the mixed bag), plus small
-    parity cases built by ``custom``."""
+    'c5_group_<rows>x<cols>' (one shape group of the mixed bag),
+    'group_<rows>x<cols>_b<B>' (B matrices of one shape, for profiling one
+    group at a reduced batch), plus small parity cases built by ``custom``."""
     beta, lr = 0.95, 0.02
     if name == "c1_fp32_64x128":
         w = Workload(name, [[64, 128]], "fp32", beta, lr, 0.0, 5,
@@ -110,6 +111,20 @@ def get(name: str, ns_steps: Optional[int] = None) -> Workload:
         w = Workload(name, [shape] * len(idx), "bf16", beta, lr, 0.1, 5,
                      p_std=[full.p_std[i] for i in idx], g_std=[full.g_std[i] for i in idx], seed=5,
                      describe=f"the {shape} group of the mixed bag ({len(idx)} matrices)")
+    elif name.startswith("group_"):
+        # B matrices of one shape with the dense model's value law, for
+        # profiling one group at a reduced batch: e.g. 'group_16384x4096_b2'
+        try:
+            dims, b = name[len("group_"):].split("_b")
+            rows, cols = (int(x) for x in dims.split("x"))
+            B = int(b)
+        except ValueError:
+            raise KeyError(name)
+        if min(rows, cols) < 1 or B < 1:
+            raise KeyError(name)
+        w = Workload(name, [[rows, cols]] * B, "bf16", beta, lr, 0.1, 5,
+                     p_std=[0.02] * B, g_std=[1e-3] * B, seed=6,
+                     describe=f"{B} matrices [{rows},{cols}], G,M ~ N(0,1e-3^2), P ~ N(0,0.02^2)")
     else:
         raise KeyError(name)
     if ns_steps is not None:

@@ -9,6 +9,9 @@ The count for m = 4096 with bn = 256 is 272 of the 512 tiles.
 Update Q Y: the grouped raster must visit every tile of the m x n output once,
 and the tiles of one group (8 tile rows sweeping the tile columns together)
 must come in one run.
+
+Groups with m >= 256 run the CTA-pair form (256 x 256 tiles, one cluster of
+two CTAs per tile); its walks must satisfy the same properties.
 """
 import ctypes as C
 
@@ -27,26 +30,37 @@ def lib():
 
 
 def walk(lib, op, m, n, bn):
-    count = lib.muon_testing_tile_walk(op, m, n, bn, None, None, 0)
+    """Tiles of the one-CTA form (bn = 128 or 256) or, for bn = "pair", of the
+    CTA-pair form (256 x 256)."""
+    if bn == "pair":
+        f = lambda tm, tn, cap: lib.muon_testing_tile_walk_pair(op, m, n, tm, tn, cap)
+    else:
+        f = lambda tm, tn, cap: lib.muon_testing_tile_walk(op, m, n, bn, tm, tn, cap)
+    count = f(None, None, 0)
     assert count > 0
     tm = (C.c_int32 * count)()
     tn = (C.c_int32 * count)()
-    assert lib.muon_testing_tile_walk(op, m, n, bn, tm, tn, count) == count
+    assert f(tm, tn, count) == count
     return list(zip(tm, tn))
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+def tile_dims(bn):
+    return (256, 256) if bn == "pair" else (BM, bn)
+
+
+@pytest.mark.parametrize("bn", [128, 256, "pair"])
 @pytest.mark.parametrize("m", [8, 100, 128, 129, 256, 300, 512, 1000, 1024, 1536, 4096])
 def test_symmetric_outputs_written_once(lib, m, bn):
     tiles = walk(lib, GRAM, m, 0, bn)
     assert tiles == walk(lib, POLY, m, 0, bn)
     assert len(set(tiles)) == len(tiles)
     assert [t[0] for t in tiles] == sorted(t[0] for t in tiles)  # tile rows in order
+    bm, bn = tile_dims(bn)
     count = np.zeros((m, m), np.int8)
     for tm, tn in tiles:
-        r0, c0 = tm * BM, tn * bn
+        r0, c0 = tm * bm, tn * bn
         assert 0 <= r0 < m and 0 <= c0 < m, (tm, tn)
-        rows = np.arange(r0, min(r0 + BM, m))[:, None]
+        rows = np.arange(r0, min(r0 + bm, m))[:, None]
         cols = np.arange(c0, min(c0 + bn, m))[None, :]
         upper = cols >= rows
         assert upper.any(), f"tile ({tm}, {tn}) lies below the diagonal"
@@ -57,12 +71,13 @@ def test_symmetric_outputs_written_once(lib, m, bn):
     assert count.min() == 1 and count.max() == 1
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 256, "pair"])
 @pytest.mark.parametrize("m,n", [(8, 8), (128, 1000), (300, 400), (1024, 1024), (1100, 7168),
                                  (4096, 16384), (2048, 7168)])
 def test_update_raster_visits_every_tile_once(lib, m, n, bn):
     tiles = walk(lib, UPDATE, m, n, bn)
-    tiles_m, tiles_n = -(-m // BM), -(-n // bn)
+    bm, bn = tile_dims(bn)
+    tiles_m, tiles_n = -(-m // bm), -(-n // bn)
     assert sorted(tiles) == [(a, b) for a in range(tiles_m) for b in range(tiles_n)]
     groups = [tm // 8 for tm, _ in tiles]
     assert groups == sorted(groups)  # one run per group of 8 tile rows
@@ -81,3 +96,8 @@ def test_counts_and_arguments(lib):
                               (UPDATE, 512, 0, 128, 0), (3, 512, 512, 128, 0)]:
         assert lib.muon_testing_tile_walk(op, m, n, bn, None, None, cap) == -1
     assert lib.muon_testing_tile_walk(GRAM, 512, 0, 128, None, None, 4) == -1
+    # the CTA-pair form: 256 x 256 tiles, for m >= 256
+    assert lib.muon_testing_tile_walk_pair(GRAM, 4096, 0, None, None, 0) == 16 * 17 // 2
+    assert lib.muon_testing_tile_walk_pair(UPDATE, 4096, 16384, None, None, 0) == 16 * 64
+    assert lib.muon_testing_tile_walk_pair(UPDATE, 512, 0, None, None, 0) == -1
+    assert [lib.muon_testing_tc_pair_form(m) for m in (128, 255, 256, 4096)] == [0, 0, 1, 1]
