@@ -106,7 +106,12 @@ def ncu_traffic(kernel_file, workload):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(workload)
-    if not d or d.get("source_sha256_16") != kernel_source_hash(kernel_file):
+    if not d:
+        return None
+    files = d.get("source_files") or [d.get("source_file", kernel_file)]
+    want = d.get("source_sha256_16")
+    want = want if isinstance(want, list) else [want]
+    if [kernel_source_hash(f) for f in files] != want:
         return None
     return d
 

@@ -185,6 +185,46 @@ __global__ void __launch_bounds__(kThreads) k_normalize_cast(KArgs a, TY* __rest
     }
     return;
   }
+  // Transposed member, 8-element alignment: the 64 x 64 parameter tile comes
+  // in as 16-byte row vectors (4 floats of M', 8 bf16 of G), is normalised in
+  // shared memory, and leaves as 16-byte vectors along the rows of Y (the
+  // parameter's columns).  Y's row pitch is a multiple of 8 >= n, so a last
+  // partial vector only touches Y's padding, which nothing reads.
+  if (T && cols % 8 == 0 && a.n_pitch % 8 == 0 && aligned16(Mp) && aligned16(Yb) &&
+      (!nest || (!a.mode_f32 && aligned16(Gp)))) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // 64 rows x 16 vectors of 4 floats
+      const int v = threadIdx.x + k * kThreads, rr = v >> 4, cc = (v & 15) * 4;
+      const int r = r0 + rr, c = c0 + cc;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (r < rows && c < cols) {
+        const int64_t o = (int64_t)r * cols + c;
+        const float4 t = *reinterpret_cast<const float4*>(Mp + o);
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+        if (nest) {
+          const uint2 graw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(Gp) + o);
+          const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
+          const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
+          x[0] = fmaf(beta, x[0], g01.x); x[1] = fmaf(beta, x[1], g01.y);
+          x[2] = fmaf(beta, x[2], g23.x); x[3] = fmaf(beta, x[3], g23.y);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tile[rr][cc + e] = x[e] * inv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // 64 rows of Y x 8 vectors of 8
+      const int v = threadIdx.x + k * kThreads, cc = v >> 3, rr = (v & 7) * 8;
+      const int c = c0 + cc, r = r0 + rr;
+      if (c >= cols || r >= rows) continue;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = tile[rr + e][cc];
+      store8(Yb + (int64_t)c * a.n_pitch + r, y);
+    }
+    return;
+  }
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
   for (int rr = ty; rr < 64; rr += 4) {
     const int r = r0 + rr, c = c0 + tx;
@@ -244,6 +284,44 @@ __global__ void __launch_bounds__(kThreads) k_write(KArgs a, const TY* __restric
       const int64_t idx = (int64_t)r * cols + c0 + cc;
       float y[8], pv[8], w[8];
       load8(Yb + (int64_t)r * a.n_pitch + c0 + cc, y);
+      load8(P + idx, pv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = fmaf(-coef, y[e], pv[e] * decay);
+      store8(P + idx, w);
+      if (dbg) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = y[e] * inv_alpha;
+        store8(dbg + idx, w);
+      }
+    }
+    return;
+  }
+  // Transposed member, 8-element alignment: the Y tile Y[c0 .. c0 + 64)
+  // [r0 .. r0 + 64) comes in as 16-byte vectors along Y's rows (Y's row pitch
+  // is a multiple of 8 >= n, so a last partial vector reads only padding),
+  // and the parameter tile is read, updated and written as 16-byte vectors
+  // along its rows (the same arithmetic per element as below).
+  if (T && cols % 8 == 0 && a.n_pitch % 8 == 0 && aligned16(P) && aligned16(Yb) &&
+      (!dbg || aligned16(dbg))) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // 64 rows of Y x 8 vectors of 8
+      const int v = threadIdx.x + k * kThreads, cc = v >> 3, rr = (v & 7) * 8;
+      const int c = c0 + cc, r = r0 + rr;
+      float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (c < cols && r < rows) load8(Yb + (int64_t)c * a.n_pitch + r, y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tile[rr + e][cc] = y[e];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // 64 parameter rows x 8 vectors of 8
+      const int v = threadIdx.x + k * kThreads, rr = v >> 3, cc = (v & 7) * 8;
+      const int r = r0 + rr, c = c0 + cc;
+      if (r >= rows || c >= cols) continue;
+      const int64_t idx = (int64_t)r * cols + c;
+      float y[8], pv[8], w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = tile[rr][cc + e];
       load8(P + idx, pv);
 #pragma unroll
       for (int e = 0; e < 8; ++e) w[e] = fmaf(-coef, y[e], pv[e] * decay);

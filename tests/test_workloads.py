@@ -114,3 +114,14 @@ def test_spread_spectrum_draws():
     assert all(torch.equal(a, b) for a, b in zip(M + G + P, again[2] + again[1] + again[0]))
     _, _, Mz = W.make_tensors(W.custom([[8, 64]], spectrum_decades=2, m_zero=True))
     assert not Mz[0].any()
+
+
+def test_reduced_batch_group_workloads():
+    """'group_<rows>x<cols>_b<B>': B matrices of one shape with the dense
+    model's value law, for profiling one group at a reduced batch."""
+    w = W.get("group_16384x4096_b2")
+    assert w.shapes == [[16384, 4096]] * 2 and w.mode == "bf16" and w.ns_steps == 5
+    assert w.g_std == [1e-3, 1e-3] and w.p_std == [0.02, 0.02]
+    for bad in ("group_16384x4096", "group_0x4_b2", "group_4x4_b0", "group_axb_b1"):
+        with pytest.raises(KeyError):
+            W.get(bad)
