@@ -49,6 +49,14 @@
 namespace muon {
 namespace gs {
 
+// Kernel variants, each instantiated in its own translation unit: plain
+// momentum with the vector path for members with rows <= cols (transposed
+// members then take the element-wise path); Nesterov (every member with
+// rows > cols on the element-wise path); plain momentum with the vector path
+// for transposed members too, for groups that hold any (its extra branches
+// cost the plain variant registers and time).
+constexpr int kVarPlain = 0, kVarNesterov = 1, kVarTransposed = 2;
+
 
 template <int MT, int NT, bool HALF>
 struct GsLayout {
@@ -111,6 +119,8 @@ struct Wide {
 struct GsCtx {
   int lane, warp, g, t4, m, n, c0, NB;  // NB: 16-column blocks of this CTA (even)
   bool vec;            // rows <= cols, cols % 8 == 0, 32 cols < 2^31, M', G and P 16-byte aligned
+  bool tvec;           // rows > cols (the parameter is [n, m]), m % 8 == 0, n m < 2^31, 16-byte
+                       // aligned, no Nesterov: a superblock is one contiguous block of 32 rows
   float* Mp;
   const __nv_bfloat16* G;
   __nv_bfloat16* P;
@@ -141,9 +151,10 @@ __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uin
 // A-fragment slot k = t4 + 4 e of k8 step st.  All three streams keep the
 // default L2 policy: measured, evict-first reads or evict-last stores here
 // only slowed the pass.
-template <int MT, int NT, bool HALF, bool NEST>
+template <int MT, int NT, bool HALF, int VAR>
 __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
                                                  float (&gacc)[GsLayout<MT, NT, HALF>::GT::N][4], float& ss) {
+  constexpr bool NEST = VAR == kVarNesterov, TP = VAR == kVarTransposed;
   using L = GsLayout<MT, NT, HALF>;
   using GT = typename L::GT;
   constexpr int NW = L::NW, S = L::S1, LB = L::LB1, R = L::R;
@@ -166,7 +177,34 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   // warp barrier.
   constexpr int RT = 8 * R;  // rows of the tile (rows >= m are zero-filled)
   auto mchunk = [](int row, int q) { return row * 128 + ((q ^ (row & 1)) << 4); };
+  // A transposed member's superblock is parameter rows J .. J + 31, one
+  // contiguous block: it is staged as such, M at the slot's start (row pitch
+  // m floats) and G after 32 m floats (row pitch m bf16), 16-byte chunks
+  // spread over the lanes; rows past n are zero-filled.
+  const int mq = c.m / 4;  // 16-byte chunks per row of M (transposed member)
+  auto issue_t = [&](int r, uint32_t dst) {
+    const int sb = r * NW + c.warp;
+    if (r < rounds && sb < nsb) {
+      const int J = c.c0 + sb * 32, nrows = min(32, c.n - J);
+      const float* mb = c.Mp + (int64_t)J * c.m;
+      const __nv_bfloat16* gb = c.G + (int64_t)J * c.m;
+      for (int k = lane; k < 8 * c.m; k += 32) {
+        const bool ok = k / mq < nrows;
+        cp_async16_hint(dst + k * 16, ok ? (const void*)(mb + 4 * k) : (const void*)c.Mp, ok ? 16 : 0, pol);
+      }
+      for (int k = lane; k < 4 * c.m; k += 32) {
+        const bool ok = 2 * k / mq < nrows;
+        cp_async16_hint(dst + 128 * c.m + k * 16, ok ? (const void*)(gb + 8 * k) : (const void*)c.G,
+                        ok ? 16 : 0, pol);
+      }
+    }
+    cp_async_commit();
+  };
   auto issue = [&](int r, uint32_t dst) {
+    if (TP && c.tvec) {
+      issue_t(r, dst);
+      return;
+    }
     const int sb = r * NW + c.warp;
     if (c.vec && r < rounds && sb < nsb) {
       const int J = c.c0 + sb * 32;
@@ -200,12 +238,28 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
     const int j0 = J + 8 * c.t4;
     // tv[mi][st][h][e]: row 16 mi + g + 8 h, tf32 slot k = t4 + 4 e of k8 step st
     uint32_t tv[MT][4][2][2];
-    if (c.vec) __syncwarp();  // every lane's copies of this round have landed
+    if (c.vec || (TP && c.tvec)) __syncwarp();  // every lane's copies of this round have landed
+    float* tm = reinterpret_cast<float*>(st);                                 // transposed: M, M'
+    const __nv_bfloat16* tg = reinterpret_cast<const __nv_bfloat16*>(st + 128 * c.m);  // and G
 #pragma unroll
     for (int s = 0; s < R; ++s) {
       const int i = row_of(s);
       float v[8];
-      if (c.vec) {
+      if (TP && c.tvec) {
+        // this lane's eight columns of the superblock are parameter rows
+        // t4 + 4 q (q = 0..7): for m = 8 mod 16 the 32 lanes then hit 32
+        // banks; any fixed assignment serves, since the Gram sums over all
+        // columns and both of its operands come from these registers
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int o = (c.t4 + 4 * q) * c.m + i;
+          v[q] = 0.f;
+          if (i < c.m && J + c.t4 + 4 * q < c.n) {
+            v[q] = fmaf(c.beta, tm[o], __bfloat162float(tg[o]));
+            tm[o] = v[q];  // M' replaces M in the block
+          }
+        }
+      } else if (c.vec) {
         float4* m0p = reinterpret_cast<float4*>(st + mchunk(i, 2 * c.t4));
         float4* m1p = reinterpret_cast<float4*>(st + mchunk(i, 2 * c.t4 + 1));
         const float4 m0 = *m0p, m1 = *m1p;
@@ -245,6 +299,15 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
         tv[s >> 1][st4][s & 1][0] = to_tf32(v[2 * st4]);
         tv[s >> 1][st4][s & 1][1] = to_tf32(v[2 * st4 + 1]);
       }
+    }
+    if (TP && c.tvec) {
+      // M' out as the contiguous block
+      __syncwarp();
+      const int nrows = min(32, c.n - J);
+      float* mb = c.Mp + (int64_t)J * c.m;
+      for (int k = lane; k < 8 * c.m; k += 32)
+        if (k / mq < nrows) st_hint(mb + 4 * k, *reinterpret_cast<const uint4*>(st + k * 16), pol);
+      __syncwarp();  // the block is read out before its slot is refilled
     }
     if (c.vec) {
       // M' out by rows, whole lines (each lane stores the chunks it will refill)
@@ -554,6 +617,143 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
   cp_async_wait<0>();
 }
 
+// Output pass of a transposed member (parameter [n, m], m % 8 == 0): each
+// superblock is parameter rows J .. J + 31, staged as one contiguous block of
+// M' (row pitch m floats) and one of P (row pitch m bf16) in the warp's ring
+// slot.  In the parameter's layout the update is O_par = Y_par Pi^T with
+// Y_par = alpha M'_par / (||M'|| + eps), so the data is the MMA's A operand
+// (rows: parameter rows, K: parameter columns) and Pi^T the constant B
+// operand.  Row tile ct (0, 1) covers rows J + 16 ct .. + 15; the accumulator
+// of n-tile nt holds rows J + 16 ct + g (+ 8), columns 8 nt + 2 t4 (+ 1).
+// Y is split into an operand-type high part and residual as on the vector
+// path; P' is formed in the staged P block and written back as the block.
+template <typename TY, int MT, int NT, bool HALF>
+__device__ __forceinline__ void gs_out_pass_t(const GsCtx& c, uint8_t* ring,
+                                              const uint32_t (&bh)[MT][GsLayout<MT, NT, HALF>::NJ][2],
+                                              const uint32_t (&bl)[MT][GsLayout<MT, NT, HALF>::NJ][2],
+                                              const float* rsc) {
+  using L = GsLayout<MT, NT, HALF>;
+  constexpr int NW = L::NW, S = L::SO, LB = L::LBO, NJ = L::NJ;
+  constexpr uint32_t kSlot = NW * 32 * LB;
+  static_assert(192 * 16 * MT - (HALF ? 192 * 8 : 0) <= 32 * LB, "transposed block exceeds the slot");
+  const int lane = c.lane, m = c.m, mq = m / 4;
+  uint8_t* ring_warp = ring + c.warp * 32 * LB;
+  const uint32_t ring0 = smem_u32(ring_warp);
+  const int nsb = c.NB / 2, rounds = (nsb + NW - 1) / NW;
+  const uint64_t last_use = l2_evict_first();
+  const float2 decay2 = make_float2(c.decay, c.decay);
+
+  auto issue = [&](int r) {
+    const int sb = r * NW + c.warp;
+    if (r < rounds && sb < nsb) {
+      const uint32_t dst = ring0 + (r % S) * kSlot;
+      const int J = c.c0 + sb * 32, nrows = min(32, c.n - J);
+      const float* mb = c.Mp + (int64_t)J * m;
+      const __nv_bfloat16* pb = c.P + (int64_t)J * m;
+      for (int k = lane; k < 8 * m; k += 32) {
+        const bool ok = k / mq < nrows;
+        cp_async16_hint(dst + k * 16, ok ? (const void*)(mb + 4 * k) : (const void*)c.Mp, ok ? 16 : 0,
+                        last_use);
+      }
+      for (int k = lane; k < 4 * m; k += 32) {
+        const bool ok = 2 * k / mq < nrows;
+        cp_async16_hint(dst + 128 * m + k * 16, ok ? (const void*)(pb + 8 * k) : (const void*)c.P,
+                        ok ? 16 : 0, last_use);
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int r = 0; r < S; ++r) issue(r);
+
+  // with four 16-row tiles, one row tile at a time keeps the accumulators
+  // within the register budget
+  constexpr int NCT = MT >= 3 ? 1 : 2;
+  for (int r = 0; r < rounds; ++r) {
+    cp_async_wait<S - 1>();
+    __syncwarp();  // every lane's copies of this round have landed
+    uint8_t* st = ring_warp + (r % S) * kSlot;
+    const int sb = r * NW + c.warp;
+    if (sb < nsb) {
+      const int J = c.c0 + sb * 32, nrows = min(32, c.n - J);
+      const float* ym = reinterpret_cast<const float*>(st);
+      __nv_bfloat16* pm = reinterpret_cast<__nv_bfloat16*>(st + 128 * m);
+#pragma unroll
+      for (int c0 = 0; c0 < 2; c0 += NCT) {
+        float d[NCT][NJ][4];
+#pragma unroll
+        for (int ct = 0; ct < NCT; ++ct)
+#pragma unroll
+          for (int nt = 0; nt < NJ; ++nt) d[ct][nt][0] = d[ct][nt][1] = d[ct][nt][2] = d[ct][nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < MT; ++kk) {
+          const bool half = HALF && kk == MT - 1;
+#pragma unroll
+          for (int ct = 0; ct < NCT; ++ct) {
+            // a[f]: rows (16 ct + g, + 8) x columns (16 kk + 2 t4, + 8), pairs of columns
+            uint32_t ah[4], al[4];
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+              const int row = 16 * (c0 + ct) + c.g + ((f & 1) ? 8 : 0);
+              const int col = 16 * kk + 2 * c.t4 + ((f & 2) ? 8 : 0);
+              float2 y = make_float2(0.f, 0.f);
+              if (!(half && (f & 2)) && col < m)
+                y = *reinterpret_cast<const float2*>(ym + row * m + col);
+              y = __fmul2_rn(y, make_float2(c.inv, c.inv));
+              ah[f] = Mma<TY>::pack(y.x, y.y);
+              const float2 yh = Mma<TY>::unpack(ah[f]);
+              al[f] = Mma<TY>::pack(y.x - yh.x, y.y - yh.y);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NJ; ++nt) {
+              if (half) {  // columns 8..15 of this k-tile are padding
+                Mma<TY>::run8(d[ct][nt], ah, bh[kk][nt][0]);
+                Mma<TY>::run8(d[ct][nt], ah, bl[kk][nt][0]);
+                Mma<TY>::run8(d[ct][nt], al, bh[kk][nt][0]);
+              } else {
+                Mma<TY>::run(d[ct][nt], ah, bh[kk][nt][0], bh[kk][nt][1]);
+                Mma<TY>::run(d[ct][nt], ah, bl[kk][nt][0], bl[kk][nt][1]);
+                Mma<TY>::run(d[ct][nt], al, bh[kk][nt][0], bh[kk][nt][1]);
+              }
+            }
+          }
+        }
+        // P' = P (1 - lr wd) - lr s O in the staged block; O's column i
+        // carries Pi's row scale rsc[i]
+#pragma unroll
+        for (int ct = 0; ct < NCT; ++ct)
+#pragma unroll
+          for (int nt = 0; nt < NJ; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = 16 * (c0 + ct) + c.g + 8 * h, col = 8 * nt + 2 * c.t4;
+              if (row >= nrows || col >= m) continue;
+              const float s0 = rsc[col], s1 = rsc[col + 1];
+              const float o0 = d[ct][nt][2 * h], o1 = d[ct][nt][2 * h + 1];
+              __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(pm + row * m + col);
+              const float2 pv = __bfloat1622float2(*pp);
+              const float2 w = __ffma2_rn(make_float2(-c.coef * s0, -c.coef * s1), make_float2(o0, o1),
+                                          __fmul2_rn(pv, decay2));
+              *pp = __floats2bfloat162_rn(w.x, w.y);
+              if (c.dbg) {
+                float* dp = c.dbg + (int64_t)(J + row) * m + col;
+                dp[0] = o0 * c.inv_alpha * s0;
+                dp[1] = o1 * c.inv_alpha * s1;
+              }
+            }
+      }
+      __syncwarp();  // the block is complete: P' out as the contiguous block
+      __nv_bfloat16* pb = c.P + (int64_t)J * m;
+      for (int k = lane; k < 4 * m; k += 32)
+        if (2 * k / mq < nrows)
+          *reinterpret_cast<uint4*>(pb + 8 * k) = *reinterpret_cast<const uint4*>(st + 128 * m + k * 16);
+    }
+    __syncwarp();  // the slot is read out before it is refilled
+    issue(r + S);
+  }
+  cp_async_wait<0>();
+}
+
 // An m x m fp32 matrix kept as two tf32 parts, x = hi + lo (both exact
 // tf32 values, pitch LD), so that the tensor-core products below read their
 // operands already split.
@@ -691,8 +891,9 @@ struct MmMats {
   }
 };
 
-template <typename TY, int MT, int NT, bool HALF, bool NEST>
+template <typename TY, int MT, int NT, bool HALF, int VAR>
 __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
+  constexpr bool NEST = VAR == kVarNesterov, TP = VAR == kVarTransposed;
   using L = GsLayout<MT, NT, HALF>;
   using GT = typename L::GT;
   constexpr int MP = L::MP, LD = L::LD, NW = L::NW;
@@ -721,6 +922,8 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   c.wd = Wide{c.cols, (int)T};
   c.vec = !T && (c.cols % 8 == 0) && 32ll * c.cols < (1ll << 31) && aligned16(c.Mp) &&
           aligned16(c.G) && aligned16(c.P);
+  c.tvec = TP && T && m % 8 == 0 && (int64_t)a.n * m < (1ll << 31) && aligned16(c.Mp) &&
+           aligned16(c.G) && aligned16(c.P);
   c.dbg = a.dbg ? a.dbg + (int64_t)b * m * a.n : nullptr;
   const int ns = a.sc->ns_steps;
   c.beta = a.sc->beta;
@@ -754,7 +957,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 #pragma unroll
   for (int q = 0; q < GT::N; ++q) gacc[q][0] = gacc[q][1] = gacc[q][2] = gacc[q][3] = 0.f;
   float ss = 0.f;
-  gs_momentum_pass<MT, NT, HALF, NEST>(c, smem, gacc, ss);
+  gs_momentum_pass<MT, NT, HALF, VAR>(c, smem, gacc, ss);
   // Hint: move this CTA's slice of P into L2 while the m x m work runs.
   if (c.vec && warp == NW - 1 && c.c0 < c.n) {
     const int ncol = min(W, c.n - c.c0);
@@ -1000,6 +1203,25 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
     }
   }
   __syncthreads();
+  if (TP && c.tvec) {
+    // Pi^T as the B operand of the transposed member's product:
+    // tb_h[kk][nt] = Pi[8 nt + g][16 kk + 2 t4 (+1)] and [16 kk + 8 + 2 t4 (+1)]
+    constexpr int NJ = L::NJ;
+    uint32_t tb_h[MT][NJ][2], tb_l[MT][NJ][2];
+    const uint32_t hb = smem_u32(Ph), lb = smem_u32(Pl);
+#pragma unroll
+    for (int kk = 0; kk < MT; ++kk)
+#pragma unroll
+      for (int nt = 0; nt < NJ; ++nt) {
+        const uint32_t o = 2u * ((nt * 8 + (lane & 7)) * (MP + 8) + kk * 16 + ((lane >> 3) & 1) * 8);
+        ldsm_x2(hb + o, tb_h[kk][nt]);
+        ldsm_x2(lb + o, tb_l[kk][nt]);
+      }
+    __syncthreads();  // the ring's bytes are reused by the output pass
+    gs_out_pass_t<TY, MT, NT, HALF>(c, smem, tb_h, tb_l, rsc);
+    cluster_wait();  // the peer may still read this CTA's partials
+    return;
+  }
   uint32_t ph[MT][MT][4], pl[MT][MT][4];
   {
     const uint32_t hb = smem_u32(Ph), lb = smem_u32(Pl);
@@ -1027,10 +1249,10 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 template <int MT>
 constexpr int gs_threads() { return MT <= 2 ? 512 : 256; }
 
-template <typename TY, int MT, bool HALF, bool NEST>
+template <typename TY, int MT, bool HALF, int VAR>
 cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
   constexpr int NT = gs_threads<MT>();
-  auto fn = k_skinny_gs<TY, MT, NT, HALF, NEST>;
+  auto fn = k_skinny_gs<TY, MT, NT, HALF, VAR>;
   constexpr int smem = GsLayout<MT, NT, HALF>::kTotal;
   if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaLaunchConfig_t lc{};
@@ -1048,10 +1270,10 @@ cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, b
   return cudaLaunchKernelEx(&lc, fn, a, (int)cfg.width, (int)(cfg.width / 16));
 }
 
-template <typename TY, int MT, bool HALF, bool NEST>
+template <typename TY, int MT, bool HALF, int VAR>
 int gs_clusters_of(int cl) {
   constexpr int NT = gs_threads<MT>();
-  auto fn = k_skinny_gs<TY, MT, NT, HALF, NEST>;
+  auto fn = k_skinny_gs<TY, MT, NT, HALF, VAR>;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(cl * 1024);
   lc.blockDim = dim3(NT);
@@ -1069,44 +1291,44 @@ int gs_clusters_of(int cl) {
 
 // HALF (a last 16-row tile of at most 8 rows, stored as half a tile) is
 // instantiated up to m = 32; beyond, such a tile is padded to 16 rows.
-template <typename TY, bool NEST>
+template <typename TY, int VAR>
 cudaError_t gs_launch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prep) {
   const bool half = a.m - 16 * (cfg.mtiles - 1) <= 8;
   switch (cfg.mtiles) {
     case 1:
-      return half ? launch_gs_t<TY, 1, true, NEST>(a, cfg, st, prep) : launch_gs_t<TY, 1, false, NEST>(a, cfg, st, prep);
+      return half ? launch_gs_t<TY, 1, true, VAR>(a, cfg, st, prep) : launch_gs_t<TY, 1, false, VAR>(a, cfg, st, prep);
     case 2:
-      return half ? launch_gs_t<TY, 2, true, NEST>(a, cfg, st, prep) : launch_gs_t<TY, 2, false, NEST>(a, cfg, st, prep);
-    case 3: return launch_gs_t<TY, 3, false, NEST>(a, cfg, st, prep);
-    default: return launch_gs_t<TY, 4, false, NEST>(a, cfg, st, prep);
+      return half ? launch_gs_t<TY, 2, true, VAR>(a, cfg, st, prep) : launch_gs_t<TY, 2, false, VAR>(a, cfg, st, prep);
+    case 3: return launch_gs_t<TY, 3, false, VAR>(a, cfg, st, prep);
+    default: return launch_gs_t<TY, 4, false, VAR>(a, cfg, st, prep);
   }
 }
 
-template <typename TY, bool NEST>
+template <typename TY, int VAR>
 int gs_clusters_ty(int m, int cl) {
   const int mt = (m + 15) / 16;
   const bool half = m - 16 * (mt - 1) <= 8;
   switch (mt) {
-    case 1: return half ? gs_clusters_of<TY, 1, true, NEST>(cl) : gs_clusters_of<TY, 1, false, NEST>(cl);
-    case 2: return half ? gs_clusters_of<TY, 2, true, NEST>(cl) : gs_clusters_of<TY, 2, false, NEST>(cl);
-    case 3: return gs_clusters_of<TY, 3, false, NEST>(cl);
-    default: return gs_clusters_of<TY, 4, false, NEST>(cl);
+    case 1: return half ? gs_clusters_of<TY, 1, true, VAR>(cl) : gs_clusters_of<TY, 1, false, VAR>(cl);
+    case 2: return half ? gs_clusters_of<TY, 2, true, VAR>(cl) : gs_clusters_of<TY, 2, false, VAR>(cl);
+    case 3: return gs_clusters_of<TY, 3, false, VAR>(cl);
+    default: return gs_clusters_of<TY, 4, false, VAR>(cl);
   }
 }
 
-// The launcher and occupancy query of one Nesterov setting (each setting is
+// The launcher and occupancy query of one kernel variant (each variant is
 // instantiated in its own translation unit).
-template <bool NEST>
+template <int VAR>
 cudaError_t gs_dispatch_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare) {
   if (a.mode_f32 || cfg.mtiles < 1 || cfg.mtiles > 4) return cudaErrorInvalidValue;
-  return a.ns_type == NS_F16 ? gs_launch_ty<__half, NEST>(a, cfg, s, prepare)
-                             : gs_launch_ty<__nv_bfloat16, NEST>(a, cfg, s, prepare);
+  return a.ns_type == NS_F16 ? gs_launch_ty<__half, VAR>(a, cfg, s, prepare)
+                             : gs_launch_ty<__nv_bfloat16, VAR>(a, cfg, s, prepare);
 }
 
-template <bool NEST>
+template <int VAR>
 int gs_clusters_t(int ns_type, int m, int cl) {
   if (m < 1 || m > 64) return -1;
-  return ns_type == NS_F16 ? gs_clusters_ty<__half, NEST>(m, cl) : gs_clusters_ty<__nv_bfloat16, NEST>(m, cl);
+  return ns_type == NS_F16 ? gs_clusters_ty<__half, VAR>(m, cl) : gs_clusters_ty<__nv_bfloat16, VAR>(m, cl);
 }
 
 }  // namespace gs

@@ -43,6 +43,7 @@ def _bands_intact(back, n, fill):
 CASES = [
     ([[24, 10240], [3, 24, 1000], [10240, 24], [17, 333], [24, 1004]], {}, 5),      # skinny, Gram space
     ([[64, 1000], [1000, 64], [2, 40, 96]], {}, 5),                                  # skinny, m > 32
+    ([[1000, 24], [3000, 40], [2, 520, 16]], {}, 5),                                # transposed skinny, ragged blocks
     ([[24, 2048], [2048, 24]], {}, 70),                                              # skinny, direct
     ([[256, 520], [520, 256], [2, 130, 384]], {}, 5),                                # tensor cores
     ([[96, 200], [2, 70, 33]], {"path": "simt"}, 5),                                 # SIMT
@@ -51,7 +52,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("shapes,opts,k", CASES,
-                         ids=["gram_space", "gram_space_m64", "direct", "tensor", "simt", "merged_shards"])
+                         ids=["gram_space", "gram_space_m64", "transposed_ragged", "direct", "tensor", "simt", "merged_shards"])
 def test_guard_bands_intact(shapes, opts, k):
     w = W.custom(shapes, seed=51, ns_steps=k)
     P, G, M = W.make_tensors(w, "cuda")

@@ -45,6 +45,8 @@ SKINNY_SHAPES = [
     [[56, 3000]],                # m = 56: last m16 tile padded, ragged superblock
     [[2048, 36], [7168, 64]],    # transposed, three and four m16 tiles
     [[4, 64, 1504]],             # 3-D, m = 64
+    [[1000, 24], [3000, 40]],    # transposed, ragged last block of 32 rows
+    [[2, 520, 16], [4104, 64]],  # transposed 3-D, m = 16; m = 64 with a ragged block
 ]
 
 

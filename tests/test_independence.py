@@ -76,9 +76,14 @@ def _enclosing(node, par, kind):
 
 
 def test_bench_reaches_the_oracle_only_from_its_cpu_legs():
+    """bench.py imports the oracle inside `time_members` only; that function
+    is called from the oracle estimate and the reference arm, and the estimate
+    from the reference arm and from main's CPU-baseline block (which the flag
+    turns off)."""
     tree = ast.parse(open(os.path.join(ROOT, "bench.py"), encoding="utf-8").read())
     par = _parents(tree)
-    importers, callers = set(), []
+    importers = set()
+    calls = {"time_members": [], "oracle_estimate": []}
     for node in ast.walk(tree):
         mod = None
         if isinstance(node, ast.ImportFrom):
@@ -89,19 +94,16 @@ def test_bench_reaches_the_oracle_only_from_its_cpu_legs():
             fn = _enclosing(node, par, ast.FunctionDef)
             assert fn is not None, "bench.py imports the oracle at module level"
             importers.add(fn.name)
-        if isinstance(node, ast.Call) and isinstance(node.func, ast.Name) \
-                and node.func.id == "oracle_time":
-            callers.append(node)
-    assert importers == {"oracle_time"}
-    names = set()
-    for call in callers:
-        fn = _enclosing(call, par, ast.FunctionDef)
-        names.add(fn.name)
-        if fn.name == "main":
-            # inside main only the CPU-baseline block, which the flag turns off
+        if isinstance(node, ast.Call) and isinstance(node.func, ast.Name) and node.func.id in calls:
+            calls[node.func.id].append(node)
+    assert importers == {"time_members"}
+    callers = {k: {_enclosing(c, par, ast.FunctionDef).name for c in v} for k, v in calls.items()}
+    assert callers["time_members"] == {"oracle_estimate", "run_reference"}
+    assert callers["oracle_estimate"] == {"run_reference", "main"}
+    for call in calls["oracle_estimate"]:
+        if _enclosing(call, par, ast.FunctionDef).name == "main":
             guard = _enclosing(call, par, ast.If)
             assert guard is not None and "no_cpu_baseline" in ast.unparse(guard.test)
-    assert names == {"run_reference", "main"}
 
 
 def test_binding_raises_without_its_library(monkeypatch):
