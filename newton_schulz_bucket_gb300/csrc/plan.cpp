@@ -647,7 +647,8 @@ muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
     PLAN_TRY(cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking));
     PLAN_TRY(cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking));
     PLAN_TRY(cudaEventCreateWithFlags(&p->up_ev, cudaEventDisableTiming));
-    for (int i = 0; i < kHostChunks; ++i) {
+    const int nev = std::max<int>(kHostChunks, (int)p->d.groups.size());  // chunks or groups
+    for (int i = 0; i < nev; ++i) {
       cudaEvent_t e0, e1, e2;
       PLAN_TRY(cudaEventCreateWithFlags(&e0, cudaEventDisableTiming));
       p->in_ev.push_back(e0);
@@ -847,6 +848,66 @@ muon_status_t host_step_pipelined(muon_plan_s* p, void* const* hp, const void* c
   return MUON_OK;
 }
 
+// muon_step_host for a plan with more than one group, not all skinny: the
+// same three-stream pipeline with the shape groups as its units.  Every
+// group's inputs are queued for copy-in at once; its kernels run on the
+// caller's stream once they have landed (groups one after another), and its
+// parameters and momenta are copied back as soon as its kernels are done, so
+// the copies of other groups hide behind each group's kernels.  Every member
+// gets the same kernels as in a whole-plan step, so its results are the same
+// bits.
+muon_status_t host_step_by_group(muon_plan_s* p, void* const* hp, const void* const* hg,
+                                 float* const* hm, std::vector<void*>& dp, std::vector<void*>& dg,
+                                 std::vector<float*>& dm, float beta, float lr, float wd,
+                                 int32_t k, float a, float b, float c, cudaStream_t s) {
+  const float coef[3] = {a, b, c};
+  if (muon_status_t st = step_impl(p, dp.data(), (const void* const*)dg.data(), dm.data(), beta, lr,
+                                   wd, k, coef, 1, s, false))
+    return st;
+  CUDA_TRY(cudaEventRecord(p->up_ev, s));
+  CUDA_TRY(cudaStreamWaitEvent(p->h2d, p->up_ev, 0));
+  const size_t pes = p_esize(p);
+  const size_t ng = p->d.groups.size();
+  // the parameters of each group, in member order, each once
+  std::vector<std::vector<int32_t>> params(ng);
+  for (size_t gi = 0; gi < ng; ++gi) {
+    const GroupPlan& g = p->d.groups[gi];
+    for (int64_t i = 0; i < g.batch; ++i) {
+      const int32_t pi = p->d.member_param[g.first_member + i];
+      if (params[gi].empty() || params[gi].back() != pi) params[gi].push_back(pi);
+    }
+  }
+  auto copy = [&](const std::vector<int32_t>& ps, const void* const* host, void* const* dev, size_t es,
+                  bool to_device, cudaStream_t st) -> cudaError_t {
+    for (int32_t pi : ps) {
+      const cudaError_t e = copy_param_runs(p, pi, pi + 1, host, dev, es, to_device, st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  };
+  std::vector<const void*> hpc(hp, hp + dp.size()), hmc(hm, hm + dp.size());
+  std::vector<void*> dmv(dm.begin(), dm.end());
+  for (size_t gi = 0; gi < ng; ++gi) {
+    CUDA_TRY(copy(params[gi], hpc.data(), dp.data(), pes, true, p->h2d));
+    CUDA_TRY(copy(params[gi], hg, dg.data(), pes, true, p->h2d));
+    CUDA_TRY(copy(params[gi], hmc.data(), dmv.data(), 4, true, p->h2d));
+    CUDA_TRY(cudaEventRecord(p->in_ev[gi], p->h2d));
+  }
+  for (size_t gi = 0; gi < ng; ++gi) {
+    CUDA_TRY(cudaStreamWaitEvent(s, p->in_ev[gi], 0));
+    const cudaError_t e = enqueue_group_kernels(p, p->d.groups[gi], k, s);
+    if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    CUDA_TRY(cudaEventRecord(p->run_ev[gi], s));
+    CUDA_TRY(cudaStreamWaitEvent(p->d2h, p->run_ev[gi], 0));
+    CUDA_TRY(copy(params[gi], hpc.data(), dp.data(), pes, false, p->d2h));
+    CUDA_TRY(copy(params[gi], hmc.data(), dmv.data(), 4, false, p->d2h));
+  }
+  CUDA_TRY(cudaEventRecord(p->out_ev[0], p->d2h));
+  CUDA_TRY(cudaStreamWaitEvent(s, p->out_ev[0], 0));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return MUON_OK;
+}
+
 }  // namespace
 
 muon_status_t muon_step(muon_plan_t p, void* const* params, const void* const* grads,
@@ -906,6 +967,8 @@ muon_status_t muon_step_host(muon_plan_t p, void* const* hp, const void* const* 
   muon_status_t st;
   if (all_skinny(p) && !p->in_ev.empty() && np > 1)
     return host_step_pipelined(p, hp, hg, hm, dp, dg, dm, beta, lr, wd, ns_steps, a, b, c, s);
+  if (p->d.groups.size() > 1 && p->in_ev.size() >= p->d.groups.size())
+    return host_step_by_group(p, hp, hg, hm, dp, dg, dm, beta, lr, wd, ns_steps, a, b, c, s);
   if ((st = copy_runs([&](int32_t i) { return (const void*)hp[i]; },
                       [&](int32_t i) { return (const void*)dp[i]; }, pes, cudaMemcpyHostToDevice)))
     return st;

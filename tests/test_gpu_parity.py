@@ -259,6 +259,29 @@ def test_step_host_equals_device_step():
     dev.close(); host.close()
 
 
+def test_step_host_by_group_equals_device_step():
+    """Plans with tensor-path groups pipeline the host step group by group
+    (copy in, kernels, copy out on three streams): same bits as the device
+    step, over two steps."""
+    w = W.custom([[256, 512], [24, 2048], [512, 256], [256, 512], [2, 64, 768]], seed=17)
+    P, G, M = W.make_tensors(w, "cuda")
+    hP = [t.cpu().pin_memory() for t in P]
+    hG = [t.cpu().pin_memory() for t in G]
+    hM = [t.cpu().pin_memory() for t in M]
+    dev = pkg.MuonPlan(w.shapes)
+    host = pkg.MuonPlan(w.shapes, host_staging=True)
+    assert len(dev.groups()) == 4
+    c = tuple(F32(v) for v in w.coeffs)
+    for _ in range(2):
+        dev.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, c)
+        host.step_host(hP, hG, hM, w.beta, w.lr, w.wd, w.ns_steps, c)
+    torch.cuda.synchronize()
+    for i in range(len(P)):
+        assert torch.equal(P[i].cpu(), hP[i])
+        assert torch.equal(M[i].cpu(), hM[i])
+    dev.close(); host.close()
+
+
 def test_bound_step_equals_step():
     w = W.custom([[24, 4096]] * 3, seed=19)
     P1, G1, M1 = W.make_tensors(w, "cuda")
