@@ -632,6 +632,14 @@ def main():
             else:
                 ent, _ = measure(wc, args, pkg, torch, dev, local, world, peaks, stream, flush, True)
                 ent.pop("wall_s_timed", None)
+                if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                    # the oracle on a smaller sample (about 5 s) of this configuration
+                    bc, fc = algorithmic_work(wc.shapes, wc.mode, wc.ns_steps)
+                    t, wall, cpu_s, note = oracle_estimate(wc, 5.0, host_member_inputs(wc))
+                    cv, cu = headline(wc, bc, fc, t)
+                    ent["cpu_baseline"] = {"value": cv, "unit": cu, "ms_per_step": t * 1e3,
+                                           "cores": busy_cores(wall, cpu_s), "kind": "oracle",
+                                           "sample": note}
             per_config.append(ent)
 
     e2e = None

@@ -83,6 +83,9 @@ struct SkinnyCfg {
   int32_t blk;       // bytes of one 16-column block in the fragment workspace
   int64_t ws_bytes;  // fragment workspace bytes per member (direct kernel)
   int32_t gram_space;  // the Gram-space kernel serves ns_steps <= kGramSpaceMaxSteps
+  int32_t auto_shards; // the plan left column_shards to the library (0): for m <= 32 the
+                       // Gram-space kernel may then run 4-CTA clusters of 8 warps for
+                       // small batches (the same reduction tree, so the same bits)
 };
 
 // Step counts the Gram-space kernel takes: along an exact null direction of

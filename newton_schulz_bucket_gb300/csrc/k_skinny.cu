@@ -535,6 +535,7 @@ bool skinny_config(int32_t rows, int32_t cols, int32_t max_m, SkinnyCfg* cfg, in
   cfg->ws_bytes = (int64_t)cl * (cfg->width / 16) * blk;  // per member (direct kernel)
   cfg->smem = 0;
   cfg->gram_space = 1;  // every skinny m (<= 64); the step count decides at launch
+  cfg->auto_shards = shards <= 0;
   return true;
 }
 

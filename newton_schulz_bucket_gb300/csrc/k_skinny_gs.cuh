@@ -58,6 +58,29 @@ namespace gs {
 constexpr int kVarPlain = 0, kVarNesterov = 1, kVarTransposed = 2;
 
 
+// Sum of N (a power of two) values as the binary tree
+// ((v0 + v1) + (v2 + v3)) + ...: a fixed order, so that a tree over more
+// leaves can be split into subtrees computed in different places.
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&v)[N]) {
+#pragma unroll
+  for (int s = 1; s < N; s *= 2)
+#pragma unroll
+    for (int k = 0; k + s < N; k += 2 * s) v[k] += v[k + s];
+  return v[0];
+}
+// The same tree over the value at `local` in each of the cluster's CL CTAs
+// (CL = 1, 2, 4 or 8), read through distributed shared memory.
+__device__ __forceinline__ float cluster_tree_sum(const float* local, int CL) {
+  float v[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = r < CL ? ld_dsmem_f32(local, (uint32_t)r) : 0.f;
+  if (CL == 1) return v[0];
+  if (CL == 2) return v[0] + v[1];
+  if (CL == 4) return (v[0] + v[1]) + (v[2] + v[3]);
+  return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+}
+
 template <int MT, int NT, bool HALF>
 struct GsLayout {
   static constexpr int MP = 16 * MT;                    // padded m
@@ -74,7 +97,11 @@ struct GsLayout {
   static constexpr int kTab = ((MP * (MP + 1) / 2) * 4 + 15) / 16 * 16;
   static constexpr int kCoef = kMaxScheduleRows * 3 * 4;  // the step's (a, b, c) rows
   static constexpr int kFixed = MP * MP * 4 + 64 + MP * 4 + kTab + kCoef;
-  static constexpr int kCap = 227 * 1024 - kFixed;
+  // shared memory of one CTA: all of it, or, for the 8-warp form of m <= 32
+  // that puts two CTAs on an SM, half the SM's 228 KB less the 1 KB the
+  // runtime reserves per CTA
+  static constexpr int kBudget = (MT <= 2 && NT == 256) ? 233472 / 2 - 1024 : 227 * 1024;
+  static constexpr int kCap = kBudget - kFixed;
   // momentum pass ring: 32 B of M and 16 B of G per row and lane; one round at a time
   static constexpr int LB1 = 48 * R;
   static constexpr int S1 = 4 * NW * 32 * LB1 <= kCap ? 4 : (3 * NW * 32 * LB1 <= kCap ? 3 : 2);
@@ -104,7 +131,7 @@ struct GsLayout {
   static constexpr int kCoefOff = kTabOff + kTab;       // schedule rows, copied from the step scalars
   static constexpr int kTotal = kCoefOff + kCoef;
   static_assert(kTotal == kU + kFixed, "layout");
-  static_assert(kTotal <= 227 * 1024, "Gram-space kernel shared memory exceeds the per-CTA limit");
+  static_assert(kTotal <= kBudget, "Gram-space kernel shared memory exceeds the per-CTA budget");
 };
 
 // Wide-iterate element (i, j) in the parameter's memory.
@@ -153,7 +180,8 @@ __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uin
 // only slowed the pass.
 template <int MT, int NT, bool HALF, int VAR>
 __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
-                                                 float (&gacc)[GsLayout<MT, NT, HALF>::GT::N][4], float& ss) {
+                                                 float (&gacc)[GsLayout<MT, NT, HALF>::GT::N][4], float& ss,
+                                                 int LS) {
   constexpr bool NEST = VAR == kVarNesterov, TP = VAR == kVarTransposed;
   using L = GsLayout<MT, NT, HALF>;
   using GT = typename L::GT;
@@ -163,7 +191,9 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   uint8_t* ring_warp = ring + c.warp * 32 * LB;
   const uint32_t ring0 = smem_u32(ring_warp);
   const int nsb = c.NB / 2;  // superblocks of this CTA
-  const int rounds = (nsb + NW - 1) / NW;
+  // warp w takes the LS superblocks w LS .. w LS + LS - 1 of the CTA (its
+  // leaf of the reduction tree), in order
+  const int rounds = LS;
   auto row_of = [&](int s) { return (s >> 1) * 16 + c.g + ((s & 1) ? 8 : 0); };
   const uint64_t pol = l2_evict_normal();
   const float2 beta2 = make_float2(c.beta, c.beta);
@@ -183,7 +213,7 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   // spread over the lanes; rows past n are zero-filled.
   const int mq = c.m / 4;  // 16-byte chunks per row of M (transposed member)
   auto issue_t = [&](int r, uint32_t dst) {
-    const int sb = r * NW + c.warp;
+    const int sb = c.warp * LS + r;
     if (r < rounds && sb < nsb) {
       const int J = c.c0 + sb * 32, nrows = min(32, c.n - J);
       const float* mb = c.Mp + (int64_t)J * c.m;
@@ -205,7 +235,7 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
       issue_t(r, dst);
       return;
     }
-    const int sb = r * NW + c.warp;
+    const int sb = c.warp * LS + r;
     if (c.vec && r < rounds && sb < nsb) {
       const int J = c.c0 + sb * 32;
 #pragma unroll
@@ -232,7 +262,7 @@ __device__ __forceinline__ void gs_momentum_pass(const GsCtx& c, uint8_t* ring,
   for (int r = 0; r < S; ++r) issue(r, ring0 + r * kSlot);
 
   auto process = [&](int r, uint8_t* st) {
-    const int sb = r * NW + c.warp;
+    const int sb = c.warp * LS + r;
     if (r >= rounds || sb >= nsb) return;
     const int J = c.c0 + sb * 32;
     const int j0 = J + 8 * c.t4;
@@ -892,7 +922,8 @@ struct MmMats {
 };
 
 template <typename TY, int MT, int NT, bool HALF, int VAR>
-__global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
+__global__ void __launch_bounds__(NT, (MT <= 2 && NT == 256) ? 2 : 1)
+    k_skinny_gs(KArgs a, int W, int NB, int LS) {
   constexpr bool NEST = VAR == kVarNesterov, TP = VAR == kVarTransposed;
   using L = GsLayout<MT, NT, HALF>;
   using GT = typename L::GT;
@@ -957,7 +988,7 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 #pragma unroll
   for (int q = 0; q < GT::N; ++q) gacc[q][0] = gacc[q][1] = gacc[q][2] = gacc[q][3] = 0.f;
   float ss = 0.f;
-  gs_momentum_pass<MT, NT, HALF, VAR>(c, smem, gacc, ss);
+  gs_momentum_pass<MT, NT, HALF, VAR>(c, smem, gacc, ss, LS);
   // Hint: move this CTA's slice of P into L2 while the m x m work runs.
   if (c.vec && warp == NW - 1 && c.c0 < c.n) {
     const int ncol = min(W, c.n - c.c0);
@@ -966,7 +997,9 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
       for (int i = lane; i < m; i += 32) prefetch_l2(c.P + (int64_t)i * c.cols + c.c0, bytes);
   }
   __syncthreads();  // every warp's ring is drained before it is reused
-  // per-warp partials, then warps summed in a fixed order into this CTA's partial
+  // per-warp (leaf) partials, then this CTA's partial as the binary tree
+  // over its warps' leaves, then (below) the cluster's as the binary tree
+  // over its CTAs: one fixed tree over all CL x NW leaves, whatever CL and NW
   ss = warp_sum(ss);
   if (lane == 0) wss[warp] = ss;
 #pragma unroll
@@ -980,32 +1013,30 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
   __syncthreads();
   for (int e = tid; e < GT::N * 128; e += NT) {
     const int q = e >> 7, w = e & 127;
-    float acc = 0.f;
-    for (int k = 0; k < NW; ++k) acc += wpart[(k * GT::N + q) * 128 + w];
+    float v[NW];
+#pragma unroll
+    for (int k = 0; k < NW; ++k) v[k] = wpart[(k * GT::N + q) * 128 + w];
     const int code = GT::code(q);
-    cpart[((code >> 4) * 16 + (w >> 3)) * MP + (code & 15) * 8 + (w & 7)] = acc;
+    cpart[((code >> 4) * 16 + (w >> 3)) * MP + (code & 15) * 8 + (w & 7)] = tree_sum<NW>(v);
   }
   if (tid == 0) {
-    float acc = 0.f;
-    for (int k = 0; k < NW; ++k) acc += wss[k];
-    misc[0] = acc;
+    float v[NW];
+#pragma unroll
+    for (int k = 0; k < NW; ++k) v[k] = wss[k];
+    misc[0] = tree_sum<NW>(v);
   }
   cluster_sync();  // (also a CTA barrier: the partials are consumed)
   for (int e = tid; e < Mats::kWords; e += NT) mats.base[e] = 0u;  // m x m arrays, padding included
   __syncthreads();
-  // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: CTAs summed in rank order
-  float ssum = 0.f;
-#pragma unroll
-  for (int r = 0; r < CL; ++r) ssum += ld_dsmem_f32(&misc[0], (uint32_t)r);
+  // the norm, then A_0 = M' M'^T / (||M'||_F + eps)^2: the CTAs' partials
+  // combined by the binary tree over ranks
+  const float ssum = cluster_tree_sum(&misc[0], CL);
   const float inv_raw = 1.f / (sqrtf(ssum) + a.eps);
   c.inv = a.alpha * inv_raw;
   const float inv2 = inv_raw * inv_raw;
   for (int e = tid; e < nup; e += NT) {
     const int i = tab[e] >> 16, j = tab[e] & 0xffff;
-    float acc = 0.f;
-#pragma unroll
-    for (int r = 0; r < CL; ++r) acc += ld_dsmem_f32(&cpart[i * MP + j], (uint32_t)r);
-    acc *= inv2;
+    const float acc = cluster_tree_sum(&cpart[i * MP + j], CL) * inv2;
     mats.put(0, i, j, acc);
     mats.put(0, j, i, acc);
   }
@@ -1249,25 +1280,67 @@ __global__ void __launch_bounds__(NT, 1) k_skinny_gs(KArgs a, int W, int NB) {
 template <int MT>
 constexpr int gs_threads() { return MT <= 2 ? 512 : 256; }
 
-template <typename TY, int MT, bool HALF, int VAR>
-cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
-  constexpr int NT = gs_threads<MT>();
+inline int gs_num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+// One launch in clusters of CL CTAs of NT threads.  The member's superblocks
+// go to CL x NW leaves of LS consecutive superblocks each (the last ones
+// possibly short or empty), warp w of CTA r taking leaf r NW + w; each CTA
+// spans NW LS superblocks.
+template <typename TY, int MT, int NT, bool HALF, int VAR>
+cudaError_t launch_gs_cl(const KArgs& a, int CL, cudaStream_t st) {
   auto fn = k_skinny_gs<TY, MT, NT, HALF, VAR>;
-  constexpr int smem = GsLayout<MT, NT, HALF>::kTotal;
-  if (prepare) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int NW = NT / 32;
+  const int sg = (a.n + 31) / 32;
+  const int LS = (sg + CL * NW - 1) / (CL * NW);
+  const int W = NW * LS * 32;
   cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3(a.B * cfg.cluster);
+  lc.gridDim = dim3(a.B * CL);
   lc.blockDim = dim3(NT);
-  lc.dynamicSmemBytes = smem;
+  lc.dynamicSmemBytes = GsLayout<MT, NT, HALF>::kTotal;
   lc.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = cfg.cluster;
+  at[0].val.clusterDim.x = CL;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, fn, a, (int)cfg.width, (int)(cfg.width / 16));
+  return cudaLaunchKernelEx(&lc, fn, a, W, W / 16, LS);
+}
+
+// For m <= 32 with the shard count left to the library, a batch too small
+// to fill the GPU with 2-CTA clusters of 16 warps runs 4-CTA clusters of 8
+// warps (two CTAs per SM): 32 leaves either way, so the reduction tree and
+// every bit of the result are the same, and twice the SMs share the work.
+template <typename TY, int MT, bool HALF, int VAR>
+cudaError_t launch_gs_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t st, bool prepare) {
+  constexpr int NT = gs_threads<MT>();
+  if (prepare) {
+    cudaError_t e = cudaFuncSetAttribute(k_skinny_gs<TY, MT, NT, HALF, VAR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GsLayout<MT, NT, HALF>::kTotal);
+    if constexpr (MT <= 2) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_skinny_gs<TY, MT, 256, HALF, VAR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GsLayout<MT, 256, HALF>::kTotal);
+    }
+    return e;
+  }
+  if constexpr (MT <= 2) {
+    if (cfg.auto_shards && cfg.cluster == 2 && 8 * 2 * a.B < 7 * gs_num_sms())
+      return launch_gs_cl<TY, MT, 256, HALF, VAR>(a, 4, st);
+  }
+  return launch_gs_cl<TY, MT, NT, HALF, VAR>(a, cfg.cluster, st);
 }
 
 template <typename TY, int MT, bool HALF, int VAR>
