@@ -143,12 +143,15 @@ typedef struct {
   uint32_t flags;            /* MUON_FLAG_*                                        */
   int32_t path_override;     /* muon_path_t for every group; AUTO = choose         */
   int32_t max_streams;       /* groups run on up to this many graph branches; 0=4  */
-  int32_t column_shards;     /* skinny path: CTAs per member (1, 2, 4 or 8; 0 = 2), */
-                             /* each owning one contiguous column shard; their     */
-                             /* partial Grams and sums of squares are added in     */
-                             /* shard order («关于分布式Muon的想法整合及讨论» §6). */
-                             /* Bits depend on it (summation order), never on the  */
-                             /* batch; more shards help small batches fill the GPU */
+  int32_t column_shards;     /* skinny path: CTAs per member (1, 2, 4 or 8), each   */
+                             /* owning one contiguous column shard; their partial  */
+                             /* Grams and sums of squares are all-reduced through  */
+                             /* distributed shared memory («关于分布式Muon的想法整合 */
+                             /* 及讨论» §6).  0 = chosen by the library: 2, or 4 for*/
+                             /* batches too small to fill the GPU when m <= 32,    */
+                             /* with the same bits either way (one fixed reduction */
+                             /* tree).  An explicit t fixes the form; the bits then*/
+                             /* depend on t, never on the batch                    */
   int32_t reserved[7];       /* must be zero                                       */
 } muon_plan_options;
 
