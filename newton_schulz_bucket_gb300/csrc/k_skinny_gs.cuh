@@ -1397,6 +1397,13 @@ cudaError_t gs_dispatch_t(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, 
   return a.ns_type == NS_F16 ? gs_launch_ty<__half, VAR>(a, cfg, s, prepare)
                              : gs_launch_ty<__nv_bfloat16, VAR>(a, cfg, s, prepare);
 }
+// The same for one operand type only (a variant split over two translation
+// units to keep each one's compile time short).
+template <typename TY, int VAR>
+cudaError_t gs_dispatch_ty(const KArgs& a, const SkinnyCfg& cfg, cudaStream_t s, bool prepare) {
+  if (a.mode_f32 || cfg.mtiles < 1 || cfg.mtiles > 4) return cudaErrorInvalidValue;
+  return gs_launch_ty<TY, VAR>(a, cfg, s, prepare);
+}
 
 template <int VAR>
 int gs_clusters_t(int ns_type, int m, int cl) {
