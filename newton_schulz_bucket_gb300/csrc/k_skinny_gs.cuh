@@ -1,6 +1,7 @@
-// Skinny path for m = min(rows, cols) <= 64 (kernel templates; k_skinny_gs.cu
-// and k_skinny_gs_nesterov.cu instantiate them): the whole Muon step of a member
-// in one kernel, with Newton-Schulz evaluated in Gram space.
+// Skinny path for m = min(rows, cols) <= 64 (kernel templates; k_skinny_gs.cu,
+// k_skinny_gs_nesterov.cu and k_skinny_gs_transposed*.cu instantiate them):
+// the whole Muon step of a member in one kernel, with Newton-Schulz evaluated
+// in Gram space.
 //
 // «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: for
 // shapes such as [24, 10240] the per-parameter iteration is dominated by host
@@ -18,30 +19,34 @@
 //      Q = a I + b A + c A^2, Pi <- Q Pi, A <- Q A Q (3xTF32 tensor-core
 //      tiles up to m = 32, where the stage is latency-bound; fp32 FFMA
 //      above, where it is throughput-bound);
-//   3. output pass: Y_0 = alpha M' / (||M'||_F + eps) in the operand type,
-//      O = Pi_k Y_0 / alpha with Pi_k split into an operand-type high part and
-//      a residual low part, and P' = P (1 - lr wd) - lr s O.
+//   3. output pass: Y_0 = alpha M' / (||M'||_F + eps) split into an
+//      operand-type high part and residual, O = Pi_k Y_0 / alpha with Pi_k
+//      split the same way, and P' = P (1 - lr wd) - lr s O.
 //
 // Each quintic step is X' = Q X with Q = a I + b A + c A^2 and A = X X^T
 // («关于分布式Muon的想法整合及讨论» §1, §2, §6).  Q is a polynomial in A, so it
 // is symmetric and commutes with A, hence A' = X' X'^T = Q A Q and
 // X_k = Pi_k X_0 with Pi_k = Q_{k-1} ... Q_0: in exact arithmetic this is the
 // iteration itself; in floating point the data is rounded to the operand
-// type once instead of once per step.  All reduction orders depend only on
-// (rows, cols), so a member gives the same bits in any batch.
+// type once instead of once per step.
 //
-// Layout: one cluster of CL CTAs per member (the plan's column shards; 2 by
-// default), CTA r owning one contiguous column shard of the wide iterate's
-// columns [r W, (r + 1) W), 16 warps up to m = 32 and 8 beyond (each lane
-// then keeps Pi's fragments for four 16-row tiles, 128 registers).  Both
-// passes walk 32-column superblocks (superblock sb by warp sb % NW).  In the
-// momentum pass lane (g, t4) holds rows 16 mi + g (+ 8) and the eight
-// consecutive columns 8 t4 .. 8 t4 + 7, which stand in tf32 A-fragment slots
-// (see gs_momentum_pass); the output pass loads Y_0 straight into B
-// fragments (see gs_out_pass).  The Gram sums over all columns and Pi X acts on each column
-// alone, so these fixed permutations of a block's columns change nothing, and
-// they turn every access into a 16-byte (fp32) or 8/16-byte (bf16) vector.
-// Operands stream through a per-lane cp.async ring.
+// Layout: one cluster of CL CTAs per member, CTA r owning one contiguous
+// column shard of the wide iterate's columns [r W, (r + 1) W).  Up to m = 32
+// a CTA has 16 warps (2-CTA clusters) or 8 warps (4-CTA clusters, two CTAs
+// per SM, for batches too small to fill the GPU); beyond, 8 warps, each lane
+// keeping Pi's fragments for four 16-row tiles (128 registers).  Both passes
+// walk 32-column superblocks.  In the momentum pass warp w of CTA r takes
+// one contiguous leaf of the member's superblocks, leaf r NW + w, and the
+// leaves' partial sums are added by one fixed binary tree (over warps, then
+// over CTAs), so the bits depend only on (rows, cols) and the number of
+// leaves, never on the batch or the launch form.  Lane (g, t4) holds rows
+// 16 mi + g (+ 8) and the eight consecutive columns 8 t4 .. 8 t4 + 7, which
+// stand in tf32 A-fragment slots (see gs_momentum_pass); the output pass
+// loads Y_0 straight into B fragments (see gs_out_pass).  The Gram sums over
+// all columns and Pi X acts on each column alone, so these fixed
+// permutations of a block's columns change nothing, and they turn every
+// access into a 16-byte (fp32) or 8/16-byte (bf16) vector.  Operands stream
+// through a per-lane cp.async ring.
 #pragma once
 
 #include "warp_mma.cuh"
