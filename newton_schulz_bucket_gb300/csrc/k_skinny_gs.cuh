@@ -526,54 +526,57 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
     };
     // With several 16-row output tiles, each k-tile's fragments are needed
     // once per output tile, and holding both parts of every k-tile in
-    // registers would not fit: on the vector path they are formed once and
-    // written over this lane's own fp32 rows of the ring slot (the same 64
-    // bytes per k-tile: chunk 4 kk + h holds bh[.][h], chunk 4 kk + 2 + h
-    // holds bl[.][h]; a half k-tile has chunks 4 kk + {0, 1} only), then
-    // read back per output tile.  The scalar path rebuilds them.
+    // registers would not fit: on the vector path the first output tile forms
+    // them and writes them over this lane's own fp32 rows of the ring slot
+    // (the same 64 bytes per k-tile: chunk 4 kk + h holds bh[.][h], chunk
+    // 4 kk + 2 + h holds bl[.][h]; a half k-tile has chunks 4 kk + {0, 1}
+    // only), and the other output tiles read them back.  The scalar path
+    // rebuilds them.
     constexpr bool kStage = MT > 1;
-    if (kStage && c.vec) {
+    const bool staged = kStage && c.vec;
+    auto store_b = [&](int kk, const uint32_t (&bh)[4][2], const uint32_t (&bl)[4][2]) {
+      uint8_t* base = const_cast<uint8_t*>(st) + (4 * kk) * 512 + lane * 16;
+      if (HALF && kk == MT - 1) {
+        *reinterpret_cast<uint4*>(base) = make_uint4(bh[0][0], bh[1][0], bh[2][0], bh[3][0]);
+        *reinterpret_cast<uint4*>(base + 512) = make_uint4(bl[0][0], bl[1][0], bl[2][0], bl[3][0]);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          *reinterpret_cast<uint4*>(base + h * 512) = make_uint4(bh[0][h], bh[1][h], bh[2][h], bh[3][h]);
+          *reinterpret_cast<uint4*>(base + (2 + h) * 512) = make_uint4(bl[0][h], bl[1][h], bl[2][h], bl[3][h]);
+        }
+      }
+    };
+    auto load_b = [&](int kk, uint32_t (&bh)[4][2], uint32_t (&bl)[4][2]) {
+      const uint8_t* base = st + (4 * kk) * 512 + lane * 16;
+      if (HALF && kk == MT - 1) {
+        const uint4 h0 = *reinterpret_cast<const uint4*>(base);
+        const uint4 l0 = *reinterpret_cast<const uint4*>(base + 512);
+        bh[0][0] = h0.x; bh[1][0] = h0.y; bh[2][0] = h0.z; bh[3][0] = h0.w;
+        bl[0][0] = l0.x; bl[1][0] = l0.y; bl[2][0] = l0.z; bl[3][0] = l0.w;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bh[q][1] = bl[q][1] = 0u;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 hv = *reinterpret_cast<const uint4*>(base + h * 512);
+          const uint4 lv = *reinterpret_cast<const uint4*>(base + (2 + h) * 512);
+          bh[0][h] = hv.x; bh[1][h] = hv.y; bh[2][h] = hv.z; bh[3][h] = hv.w;
+          bl[0][h] = lv.x; bl[1][h] = lv.y; bl[2][h] = lv.z; bl[3][h] = lv.w;
+        }
+      }
+    };
+    // up to two output tiles the first one stages the fragments as it goes;
+    // with more, a separate pass does (it keeps the registers lower)
+    constexpr bool kFuse = MT <= 2;
+    if (!kFuse && staged) {
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
         uint32_t bh[4][2], bl[4][2];
         make_b(kk, bh, bl);
-        uint8_t* base = const_cast<uint8_t*>(st) + (4 * kk) * 512 + lane * 16;
-        if (HALF && kk == MT - 1) {
-          *reinterpret_cast<uint4*>(base) = make_uint4(bh[0][0], bh[1][0], bh[2][0], bh[3][0]);
-          *reinterpret_cast<uint4*>(base + 512) = make_uint4(bl[0][0], bl[1][0], bl[2][0], bl[3][0]);
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            *reinterpret_cast<uint4*>(base + h * 512) = make_uint4(bh[0][h], bh[1][h], bh[2][h], bh[3][h]);
-            *reinterpret_cast<uint4*>(base + (2 + h) * 512) =
-                make_uint4(bl[0][h], bl[1][h], bl[2][h], bl[3][h]);
-          }
-        }
+        store_b(kk, bh, bl);
       }
     }
-    auto load_b = [&](int kk, uint32_t (&bh)[4][2], uint32_t (&bl)[4][2]) {
-      if (kStage && c.vec) {
-        const uint8_t* base = st + (4 * kk) * 512 + lane * 16;
-        if (HALF && kk == MT - 1) {
-          const uint4 h0 = *reinterpret_cast<const uint4*>(base);
-          const uint4 l0 = *reinterpret_cast<const uint4*>(base + 512);
-          bh[0][0] = h0.x; bh[1][0] = h0.y; bh[2][0] = h0.z; bh[3][0] = h0.w;
-          bl[0][0] = l0.x; bl[1][0] = l0.y; bl[2][0] = l0.z; bl[3][0] = l0.w;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) bh[q][1] = bl[q][1] = 0u;
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 hv = *reinterpret_cast<const uint4*>(base + h * 512);
-            const uint4 lv = *reinterpret_cast<const uint4*>(base + (2 + h) * 512);
-            bh[0][h] = hv.x; bh[1][h] = hv.y; bh[2][h] = hv.z; bh[3][h] = hv.w;
-            bl[0][h] = lv.x; bl[1][h] = lv.y; bl[2][h] = lv.z; bl[3][h] = lv.w;
-          }
-        }
-      } else {
-        make_b(kk, bh, bl);
-      }
-    };
 #pragma unroll
     for (int mi = 0; mi < MT; ++mi) {
       float d[4][4];
@@ -582,7 +585,12 @@ __device__ __forceinline__ void gs_out_pass(const GsCtx& c, uint8_t* ring,
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
         uint32_t bh[4][2], bl[4][2];
-        load_b(kk, bh, bl);
+        if (staged && (mi > 0 || !kFuse)) {
+          load_b(kk, bh, bl);
+        } else {
+          make_b(kk, bh, bl);
+          if (staged) store_b(kk, bh, bl);
+        }
         // O += Pi_hi Y_hi + Pi_lo Y_hi + Pi_hi Y_lo (Pi_lo Y_lo is below fp32's resolution)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
