@@ -206,14 +206,16 @@ __device__ __forceinline__ void store_row32(TY* dst, const float* v, int nvalid)
 // The epilogue of one output tile for one epilogue warp: rows
 // rbase + quarter * 32 + lane (one accumulator row per thread, TMEM lanes
 // quarter * 32 ..), columns cbase .. cbase + BN - 1 from the accumulator at
-// TMEM column tmem_acc, in chunks of 32 columns.  GRAM scales by 1 / alpha^2,
-// POLY forms a I + b A + c A^2 (A read from p.aux); GRAM and POLY write the
-// elements with col >= row in place and mirror those with col > row through
-// this warp's 32 x 32 staging block `epi`; UPDATE stores the row.
+// TMEM column tmem_acc, in chunks of 32 columns (chunks ch0 .. ch1 - 1 of
+// the tile, so that two warps can share a row quarter).  GRAM scales by
+// 1 / alpha^2, POLY forms a I + b A + c A^2 (A read from p.aux); GRAM and
+// POLY write the elements with col >= row in place and mirror those with
+// col > row through this warp's 32 x 32 staging block `sw`; UPDATE stores
+// the row.
 template <typename TY, int OP, int BN>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& p, uint32_t tmem_acc, int quarter, int lane,
                                               int b, int rbase, int cbase, float ca, float cb, float cc,
-                                              uint32_t* epi) {
+                                              uint32_t* sw, int ch0 = 0, int ch1 = BN / 32) {
   const int row_in_tile = quarter * 32 + lane;
   const int row = rbase + row_in_tile;
   const int row0 = rbase + quarter * 32;  // this warp's first row
@@ -222,7 +224,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& p, uint32_t tmem_acc
                                        (int64_t)row * p.ldc
                                  : nullptr;
 #pragma unroll 1
-  for (int ch = 0; ch < BN / 32; ++ch) {
+  for (int ch = ch0; ch < ch1; ++ch) {
     uint32_t r[32];
     const uint32_t taddr = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ch * 32);
     tmem_ld32(taddr, r);
@@ -277,7 +279,6 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& p, uint32_t tmem_acc
       // strictly above also at (j, i): the warp's 32 x 32 block goes
       // through shared memory, so that lane j then writes row col0 + j of
       // the mirror, 32 values from column row0, as 16-byte stores
-      uint32_t* sw = epi + quarter * (32 * 17);
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const TY lo = from_f32<TY>(v[2 * q]), hi = from_f32<TY>(v[2 * q + 1]);
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(tfull(acc), aph, abort_flag, p.err, 8)) break;
       tc_fence_after();
       epilogue_tile<TY, OP, BN>(p, tmem_base + (uint32_t)(acc * BN), quarter, lane, b, tm * BM, tn * BN,
-                                ca, cb, cc, epi);
+                                ca, cb, cc, epi + quarter * (32 * 17));
       tc_fence_before();
       mbar_arrive(tempty(acc));
       if (++acc == 2) { acc = 0; aph ^= 1; }
@@ -459,6 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // its part of an accumulator.
 constexpr int kStages2 = 6;
 constexpr int BM2 = 256;  // rows of a pair tile
+// Warps of a pair CTA: a TMA producer, the MMA issuer, and eight epilogue
+// warps, two per 32-lane quarter of TMEM, each taking half the tile's
+// columns: with short K (m up to ~2048 for the polynomial and Gram
+// products) the epilogue would otherwise take longer than the next tile's
+// MMAs and set the pace.
+constexpr int kEpiWarps2 = 8;
+constexpr int kThreads2 = 64 + 32 * kEpiWarps2;
 
 struct TcSmem2 {
   static constexpr uint32_t kA = 128 * BK * 2;           // 16 KB: this CTA's A rows
@@ -466,7 +474,7 @@ struct TcSmem2 {
   static constexpr uint32_t kStage = kA + kB;
   static constexpr uint32_t kBars = kStages2 * kStage;   // full, empty, tfull, tempty, done
   static constexpr uint32_t kEpi = kBars + 256;
-  static constexpr uint32_t kEpiBytes = 4 * 32 * 17 * 4;
+  static constexpr uint32_t kEpiBytes = kEpiWarps2 * 32 * 17 * 4;
   static constexpr uint32_t kTotal = kEpi + kEpiBytes + 1024;  // + alignment slack
   static_assert(kTotal <= 227 * 1024, "pair GEMM shared memory exceeds the per-CTA limit");
 };
@@ -519,7 +527,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 
 template <typename TY, int OP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads2, 1)
     k_tc_gemm2(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                TcArgs p) {
   constexpr int BN = 256;
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages2; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
     // tempty: one arrival per epilogue warp of both CTAs
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 8); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 2 * kEpiWarps2); }
     mbar_init(done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -632,8 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int keep_waiting = 0;
       mbar_wait(done, 0, &keep_waiting, p.err, 16);
     }
-  } else {  // ---- epilogue: warps 2..5 of both CTAs, one accumulator row per thread ----
-    const int quarter = warp & 3;
+  } else {  // ---- epilogue: warps 2..9 of both CTAs, one accumulator row per thread ----
+    const int quarter = warp & 3;                 // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;             // which half of the tile's columns
+    constexpr int kHalf = BN / 64;                // chunks of 32 columns per half
     float ca = 0.f, cb = 0.f, cc = 0.f;
     if (OP == TC_POLY) {
       const float* cf = step_coef(p.sc, p.step);
@@ -647,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(tfull(acc), aph, abort_flag, p.err, 8)) break;
       tc_fence_after();
       epilogue_tile<TY, OP, BN>(p, tmem_base + (uint32_t)(acc * BN), quarter, lane, b,
-                                tm * BM2 + (int)rank * 128, tn * BN, ca, cb, cc, epi);
+                                tm * BM2 + (int)rank * 128, tn * BN, ca, cb, cc,
+                                epi + (warp - 2) * (32 * 17), half * kHalf, half * kHalf + kHalf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to(tempty(acc), 0));
@@ -769,7 +780,7 @@ cudaError_t run_pair(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs&
   const int pairs = tiles < num_sms() / 2 ? tiles : num_sms() / 2;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(2 * pairs);
-  lc.blockDim = dim3(kThreads);
+  lc.blockDim = dim3(kThreads2);
   lc.dynamicSmemBytes = TcSmem2::kTotal;
   lc.stream = s;
   cudaLaunchAttribute at[1];
