@@ -521,8 +521,13 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t mbar, uint16_t mask) {
       "h"(mask)
       : "memory");
 }
+// Arrival of an epilogue warp on the leader's `tempty` barrier.  It only
+// hands the TMEM accumulator back: the tcgen05 fences around it order the
+// warp's tcgen05.ld reads before the leader's next MMAs, and the epilogue's
+// global stores need no ordering with it, so the arrival is relaxed (a
+// release at cluster scope would first wait for those stores to drain).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 
