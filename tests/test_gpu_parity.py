@@ -324,3 +324,46 @@ def test_argument_errors():
     plan.step(P, G, M, 0.9, 0.1, 0.0)
     plan.check_error()
     plan.close()
+
+
+def test_batch_invariance_bitwise_transposed():
+    """The transposed members' vector path: a member of a 74-member batch
+    (2-CTA clusters of 16 warps) equals, bit for bit, the same member alone
+    and in a batch of 5 (4-CTA clusters of 8 warps)."""
+    w = W.custom([[10240, 24]] * 74, seed=25)
+    full = GpuRun(w, sample=[(3, 0), (40, 0), (73, 0)])
+    for idx in ([40], [3, 9, 40, 41, 73]):
+        sub = W.custom([w.shapes[i] for i in idx], seed=0)
+        sub.beta, sub.lr, sub.wd = w.beta, w.lr, w.wd
+        run = GpuRun(sub, tensors=_member_tensors(w, idx))
+        for j, i in enumerate(idx):
+            if (i, 0) not in full.members:
+                continue
+            assert np.array_equal(run.p1(j), full.p1(i))
+            assert np.array_equal(run.m1(j), full.m1(i))
+            assert np.array_equal(run.O(j), full.O(i))
+        run.close()
+    full.close()
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_skinny_shapes_against_the_oracle(case):
+    """Seeded random skinny groups: m in [1, 64], n up to 6000, either
+    orientation, 1-3 parameters (some 3-D), k in 0..10 -- across the vector,
+    transposed-vector and element-wise paths and both launch forms."""
+    rng = np.random.default_rng(1000 + case)
+    shapes = []
+    for _ in range(int(rng.integers(1, 4))):
+        m = int(rng.integers(1, 65))
+        n = int(rng.integers(m, 6001))
+        if rng.random() < 0.3:
+            m = 8 * max(1, m // 8)  # often a multiple of 8 (vector paths)
+        r, c = (n, m) if rng.random() < 0.5 else (m, n)
+        shapes.append([int(rng.integers(2, 5)), r, c] if rng.random() < 0.3 else [r, c])
+    k = int(rng.integers(0, 11))
+    w = W.custom(shapes, seed=2000 + case, ns_steps=k)
+    run = GpuRun(w)
+    for g in run.plan.groups():
+        assert g["path"] == "skinny", g
+    check_all(run)
+    run.close()

@@ -144,3 +144,24 @@ def test_tensor_batch_invariance_bitwise():
     assert np.array_equal(run.m1(0, 0), full.m1(0, 2))
     assert np.array_equal(run.O(0, 0), full.O(0, 2))
     full.close(); run.close()
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_random_tensor_shapes_against_the_oracle(case):
+    """Seeded random tensor-path groups: m in [65, 700] (one-CTA form below
+    256, CTA-pair form from 256), n up to 2500, either orientation, ragged
+    tiles, sometimes 3-D, k in 1..6."""
+    rng = np.random.default_rng(3000 + case)
+    shapes = []
+    for _ in range(int(rng.integers(1, 3))):
+        m = int(rng.integers(65, 701))
+        n = int(rng.integers(m, 2501))
+        r, c = (n, m) if rng.random() < 0.5 else (m, n)
+        shapes.append([2, r, c] if rng.random() < 0.25 else [r, c])
+    k = int(rng.integers(1, 7))
+    w = W.custom(shapes, seed=4000 + case, ns_steps=k)
+    run = GpuRun(w)
+    for g in run.plan.groups():
+        assert g["path"] == "tensor", g
+    check_all(run)
+    run.close()
