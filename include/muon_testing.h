@@ -44,8 +44,9 @@ MUON_API int32_t muon_testing_tile_walk(int32_t op, int64_t m, int64_t n, int32_
 /* The same walk for the CTA-pair form of the products (a cluster of two CTAs
  * per 256 x 256 tile, tcgen05.mma.cta_group::2), which groups with
  * min(rows, cols) >= 256 use: tm[t] / tn[t] count 256-row / 256-column
- * tiles.  Same return values and errors as muon_testing_tile_walk.  Host
- * only. */
+ * tiles.  The products are those of muon_testing_tc_gemm («关于分布式Muon的
+ * 想法整合及讨论» §2).  Same return values and errors as
+ * muon_testing_tile_walk.  Host only. */
 MUON_API int32_t muon_testing_tile_walk_pair(int32_t op, int64_t m, int64_t n, int32_t* tm,
                                              int32_t* tn, int32_t cap);
 
