@@ -8,12 +8,13 @@
 // aX + (bA + cAA)X as (aI + bA + cAA)X folds the axpy into the polynomial
 // matrix, so each step is three dense products with fused epilogues.
 //
-// Design (sm_103a): persistent CTAs (one per SM), 192 threads:
+// Design (sm_103a): persistent CTAs (one per SM), 320 threads:
 //   warp 0      TMA producer: 128-byte-swizzled tiles into a 4-stage ring;
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128,
 //               N=BN, K=16, fp16/bf16 operands, fp32 accumulators in TMEM);
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
-//               fused scale / polynomial / cast, stores.
+//   warps 2..9  epilogue, two warps per 32-lane TMEM quarter, each on half
+//               of the tile's columns: tcgen05.ld of the accumulator (one
+//               row per thread), fused scale / polynomial / cast, stores.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Every wait is bounded: on timeout the kernel sets the plan's error
 // word and all roles leave their loops.
@@ -35,7 +36,12 @@ namespace muon {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, kStages = 4, kThreads = 192;
+constexpr int BM = 128, BK = 64, kStages = 4;
+// Warps of a one-CTA GEMM: a TMA producer, the MMA issuer, and eight
+// epilogue warps, two per 32-lane quarter of TMEM, each on half the tile's
+// columns (short-K products would otherwise wait on the epilogue).
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 enum TcOp { TC_GRAM = 0, TC_POLY = 1, TC_UPDATE = 2 };
 
@@ -124,8 +130,9 @@ struct TcSmem {
   // GRAM / POLY: per epilogue warp a 32 x 32 block of 16-bit values as 32 rows
   // of 17 words (a padded row keeps the column reads free of bank conflicts)
   static constexpr uint32_t kEpi = kBars + 256;
-  static constexpr uint32_t kEpiBytes = 4 * 32 * 17 * 4;
+  static constexpr uint32_t kEpiBytes = kEpiWarps * 32 * 17 * 4;
   static constexpr uint32_t kTotal = kEpi + kEpiBytes + 1024;  // + alignment slack
+  static_assert(kTotal <= 227 * 1024, "GEMM shared memory exceeds the per-CTA limit");
 };
 
 // Tile r of one batch's full output in grouped order: 8 tile-rows share a
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 128); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 32 * kEpiWarps); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&mapA) : "memory");
@@ -413,8 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     mma_done:;
     }
-  } else {  // ---- epilogue: warps 2..5, one accumulator row per thread ----
-    const int quarter = warp & 3;
+  } else {  // ---- epilogue: warps 2..9, one accumulator row per thread ----
+    const int quarter = warp & 3;                 // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;             // which half of the tile's columns
+    constexpr int kHalf = BN / 64;                // chunks of 32 columns per half
     float ca = 0.f, cb = 0.f, cc = 0.f;
     if (OP == TC_POLY) {
       const float* cf = step_coef(p.sc, p.step);
@@ -428,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(tfull(acc), aph, abort_flag, p.err, 8)) break;
       tc_fence_after();
       epilogue_tile<TY, OP, BN>(p, tmem_base + (uint32_t)(acc * BN), quarter, lane, b, tm * BM, tn * BN,
-                                ca, cb, cc, epi + quarter * (32 * 17));
+                                ca, cb, cc, epi + (warp - 2) * (32 * 17), half * kHalf,
+                                half * kHalf + kHalf);
       tc_fence_before();
       mbar_arrive(tempty(acc));
       if (++acc == 2) { acc = 0; aph ^= 1; }
