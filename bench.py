@@ -48,6 +48,7 @@ PER_CONFIG = [("c1_fp32_64x128", None), ("c2_skinny_74x24x10240", None),
               ("c5_mixed_1000", 5), ("c5_mixed_1000", 10)]
 L2_BYTES = 129 * 2 ** 20
 SKINNY_MAX_M = 64  # the planner's default skinny threshold (min(rows, cols) <= 64)
+RESIDENT_MAX = (128, 4096)  # the planner's resident path: rows <= 128, cols <= 4096, cols % 8 == 0
 
 
 def algorithmic_work(shapes, mode, k):
@@ -77,7 +78,10 @@ def shape_groups(shapes, mode):
         groups[key] = groups.get(key, 0) + E
     out = []
     for (r, c), b in groups.items():
-        path = "simt" if mode == "fp32" else ("skinny" if min(r, c) <= SKINNY_MAX_M else "tensor")
+        m, n = min(r, c), max(r, c)
+        res = r <= c and m <= RESIDENT_MAX[0] and n <= RESIDENT_MAX[1] and n % 8 == 0
+        path = ("simt" if mode == "fp32" else "skinny" if m <= SKINNY_MAX_M else
+                "resident" if res else "tensor")
         out.append({"rows": r, "cols": c, "batch": b, "path": path})
     return out
 
@@ -312,8 +316,9 @@ def oracle_estimate(w, budget_s, get):
 
 
 def headline(w, byts, flops, seconds):
-    """GB/s for workloads made only of skinny groups, else TFLOP/s."""
-    if all(g["path"] == "skinny" for g in shape_groups(w.shapes, w.mode)):
+    """GB/s for workloads made only of HBM-bound (skinny, resident) groups,
+    else TFLOP/s."""
+    if all(g["path"] in ("skinny", "resident") for g in shape_groups(w.shapes, w.mode)):
         return byts / seconds / 1e9, "GB/s"
     return flops / seconds / 1e12, "TFLOP/s"
 
@@ -383,7 +388,7 @@ def executed_flop_fraction(rows, cols):
 def executed_flops(w, groups):
     """Newton-Schulz FLOPs the step executes (the dense count, with the
     symmetric products of tensor-path groups reduced to their computed tiles;
-    skinny groups are counted dense)."""
+    skinny and resident groups are counted dense)."""
     tot = 0.0
     for g in groups:
         f = member_flops(g["rows"], g["cols"], w.ns_steps) * g["batch"]
@@ -402,7 +407,7 @@ def group_entry(info, gms, w, peaks):
         return ent
     ent["matrices_per_s"] = info["batch"] / (gms / 1e3)
     ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if info["path"] == "skinny" or gf / gb < ridge:
+    if info["path"] in ("skinny", "resident") or gf / gb < ridge:
         ach = gb / (gms / 1e3) / 1e9
         ent.update({"GB_s": ach, "roofline_frac": ach / peaks["hbm_gbs"], "bound": "hbm",
                     "flop_per_byte": gf / gb})
@@ -425,6 +430,9 @@ def roofline_of(w, dg, peaks):
             kfile = "k_skinny_gs.cuh" if gram_space else "k_skinny.cu"
             kernel = ("k_skinny_gs (momentum + Gram-space Newton-Schulz + write, one launch)"
                       if gram_space else "k_momentum_partial + k_skinny_ns")
+        elif dg["path"] == "resident":
+            kfile = "k_resident.cu"
+            kernel = "k_resident (momentum, the k Newton-Schulz steps on chip, write; one launch)"
         else:
             kfile = None
             kernel = f"group {dg['shape']} x {dg['batch']}: k_tc_gemm chain and the elementwise passes"

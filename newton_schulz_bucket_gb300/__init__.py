@@ -21,7 +21,8 @@ _NS = {"fp16": _c.MUON_NS_FP16, "bf16": _c.MUON_NS_BF16}
 _SCALES = {"sqrt_aspect": _c.MUON_SCALE_SQRT_ASPECT, "rms_0_2": _c.MUON_SCALE_RMS_0_2,
            "none": _c.MUON_SCALE_NONE}
 _PATHS = {"auto": _c.MUON_PATH_AUTO, "skinny": _c.MUON_PATH_SKINNY,
-          "tensor": _c.MUON_PATH_TENSOR, "simt": _c.MUON_PATH_SIMT}
+          "tensor": _c.MUON_PATH_TENSOR, "simt": _c.MUON_PATH_SIMT,
+          "resident": _c.MUON_PATH_RESIDENT}
 PATH_NAMES = {v: k for k, v in _PATHS.items()}
 
 
@@ -245,6 +246,8 @@ class MuonPlan:
             if g["path"] == "skinny":
                 # one fused kernel in Gram space (up to 64 steps), else momentum + iteration
                 n += 1 if ns_steps <= 64 else 2
+            elif g["path"] == "resident":
+                n += 1  # the whole step of the group in one kernel
             else:
                 n += 4 + 3 * int(ns_steps)
         return n

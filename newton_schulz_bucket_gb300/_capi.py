@@ -28,6 +28,7 @@ MUON_PATH_AUTO = 0
 MUON_PATH_SKINNY = 1
 MUON_PATH_TENSOR = 2
 MUON_PATH_SIMT = 3
+MUON_PATH_RESIDENT = 4
 MUON_FLAG_KEEP_UPDATE = 1
 MUON_FLAG_NO_GRAPH = 2
 MUON_FLAG_HOST_STAGING = 4

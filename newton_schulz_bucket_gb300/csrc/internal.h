@@ -36,7 +36,7 @@ struct MemberPtrs {
   float scale;
 };
 
-enum Path : int32_t { PATH_AUTO = 0, PATH_SKINNY = 1, PATH_TENSOR = 2, PATH_SIMT = 3 };
+enum Path : int32_t { PATH_AUTO = 0, PATH_SKINNY = 1, PATH_TENSOR = 2, PATH_SIMT = 3, PATH_RESIDENT = 4 };
 // Element type of the Newton-Schulz iterate / Gram / polynomial buffers.
 enum NsType : int32_t { NS_F32 = 0, NS_F16 = 1, NS_BF16 = 2 };
 

@@ -24,6 +24,7 @@
 
 #include "../../include/muon.h"
 #include "internal.h"
+#include "resident.h"
 
 namespace muon {
 namespace {
@@ -60,6 +61,7 @@ struct GroupPlan {
   int32_t ns_type = NS_F16;
   float alpha = 1.f, scale = 1.f;
   SkinnyCfg sk{};
+  ResidentCfg rc{};     // RESIDENT path: cluster and columns per CTA
   TcMaps tc{};          // TENSOR path: TMA descriptors of the workspace
   size_t off_y0 = 0, off_y1 = 0, off_a = 0, off_q = 0, off_part = 0, off_invn = 0, off_dbg = 0;
   size_t off_u = 0;  // skinny groups under Nesterov: U for the direct kernel (0: none)
@@ -91,7 +93,7 @@ muon_status_t check_options(const muon_plan_options& o) {
     return fail(MUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (o.ns_dtype != MUON_NS_FP16 && o.ns_dtype != MUON_NS_BF16)
     return fail(MUON_ERR_INVALID_ARG, "ns_dtype %d is not a muon_ns_dtype_t", o.ns_dtype);
-  if (o.path_override < MUON_PATH_AUTO || o.path_override > MUON_PATH_SIMT)
+  if (o.path_override < MUON_PATH_AUTO || o.path_override > MUON_PATH_RESIDENT)
     return fail(MUON_ERR_INVALID_ARG, "path_override %d is not a muon_path_t", o.path_override);
   if (o.mode == MUON_MODE_FP32 && o.path_override != MUON_PATH_AUTO &&
       o.path_override != MUON_PATH_SIMT)
@@ -208,7 +210,14 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
     } else if (path == PATH_AUTO) {
       const bool sk = thr > 0 && skinny_config((int32_t)gp.rows, (int32_t)gp.cols, thr, &gp.sk,
                                                o.column_shards);
-      path = sk ? PATH_SKINNY : PATH_TENSOR;
+      // RESIDENT for untransposed groups whose rows are whole 16-byte vectors;
+      // transposed and odd-width groups measured faster on TENSOR
+      const bool res = gp.transposed == 0 && gp.n % 8 == 0 && resident_config(gp.m, gp.n, &gp.rc);
+      path = sk ? PATH_SKINNY : res ? PATH_RESIDENT : PATH_TENSOR;
+    } else if (path == PATH_RESIDENT) {
+      if (!resident_config(gp.m, gp.n, &gp.rc))
+        return fail(MUON_ERR_UNSUPPORTED, "group %zu [%lld,%lld] does not fit the resident path", g,
+                    (long long)gp.rows, (long long)gp.cols);
     } else if (path == PATH_SKINNY) {
       if (!skinny_config((int32_t)gp.rows, (int32_t)gp.cols, 64, &gp.sk, o.column_shards))
         return fail(MUON_ERR_UNSUPPORTED, "group %zu [%lld,%lld] does not fit the skinny path", g,
@@ -223,7 +232,7 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
       if (o.flags & MUON_FLAG_NESTEROV) {  // read only by the direct kernel (k > kGramSpaceMaxSteps)
         gp.off_u = o2; o2 = align_up(o2 + (size_t)gp.batch * gp.rows * gp.cols * 4, kAlign);
       }
-    } else {
+    } else if (path == PATH_TENSOR || path == PATH_SIMT) {
       const size_t es = ns_esize(gp.ns_type);
       const size_t yb = (size_t)gp.batch * gp.m * gp.n_pitch * es;
       const size_t ab = (size_t)gp.batch * gp.m * gp.m_pitch * es;
@@ -312,7 +321,7 @@ KArgs make_args(const muon_plan_s* p, const GroupPlan& g) {
   a.alpha = g.alpha;
   a.y0 = base + g.off_y0;
   a.part = reinterpret_cast<float*>(base + g.off_part);
-  if (g.path != PATH_SKINNY) {
+  if (g.path == PATH_TENSOR || g.path == PATH_SIMT) {
     a.y1 = base + g.off_y1;
     a.A = base + g.off_a; a.Q = base + g.off_q;
     a.invn = reinterpret_cast<float*>(base + g.off_invn);
@@ -332,6 +341,7 @@ cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int3
   const KArgs a = make_args(p, g);
   cudaError_t e;
   if (g.path == PATH_SKINNY) return launch_skinny(a, g.sk, k, s);
+  if (g.path == PATH_RESIDENT) return launch_resident(a, g.rc, s);
   if ((e = launch_momentum_partial(a, s))) return e;
   if ((e = launch_norm_finalize(a, s))) return e;
   if ((e = launch_normalize_cast(a, a.y0, s))) return e;
@@ -377,6 +387,7 @@ bool fills_gpu(const muon_plan_s* p, const GroupPlan& g) {
     const int64_t bn = g.n >= 256 ? 256 : 128;
     return g.batch * ((g.m + 127) / 128) * ((g.n + bn - 1) / bn) >= p->num_sms;
   }
+  if (g.path == PATH_RESIDENT) return g.batch * g.rc.cluster >= p->num_sms;
   return g.path == PATH_SKINNY && g.batch * g.sk.cluster >= p->num_sms;
 }
 
@@ -523,7 +534,8 @@ double member_seconds(const GroupPlan& g, int32_t ns_steps, bool f32) {
   const double bytes = m * n * (f32 ? 20.0 : 14.0);
   const double flops = (double)ns_steps * (4 * m * m * n + 2 * m * m * m);
   const double rate = f32 ? kFp32 : kTensor;
-  return std::max(bytes / kHbm, g.path == PATH_SKINNY ? 0.0 : flops / rate);
+  const bool hbm_bound = g.path == PATH_SKINNY || g.path == PATH_RESIDENT;
+  return std::max(bytes / kHbm, hbm_bound ? 0.0 : flops / rate);
 }
 
 }  // namespace
@@ -627,6 +639,7 @@ muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
   bool tc_ready[3] = {false, false, false};
   for (GroupPlan& g : p->d.groups) {
     if (g.path == PATH_SKINNY) PLAN_TRY(prepare_skinny(make_args(p, g), g.sk));
+    if (g.path == PATH_RESIDENT) PLAN_TRY(prepare_resident(g.ns_type));
     if (g.path == PATH_TENSOR) {
       if (!tc_ready[g.ns_type]) {
         PLAN_TRY(prepare_tc(g.ns_type));

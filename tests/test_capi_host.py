@@ -166,3 +166,12 @@ def test_describe_large_config_without_device(lib):
     assert [(g["rows"], g["cols"], g["batch"]) for g in d["groups"]] == [
         (4096, 12288, 32), (4096, 4096, 32), (4096, 16384, 32), (16384, 4096, 32)]
     assert d["groups"][3]["transposed"]
+
+
+def test_resident_path_choice(lib):
+    """AUTO: resident for untransposed groups of width a multiple of 8,
+    tensor for transposed, odd-width and mixed groups."""
+    d = pkg.describe([[128, 4096], [96, 2048], [4096, 128], [100, 700], [72, 4104]])
+    assert [g["path"] for g in d["groups"]] == ["resident", "resident", "tensor", "tensor", "tensor"]
+    d = pkg.describe([[128, 1000], [1000, 128]], merge_transposed=True)
+    assert [g["path"] for g in d["groups"]] == ["tensor"]

@@ -48,11 +48,13 @@ CASES = [
     ([[256, 520], [520, 256], [2, 130, 384]], {}, 5),                                # tensor cores
     ([[96, 200], [2, 70, 33]], {"path": "simt"}, 5),                                 # SIMT
     ([[24, 4096], [4096, 24], [64, 256]], {"merge_transposed": True, "column_shards": 8}, 5),
+    ([[100, 700], [700, 100], [2, 128, 520], [96, 2049], [2049, 96]], {"path": "resident"}, 5),
 ]
 
 
 @pytest.mark.parametrize("shapes,opts,k", CASES,
-                         ids=["gram_space", "gram_space_m64", "transposed_ragged", "direct", "tensor", "simt", "merged_shards"])
+                         ids=["gram_space", "gram_space_m64", "transposed_ragged", "direct", "tensor", "simt", "merged_shards",
+                              "resident"])
 def test_guard_bands_intact(shapes, opts, k):
     w = W.custom(shapes, seed=51, ns_steps=k)
     P, G, M = W.make_tensors(w, "cuda")
@@ -102,8 +104,9 @@ def test_resume_through_host_equals_continuous(shapes):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("shapes", [[[24, 4096]] * 6, [[64, 1000]] * 4, [[256, 512]] * 3, [[2, 130, 384]]],
-                         ids=["gram_space", "gram_space_m64", "tensor", "tensor_experts"])
+@pytest.mark.parametrize("shapes", [[[24, 4096]] * 6, [[64, 1000]] * 4, [[256, 512]] * 3, [[2, 130, 384]],
+                                    [[128, 1024]] * 3],
+                         ids=["gram_space", "gram_space_m64", "tensor", "tensor_experts", "resident"])
 def test_nonfinite_member_stays_isolated(shapes):
     """A NaN in one member's gradient propagates into that member only (no
     special casing, as stated); every other member gives the same bits as in

@@ -160,7 +160,7 @@ def test_random_tensor_shapes_against_the_oracle(case):
         shapes.append([2, r, c] if rng.random() < 0.25 else [r, c])
     k = int(rng.integers(1, 7))
     w = W.custom(shapes, seed=4000 + case, ns_steps=k)
-    run = GpuRun(w)
+    run = GpuRun(w, path="tensor")
     for g in run.plan.groups():
         assert g["path"] == "tensor", g
     check_all(run)

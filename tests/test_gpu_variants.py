@@ -21,8 +21,9 @@ PATHS = [
     ([[24, 2048], [48, 1000]], {}, 70),                     # skinny, direct iteration (k > 64)
     ([[256, 512], [512, 256]], {}, 6),                      # tensor cores (tcgen05)
     ([[96, 200], [2, 70, 33]], {"path": "simt"}, 6),        # SIMT, bf16 mode
+    ([[128, 1000], [1000, 128], [2, 96, 520], [100, 700]], {"path": "resident"}, 6),  # resident
 ]
-IDS = ["gram_space", "direct", "tensor", "simt"]
+IDS = ["gram_space", "direct", "tensor", "simt", "resident"]
 
 
 def _workload(shapes, k, seed, mode="bf16", **kw):
@@ -122,6 +123,7 @@ MERGED = [
     ([[24, 2048], [2048, 24]], {}, 70),                                         # skinny, direct
     ([[256, 512], [512, 256], [2, 512, 256]], {}, 5),                           # tensor cores
     ([[96, 200], [200, 96]], {"path": "simt"}, 5),                              # SIMT
+    ([[128, 1000], [1000, 128], [2, 100, 700], [700, 100]], {"path": "resident"}, 5),  # resident
 ]
 
 

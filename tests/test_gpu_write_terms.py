@@ -10,6 +10,7 @@ of those mistakes moves P' outside the bound (one bf16 ulp of P' plus
 lr s |dO|).
 Each kernel that writes P is covered: the Gram-space skinny kernel (both
 orientations, m = 24 and m = 64), the direct skinny iteration (k = 70), the
+resident kernel (both orientations, vector and element-wise forms), the
 tensor path (both orientations), merged [r, c] + [c, r] buckets, and both
 non-trivial scale modes."""
 import numpy as np
@@ -45,6 +46,16 @@ def test_write_terms_gram_space_skinny(scale_mode):
     w = W.custom([[24, 4096], [4096, 24], [2, 64, 1504], [1504, 64]], seed=41, **BIG)
     run = GpuRun(w, scale=scale_mode)
     assert {g["path"] for g in run.plan.groups()} == {"skinny"}
+    _terms_visible(run, scale_mode)
+    check_all(run, scale_mode=scale_mode)
+    run.close()
+
+
+@pytest.mark.parametrize("scale_mode", ["sqrt_aspect", "rms_0_2"])
+def test_write_terms_resident_path(scale_mode):
+    w = W.custom([[128, 768], [768, 128], [100, 700]], seed=45, **BIG)
+    run = GpuRun(w, scale=scale_mode, path="resident")
+    assert {g["path"] for g in run.plan.groups()} == {"resident"}
     _terms_visible(run, scale_mode)
     check_all(run, scale_mode=scale_mode)
     run.close()
