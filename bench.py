@@ -48,7 +48,6 @@ PER_CONFIG = [("c1_fp32_64x128", None), ("c2_skinny_74x24x10240", None),
               ("c5_mixed_1000", 5), ("c5_mixed_1000", 10)]
 L2_BYTES = 129 * 2 ** 20
 SKINNY_MAX_M = 64  # the planner's default skinny threshold (min(rows, cols) <= 64)
-RESIDENT_MAX = (128, 4096)  # the planner's resident path: rows <= 128, cols <= 4096, cols % 8 == 0
 
 
 def algorithmic_work(shapes, mode, k):
@@ -78,10 +77,7 @@ def shape_groups(shapes, mode):
         groups[key] = groups.get(key, 0) + E
     out = []
     for (r, c), b in groups.items():
-        m, n = min(r, c), max(r, c)
-        res = r <= c and m <= RESIDENT_MAX[0] and n <= RESIDENT_MAX[1] and n % 8 == 0
-        path = ("simt" if mode == "fp32" else "skinny" if m <= SKINNY_MAX_M else
-                "resident" if res else "tensor")
+        path = "simt" if mode == "fp32" else ("skinny" if min(r, c) <= SKINNY_MAX_M else "tensor")
         out.append({"rows": r, "cols": c, "batch": b, "path": path})
     return out
 
@@ -462,6 +458,13 @@ def roofline_of(w, dg, peaks):
     return roof
 
 
+def plan_options(args):
+    """Plan options from the command line: `--path` forces one kernel path
+    for every group (default: the planner's choice)."""
+    path = getattr(args, "path", "auto")
+    return {} if path == "auto" else {"path": path}
+
+
 def measure(w, args, pkg, torch, dev, local, world, peaks, stream, flush, sample_clocks):
     """Times workload w on this GPU: K timed steps (the whole step, every
     group), then per-group times from a second plan that runs the groups one
@@ -469,7 +472,7 @@ def measure(w, args, pkg, torch, dev, local, world, peaks, stream, flush, sample
     from newton_schulz_bucket_gb300 import workloads as W
     byts, flops = algorithmic_work(w.shapes, w.mode, w.ns_steps)
     tensors = W.make_tensors(w, dev)
-    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode)
+    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, **plan_options(args))
     groups = plan.groups()
     bound = plan.bind(*tensors)
     sp = stream.cuda_stream
@@ -504,7 +507,8 @@ def measure(w, args, pkg, torch, dev, local, world, peaks, stream, flush, sample
     plan.close()
     # per-group kernel times from events recorded inside the step graph of a
     # plan that runs the groups one after another
-    tplan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, group_timing=True, max_streams=1)
+    tplan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, group_timing=True, max_streams=1,
+                         **plan_options(args))
     tbound = tplan.bind(*tensors)
     gtimes = [[] for _ in groups]
     for j in range(min(args.steps, 6) + 1):
@@ -563,7 +567,7 @@ def run_e2e(args, w, pkg, torch, dev, local, byts, flops, world):
         vP[i].copy_(P[i]); vG[i].copy_(G[i]); vM[i].copy_(M[i])
     del P, G, M
     torch.cuda.empty_cache()
-    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, host_staging=True)
+    plan = pkg.MuonPlan(w.shapes, device=local, mode=w.mode, host_staging=True, **plan_options(args))
     stream = torch.cuda.Stream(dev)
     for _ in range(max(2, args.warmup // 2)):
         plan.step_host(vP, vG, vM, w.beta, w.lr, w.wd, w.ns_steps, w.coeffs, stream=stream)
@@ -598,6 +602,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "skinny", "tensor", "simt", "resident"],
+                    help="force one kernel path for every group (profiling; default: the planner's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -670,7 +676,7 @@ def main():
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.mode == "bf16" else "f32",
                 "data": "synthetic: seeded Gaussian G, M0, P (per-config stds); no dataset",
-                "config": config_dict(w, world),
+                "config": dict(config_dict(w, world), **plan_options(args)),
                 "matrices_per_s": head["matrices_per_s"], "tflops": head["tflops"],
                 "gbs": head["gbs"], "tflops_executed": head["tflops_executed"],
                 "per_group": head["per_group"], "roofline": head["roofline"],

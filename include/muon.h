@@ -97,14 +97,13 @@ typedef enum {
  * the data twice (momentum with the Gram matrix and the norm, then the
  * output) and iterates in m x m Gram space on chip; beyond 64 steps, a
  * momentum kernel and the direct iteration on a fragment-ordered, L2-resident
- * workspace.  Else RESIDENT for groups of rows <= cols with rows <= 128,
- * cols <= 4096 and cols a multiple of 8: one kernel per group, a cluster of
- * up to 8 CTAs per matrix whose shared memory holds the iterate for all k
- * steps (the TENSOR path's arithmetic on tcgen05, partial Gram matrices
- * added through distributed shared memory), so HBM sees only G, M, P read
- * and M', P' written.  TENSOR otherwise (tcgen05 GEMMs on TMEM accumulators,
- * fed by TMA).  RESIDENT may also be asked for any group with
- * min(rows, cols) <= 128 and max(rows, cols) <= 4096, either orientation.
+ * workspace.  TENSOR otherwise (tcgen05 GEMMs on TMEM accumulators, fed by
+ * TMA).  RESIDENT, only when asked for, takes groups with min(rows, cols)
+ * <= 128 and max(rows, cols) <= 4096: one kernel per group, a cluster of up
+ * to 8 CTAs per matrix whose shared memory holds the iterate for all k steps
+ * (the TENSOR path's arithmetic on tcgen05, partial Gram matrices added
+ * through distributed shared memory), so HBM sees only G, M, P read and M',
+ * P' written; it is bound by the latency of its per-step cluster exchange.
  * FP32 mode always uses SIMT (fp32 FMA). */
 typedef enum {
   MUON_PATH_AUTO = 0,

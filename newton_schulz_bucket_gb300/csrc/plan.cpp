@@ -210,10 +210,9 @@ muon_status_t build_desc(const muon_shape_t* shapes, int32_t n_params,
     } else if (path == PATH_AUTO) {
       const bool sk = thr > 0 && skinny_config((int32_t)gp.rows, (int32_t)gp.cols, thr, &gp.sk,
                                                o.column_shards);
-      // RESIDENT for untransposed groups whose rows are whole 16-byte vectors;
-      // transposed and odd-width groups measured faster on TENSOR
-      const bool res = gp.transposed == 0 && gp.n % 8 == 0 && resident_config(gp.m, gp.n, &gp.rc);
-      path = sk ? PATH_SKINNY : res ? PATH_RESIDENT : PATH_TENSOR;
+      // (RESIDENT only on request: under the power cap of a full step it
+      // measured slower than TENSOR on every shape it takes)
+      path = sk ? PATH_SKINNY : PATH_TENSOR;
     } else if (path == PATH_RESIDENT) {
       if (!resident_config(gp.m, gp.n, &gp.rc))
         return fail(MUON_ERR_UNSUPPORTED, "group %zu [%lld,%lld] does not fit the resident path", g,

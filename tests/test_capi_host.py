@@ -168,10 +168,18 @@ def test_describe_large_config_without_device(lib):
     assert d["groups"][3]["transposed"]
 
 
-def test_resident_path_choice(lib):
-    """AUTO: resident for untransposed groups of width a multiple of 8,
-    tensor for transposed, odd-width and mixed groups."""
-    d = pkg.describe([[128, 4096], [96, 2048], [4096, 128], [100, 700], [72, 4104]])
-    assert [g["path"] for g in d["groups"]] == ["resident", "resident", "tensor", "tensor", "tensor"]
-    d = pkg.describe([[128, 1000], [1000, 128]], merge_transposed=True)
-    assert [g["path"] for g in d["groups"]] == ["tensor"]
+def test_resident_path_on_request(lib):
+    """The resident path runs only when asked for, on groups with min dim <=
+    128 and max dim <= 4096 (either orientation, any width); it keeps no
+    scratch of its own (only the optional copy of O)."""
+    shapes = [[128, 4096], [4096, 128], [100, 700], [65, 65]]
+    assert {g["path"] for g in pkg.describe(shapes)["groups"]} == {"tensor"}
+    d = pkg.describe(shapes, path="resident")
+    assert [g["path"] for g in d["groups"]] == ["resident"] * 4
+    assert all(g["workspace_bytes"] == 0 for g in d["groups"])
+    assert pkg.describe(shapes, path="resident", keep_update=True)["groups"][0]["workspace_bytes"] >= \
+        4 * 128 * 4096
+    for bad in ([129, 4096], [128, 4104], [4104, 128]):
+        with pytest.raises(pkg.MuonError) as ei:
+            pkg.describe([bad], path="resident")
+        assert ei.value.status == 2  # MUON_ERR_UNSUPPORTED

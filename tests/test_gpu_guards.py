@@ -104,10 +104,10 @@ def test_resume_through_host_equals_continuous(shapes):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("shapes", [[[24, 4096]] * 6, [[64, 1000]] * 4, [[256, 512]] * 3, [[2, 130, 384]],
-                                    [[128, 1024]] * 3],
+@pytest.mark.parametrize("shapes,opts", [([[24, 4096]] * 6, {}), ([[64, 1000]] * 4, {}), ([[256, 512]] * 3, {}),
+                                         ([[2, 130, 384]], {}), ([[128, 1024]] * 3, {"path": "resident"})],
                          ids=["gram_space", "gram_space_m64", "tensor", "tensor_experts", "resident"])
-def test_nonfinite_member_stays_isolated(shapes):
+def test_nonfinite_member_stays_isolated(shapes, opts):
     """A NaN in one member's gradient propagates into that member only (no
     special casing, as stated); every other member gives the same bits as in
     a run without it."""
@@ -118,7 +118,7 @@ def test_nonfinite_member_stays_isolated(shapes):
     target = G[bad_param][bad_expert] if len(shapes[bad_param]) == 3 else G[bad_param]
     target[3, 5] = float("nan")
     for tensors in ((P, G, M), clean):
-        plan = pkg.MuonPlan(w.shapes)
+        plan = pkg.MuonPlan(w.shapes, **opts)
         plan.step(*tensors, w.beta, w.lr, w.wd, 5)
         torch.cuda.synchronize()
         plan.close()

@@ -1,8 +1,7 @@
 """GPU parity of the resident path (one kernel per group, the iterate held in
 a cluster's shared memory for all k steps; min dim <= 128, max dim <= 4096)
-against the oracle, and its batch invariance.  The planner takes it by
-default for untransposed groups whose width is a multiple of 8; the tests
-ask for it explicitly so that every access form runs.
+against the oracle, and its batch invariance.  The planner takes it only
+when asked for (path="resident").
 
 The shapes cover every access form of its passes: 16-byte vectors along the
 parameter's rows (rows <= cols, n % 8 == 0), the 8 x 8 transposing blocks

@@ -34,11 +34,8 @@ def test_planner_equals_oracle_bucketing(shapes, merge):
         orient = {shapes[p][-2] > shapes[p][-1] for p, _ in rg["members"]}
         assert g["transposed"] == ("mixed" if len(orient) == 2 else orient.pop())
         m = min(g["rows"], g["cols"])
-        n = max(g["rows"], g["cols"])
-        res = g["transposed"] is False and m <= 128 and n <= 4096 and n % 8 == 0
-        assert g["path"] == ("skinny" if m <= 64 else "resident" if res else "tensor")
-        # the resident path keeps everything on chip: no scratch of its own
-        assert g["workspace_bytes"] > 0 or g["path"] == "resident"
+        assert g["path"] == ("skinny" if m <= 64 else "tensor")
+        assert g["workspace_bytes"] > 0
     assert first == sum(s[0] if len(s) == 3 else 1 for s in shapes)
     # one workspace holds every group's scratch plus the per-member pointer
     # table (three pointers, the orientation and the scale: 32 bytes each)
@@ -63,11 +60,8 @@ def test_options_add_their_buffers():
 @hypothesis.given(shapes=shape_lists)
 def test_fp32_mode_and_thresholds(shapes):
     """fp32 mode sends every group to the SIMT path; a lower skinny threshold
-    moves exactly the groups above it to the resident path (untransposed,
-    rows <= 128, cols <= 4096 and a multiple of 8) or else the tensor path."""
+    moves exactly the groups above it to the tensor path."""
     assert {g["path"] for g in pkg.describe(shapes, mode="fp32")["groups"]} == {"simt"}
     d = pkg.describe(shapes, skinny_threshold=8)
     for g in d["groups"]:
-        m, n = min(g["rows"], g["cols"]), max(g["rows"], g["cols"])
-        res = g["transposed"] is False and m <= 128 and n <= 4096 and n % 8 == 0
-        assert g["path"] == ("skinny" if m <= 8 else "resident" if res else "tensor")
+        assert g["path"] == ("skinny" if min(g["rows"], g["cols"]) <= 8 else "tensor")
