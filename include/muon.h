@@ -274,13 +274,13 @@ MUON_API muon_status_t muon_step_schedule(muon_plan_t plan, void* const* params,
  * gradient and momentum to the plan's device mirrors, runs muon_step on them,
  * copies params and momenta back, and returns after `stream` has finished
  * (results are in the host buffers on return).  Needs MUON_FLAG_HOST_STAGING
- * at plan creation (UNSUPPORTED otherwise).  Contiguous host ranges of
- * consecutive parameters are moved with one copy each.  When every group
- * takes the skinny path the step runs in chunks of parameters, and otherwise
- * (more than one group) in shape groups: each unit is copied in, updated and
- * copied out on its own stream order so that copies in both directions and
- * the kernels overlap; every member gets the same kernels as in muon_step,
- * so the results are the same bits.  One (a, b, c) triple per
+ * at plan creation (UNSUPPORTED otherwise).  Contiguous host ranges are
+ * moved with one copy each.  When every group takes the skinny path the step
+ * runs in chunks of parameters, and otherwise in slices of whole members of
+ * a group (about 1/16 of the plan's elements each): each unit is copied in,
+ * updated and copied out on its own stream order so that copies in both
+ * directions and the kernels overlap; every member gets the same kernels as
+ * in muon_step, so the results are the same bits.  One (a, b, c) triple per
  * call: a per-step schedule needs device buffers (muon_step_schedule). */
 MUON_API muon_status_t muon_step_host(muon_plan_t plan, void* const* host_params,
                                       const void* const* host_grads,

@@ -269,6 +269,9 @@ using namespace muon;
 
 // Chunks of the pipelined host-buffer step (muon_step_host on skinny-only plans).
 constexpr int kHostChunks = 4;
+// Units of the pipelined muon_step_host for other plans: slices of whole
+// members of a group, about 1/kHostUnits of the plan's elements each.
+constexpr int kHostUnits = 16;
 
 struct muon_plan_s {
   PlanDesc d;
@@ -296,6 +299,14 @@ struct muon_plan_s {
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t up_ev = nullptr;
   std::vector<cudaEvent_t> in_ev, run_ev, out_ev;
+  // pipelined muon_step_host (other plans): members [i0, i0 + cnt) of group g
+  // per unit, with the tensor maps of that slice of the group's workspace
+  struct HostUnit {
+    int32_t g;
+    int64_t i0, cnt;
+    TcMaps tc;
+  };
+  std::vector<HostUnit> units;
 };
 
 namespace {
@@ -334,10 +345,36 @@ KArgs make_args(const muon_plan_s* p, const GroupPlan& g) {
   return a;
 }
 
-// Enqueue one group's whole step on stream s.
-cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int32_t k,
-                                  cudaStream_t s) {
-  const KArgs a = make_args(p, g);
+// Kernel arguments of members [i0, i0 + cnt) of group g: every per-member
+// pointer (the caller's buffers through the member table, and the group's
+// scratch) moves by i0 members.
+KArgs sub_args(const KArgs& a, const GroupPlan& g, int64_t i0, int64_t cnt) {
+  KArgs r = a;
+  r.B = (int32_t)cnt;
+  r.mem = a.mem + i0;
+  const int64_t mn = g.m * g.n;
+  if (a.dbg) r.dbg = a.dbg + i0 * mn;
+  if (g.path == PATH_SKINNY) {
+    r.part = a.part + i0 * a.n_chunks;
+    r.y0 = static_cast<unsigned char*>(a.y0) + i0 * g.sk.ws_bytes;
+    if (a.u) r.u = a.u + i0 * mn;
+  } else if (g.path == PATH_TENSOR || g.path == PATH_SIMT) {
+    const size_t es = ns_esize(g.ns_type);
+    const size_t yb = (size_t)g.m * g.n_pitch * es, ab = (size_t)g.m * g.m_pitch * es;
+    r.y0 = static_cast<unsigned char*>(a.y0) + i0 * yb;
+    r.y1 = static_cast<unsigned char*>(a.y1) + i0 * yb;
+    r.A = static_cast<unsigned char*>(a.A) + i0 * ab;
+    r.Q = static_cast<unsigned char*>(a.Q) + i0 * ab;
+    r.part = a.part + i0 * a.n_chunks;
+    r.invn = a.invn + i0;
+  }
+  return r;
+}
+
+// Enqueue the whole step of the members `a` describes (a group, or a slice of
+// one with its own tensor maps `tc`) on stream s.
+cudaError_t enqueue_kernels(const KArgs& a, const GroupPlan& g, const TcMaps& tc, int32_t k,
+                            cudaStream_t s) {
   cudaError_t e;
   if (g.path == PATH_SKINNY) return launch_skinny(a, g.sk, k, s);
   if (g.path == PATH_RESIDENT) return launch_resident(a, g.rc, s);
@@ -347,9 +384,9 @@ cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int3
   if (g.path == PATH_TENSOR) {
     int src = 0;
     for (int32_t it = 0; it < k; ++it) {
-      if ((e = launch_tc_gram(a, g.tc, src, s))) return e;
-      if ((e = launch_tc_poly(a, g.tc, it, s))) return e;
-      if ((e = launch_tc_update(a, g.tc, src, s))) return e;
+      if ((e = launch_tc_gram(a, tc, src, s))) return e;
+      if ((e = launch_tc_poly(a, tc, it, s))) return e;
+      if ((e = launch_tc_update(a, tc, src, s))) return e;
       src ^= 1;
     }
     return launch_write(a, src == 0 ? a.y0 : a.y1, s);
@@ -363,6 +400,12 @@ cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int3
     std::swap(ys, yd);
   }
   return launch_write(a, ys, s);
+}
+
+// Enqueue one group's whole step on stream s.
+cudaError_t enqueue_group_kernels(const muon_plan_s* p, const GroupPlan& g, int32_t k,
+                                  cudaStream_t s) {
+  return enqueue_kernels(make_args(p, g), g, g.tc, k, s);
 }
 
 cudaError_t record(const muon_plan_s* p, cudaEvent_t ev, cudaStream_t s) {
@@ -659,7 +702,27 @@ muon_status_t muon_plan_create(const muon_shape_t* shapes, int32_t n_params,
     PLAN_TRY(cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking));
     PLAN_TRY(cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking));
     PLAN_TRY(cudaEventCreateWithFlags(&p->up_ev, cudaEventDisableTiming));
-    const int nev = std::max<int>(kHostChunks, (int)p->d.groups.size());  // chunks or groups
+    bool skinny_only = true;
+    for (const GroupPlan& g : p->d.groups) skinny_only = skinny_only && g.path == PATH_SKINNY;
+    if (!skinny_only) {
+      int64_t total = 0;
+      for (const GroupPlan& g : p->d.groups) total += g.batch * g.m * g.n;
+      const int64_t target = std::max<int64_t>(1, total / kHostUnits);
+      for (int32_t gi = 0; gi < (int32_t)p->d.groups.size(); ++gi) {
+        const GroupPlan& g = p->d.groups[gi];
+        const int64_t nsl = std::min<int64_t>(g.batch, std::max<int64_t>(1, (g.batch * g.m * g.n + target - 1) / target));
+        const int64_t per = (g.batch + nsl - 1) / nsl;
+        for (int64_t i0 = 0; i0 < g.batch; i0 += per) {
+          muon_plan_s::HostUnit u{};
+          u.g = gi;
+          u.i0 = i0;
+          u.cnt = std::min(per, g.batch - i0);
+          if (g.path == PATH_TENSOR) PLAN_TRY(tc_make_maps(sub_args(make_args(p, g), g, u.i0, u.cnt), &u.tc));
+          p->units.push_back(u);
+        }
+      }
+    }
+    const int nev = std::max<int>(kHostChunks, (int)p->units.size());  // chunks or units
     for (int i = 0; i < nev; ++i) {
       cudaEvent_t e0, e1, e2;
       PLAN_TRY(cudaEventCreateWithFlags(&e0, cudaEventDisableTiming));
@@ -750,19 +813,6 @@ muon_status_t step_impl(muon_plan_t p, void* const* params, const void* const* g
   return MUON_OK;
 }
 
-// Kernel arguments of members [i0, i0 + cnt) of a skinny group.
-KArgs skinny_sub_args(const KArgs& a, const GroupPlan& g, int64_t i0, int64_t cnt) {
-  KArgs r = a;
-  const int64_t mn = g.m * g.n;
-  r.B = (int32_t)cnt;
-  r.mem = a.mem + i0;
-  r.part = a.part + i0 * a.n_chunks;
-  r.y0 = static_cast<unsigned char*>(a.y0) + i0 * g.sk.ws_bytes;
-  if (a.dbg) r.dbg = a.dbg + i0 * mn;
-  if (a.u) r.u = a.u + i0 * mn;
-  return r;
-}
-
 bool all_skinny(const muon_plan_s* p) {
   for (const GroupPlan& g : p->d.groups)
     if (g.path != PATH_SKINNY) return false;
@@ -846,7 +896,7 @@ muon_status_t host_step_pipelined(muon_plan_s* p, void* const* hp, const void* c
         }
       }
       if (!cnt) continue;
-      const cudaError_t e = launch_skinny(skinny_sub_args(make_args(p, g), g, i0, cnt), g.sk, k, s);
+      const cudaError_t e = launch_skinny(sub_args(make_args(p, g), g, i0, cnt), g.sk, k, s);
       if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
     CUDA_TRY(cudaEventRecord(p->run_ev[ci], s));
@@ -860,18 +910,19 @@ muon_status_t host_step_pipelined(muon_plan_s* p, void* const* hp, const void* c
   return MUON_OK;
 }
 
-// muon_step_host for a plan with more than one group, not all skinny: the
-// same three-stream pipeline with the shape groups as its units.  Every
-// group's inputs are queued for copy-in at once; its kernels run on the
-// caller's stream once they have landed (groups one after another), and its
-// parameters and momenta are copied back as soon as its kernels are done, so
-// the copies of other groups hide behind each group's kernels.  Every member
-// gets the same kernels as in a whole-plan step, so its results are the same
-// bits.
-muon_status_t host_step_by_group(muon_plan_s* p, void* const* hp, const void* const* hg,
-                                 float* const* hm, std::vector<void*>& dp, std::vector<void*>& dg,
-                                 std::vector<float*>& dm, float beta, float lr, float wd,
-                                 int32_t k, float a, float b, float c, cudaStream_t s) {
+// muon_step_host for other plans: the same three-stream pipeline with slices
+// of whole members of a group as its units (about 1/kHostUnits of the plan's
+// elements each, so that the copy in before the first kernels and the copy
+// out after the last ones are short).  Every unit's inputs are queued for
+// copy-in at once; its kernels run on the caller's stream once they have
+// landed (units one after another), and its parameters and momenta are
+// copied back as soon as its kernels are done, so the copies of other units
+// hide behind each unit's kernels.  Every member gets the same kernels as in
+// a whole-plan step, so its results are the same bits.
+muon_status_t host_step_units(muon_plan_s* p, void* const* hp, const void* const* hg,
+                              float* const* hm, std::vector<void*>& dp, std::vector<void*>& dg,
+                              std::vector<float*>& dm, float beta, float lr, float wd,
+                              int32_t k, float a, float b, float c, cudaStream_t s) {
   const float coef[3] = {a, b, c};
   if (muon_status_t st = step_impl(p, dp.data(), (const void* const*)dg.data(), dm.data(), beta, lr,
                                    wd, k, coef, 1, s, false))
@@ -879,40 +930,58 @@ muon_status_t host_step_by_group(muon_plan_s* p, void* const* hp, const void* co
   CUDA_TRY(cudaEventRecord(p->up_ev, s));
   CUDA_TRY(cudaStreamWaitEvent(p->h2d, p->up_ev, 0));
   const size_t pes = p_esize(p);
-  const size_t ng = p->d.groups.size();
-  // the parameters of each group, in member order, each once
-  std::vector<std::vector<int32_t>> params(ng);
-  for (size_t gi = 0; gi < ng; ++gi) {
-    const GroupPlan& g = p->d.groups[gi];
-    for (int64_t i = 0; i < g.batch; ++i) {
-      const int32_t pi = p->d.member_param[g.first_member + i];
-      if (params[gi].empty() || params[gi].back() != pi) params[gi].push_back(pi);
-    }
-  }
-  auto copy = [&](const std::vector<int32_t>& ps, const void* const* host, void* const* dev, size_t es,
+  using Unit = muon_plan_s::HostUnit;
+  // one copy per run of the unit's members whose host and device bytes are
+  // both back to back
+  auto copy = [&](const Unit& u, const void* const* host, const void* const* dev, size_t es,
                   bool to_device, cudaStream_t st) -> cudaError_t {
-    for (int32_t pi : ps) {
-      const cudaError_t e = copy_param_runs(p, pi, pi + 1, host, dev, es, to_device, st);
+    const GroupPlan& g = p->d.groups[u.g];
+    const size_t mb = (size_t)g.m * g.n * es;  // bytes of one member
+    auto at = [&](const void* const* base, int64_t i) {
+      const int64_t mi = g.first_member + u.i0 + i;
+      return static_cast<const unsigned char*>(base[p->d.member_param[mi]]) +
+             (size_t)p->d.member_expert[mi] * mb;
+    };
+    int64_t i = 0;
+    while (i < u.cnt) {
+      int64_t j = i + 1;
+      size_t bytes = mb;
+      while (j < u.cnt && at(host, j) == at(host, i) + bytes && at(dev, j) == at(dev, i) + bytes) {
+        bytes += mb;
+        ++j;
+      }
+      void* h = const_cast<unsigned char*>(at(host, i));
+      void* d = const_cast<unsigned char*>(at(dev, i));
+      const cudaError_t e = to_device ? cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice, st)
+                                      : cudaMemcpyAsync(h, d, bytes, cudaMemcpyDeviceToHost, st);
       if (e != cudaSuccess) return e;
+      i = j;
     }
     return cudaSuccess;
   };
-  std::vector<const void*> hpc(hp, hp + dp.size()), hmc(hm, hm + dp.size());
-  std::vector<void*> dmv(dm.begin(), dm.end());
-  for (size_t gi = 0; gi < ng; ++gi) {
-    CUDA_TRY(copy(params[gi], hpc.data(), dp.data(), pes, true, p->h2d));
-    CUDA_TRY(copy(params[gi], hg, dg.data(), pes, true, p->h2d));
-    CUDA_TRY(copy(params[gi], hmc.data(), dmv.data(), 4, true, p->h2d));
-    CUDA_TRY(cudaEventRecord(p->in_ev[gi], p->h2d));
+  const void* const* hpc = (const void* const*)hp;
+  const void* const* hmc = (const void* const*)hm;
+  const void* const* dpc = (const void* const*)dp.data();
+  const void* const* dgc = (const void* const*)dg.data();
+  const void* const* dmc = (const void* const*)dm.data();
+  const size_t nu = p->units.size();
+  for (size_t ui = 0; ui < nu; ++ui) {
+    const Unit& u = p->units[ui];
+    CUDA_TRY(copy(u, hpc, dpc, pes, true, p->h2d));
+    CUDA_TRY(copy(u, hg, dgc, pes, true, p->h2d));
+    CUDA_TRY(copy(u, hmc, dmc, 4, true, p->h2d));
+    CUDA_TRY(cudaEventRecord(p->in_ev[ui], p->h2d));
   }
-  for (size_t gi = 0; gi < ng; ++gi) {
-    CUDA_TRY(cudaStreamWaitEvent(s, p->in_ev[gi], 0));
-    const cudaError_t e = enqueue_group_kernels(p, p->d.groups[gi], k, s);
+  for (size_t ui = 0; ui < nu; ++ui) {
+    const Unit& u = p->units[ui];
+    const GroupPlan& g = p->d.groups[u.g];
+    CUDA_TRY(cudaStreamWaitEvent(s, p->in_ev[ui], 0));
+    const cudaError_t e = enqueue_kernels(sub_args(make_args(p, g), g, u.i0, u.cnt), g, u.tc, k, s);
     if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
-    CUDA_TRY(cudaEventRecord(p->run_ev[gi], s));
-    CUDA_TRY(cudaStreamWaitEvent(p->d2h, p->run_ev[gi], 0));
-    CUDA_TRY(copy(params[gi], hpc.data(), dp.data(), pes, false, p->d2h));
-    CUDA_TRY(copy(params[gi], hmc.data(), dmv.data(), 4, false, p->d2h));
+    CUDA_TRY(cudaEventRecord(p->run_ev[ui], s));
+    CUDA_TRY(cudaStreamWaitEvent(p->d2h, p->run_ev[ui], 0));
+    CUDA_TRY(copy(u, hpc, dpc, pes, false, p->d2h));
+    CUDA_TRY(copy(u, hmc, dmc, 4, false, p->d2h));
   }
   CUDA_TRY(cudaEventRecord(p->out_ev[0], p->d2h));
   CUDA_TRY(cudaStreamWaitEvent(s, p->out_ev[0], 0));
@@ -979,8 +1048,8 @@ muon_status_t muon_step_host(muon_plan_t p, void* const* hp, const void* const* 
   muon_status_t st;
   if (all_skinny(p) && !p->in_ev.empty() && np > 1)
     return host_step_pipelined(p, hp, hg, hm, dp, dg, dm, beta, lr, wd, ns_steps, a, b, c, s);
-  if (p->d.groups.size() > 1 && p->in_ev.size() >= p->d.groups.size())
-    return host_step_by_group(p, hp, hg, hm, dp, dg, dm, beta, lr, wd, ns_steps, a, b, c, s);
+  if (p->units.size() > 1 && p->in_ev.size() >= p->units.size())
+    return host_step_units(p, hp, hg, hm, dp, dg, dm, beta, lr, wd, ns_steps, a, b, c, s);
   if ((st = copy_runs([&](int32_t i) { return (const void*)hp[i]; },
                       [&](int32_t i) { return (const void*)dp[i]; }, pes, cudaMemcpyHostToDevice)))
     return st;

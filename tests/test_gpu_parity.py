@@ -261,18 +261,22 @@ def test_step_host_equals_device_step():
     dev.close(); host.close()
 
 
-def test_step_host_by_group_equals_device_step():
-    """Plans with tensor-path groups pipeline the host step group by group
-    (copy in, kernels, copy out on three streams): same bits as the device
-    step, over two steps."""
-    w = W.custom([[256, 512], [24, 2048], [512, 256], [256, 512], [2, 64, 768]], seed=17)
+@pytest.mark.parametrize("shapes,opts", [
+    ([[256, 512], [24, 2048], [512, 256], [256, 512], [2, 64, 768]], {}),
+    ([[6, 256, 512], [24, 2048], [300, 256], [5, 96, 640]], {}),
+    ([[12, 128, 640], [640, 128], [3, 100, 700]], {"path": "resident"}),
+], ids=["groups", "expert_slices", "resident"])
+def test_step_host_by_group_equals_device_step(shapes, opts):
+    """Plans that are not all skinny pipeline the host step in slices of whole
+    members of a group (copy in, kernels, copy out on three streams; slices
+    may cut a 3-D parameter): same bits as the device step, over two steps."""
+    w = W.custom(shapes, seed=17)
     P, G, M = W.make_tensors(w, "cuda")
     hP = [t.cpu().pin_memory() for t in P]
     hG = [t.cpu().pin_memory() for t in G]
     hM = [t.cpu().pin_memory() for t in M]
-    dev = pkg.MuonPlan(w.shapes)
-    host = pkg.MuonPlan(w.shapes, host_staging=True)
-    assert len(dev.groups()) == 4
+    dev = pkg.MuonPlan(w.shapes, **opts)
+    host = pkg.MuonPlan(w.shapes, host_staging=True, **opts)
     c = tuple(F32(v) for v in w.coeffs)
     for _ in range(2):
         dev.step(P, G, M, w.beta, w.lr, w.wd, w.ns_steps, c)
