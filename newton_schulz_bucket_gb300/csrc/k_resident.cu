@@ -1,16 +1,18 @@
-// Resident path for 64 < m <= 128 (m = min(rows, cols)) and n <= 4096: the
-// whole Muon step of a member in one kernel, its m x n iterate held in the
-// shared memory of one cluster for all k Newton-Schulz steps.
+// Resident path (taken on request) for m = min(rows, cols) <= 128 and
+// n <= 4096: the whole Muon step of a member in one kernel, its m x n
+// iterate held in the shared memory of one cluster for all k Newton-Schulz
+// steps.
 //
 // «MindSpore HyperParallel X 盘古,Muon优化器实现6倍性能跃升», 矩阵融合优化: small
 // matrices are bound by dispatch and data movement rather than arithmetic,
 // and fusing a shape's members into one launch removes the dispatch (Fig. 6,
-// Fig. 7).  On this GPU a [128, 4096] member's three products per step run
-// in microseconds on the tensor cores, so what bounds the step is the bytes
-// that cross HBM.  Keeping the iterate on chip across the k steps leaves only
-// the compulsory ones: G, M and P read, M' and P' written (14 B per element
-// in bf16 mode), against about 50 for three GEMM launches per step that each
-// stream the iterate through HBM.
+// Fig. 7).  On this GPU a [128, 4096] member's three products per step take
+// microseconds on the tensor cores, while the TENSOR path's three GEMM
+// launches per step stream the iterate through HBM (about 50 B per element
+// over a step, against the compulsory 14: G, M and P read, M' and P'
+// written, in bf16 mode).  Keeping the iterate on chip leaves only the
+// compulsory bytes; what bounds this kernel instead is the latency of the
+// per-step exchange of partial Gram matrices across the cluster.
 //
 // The arithmetic per step is the TENSOR path's («关于分布式Muon的想法整合及讨论»
 // §1, §2, §6): with Y = alpha X in the operand type,
