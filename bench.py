@@ -431,7 +431,8 @@ def roofline_of(w, dg, peaks):
             kernel = "k_resident (momentum, the k Newton-Schulz steps on chip, write; one launch)"
         else:
             kfile = None
-            kernel = f"group {dg['shape']} x {dg['batch']}: k_tc_gemm chain and the elementwise passes"
+            chain = "k_simt_gemm (fp32 FFMA)" if dg["path"] == "simt" else "k_tc_gemm"
+            kernel = f"group {dg['shape']} x {dg['batch']}: {chain} chain and the elementwise passes"
         tr = ncu_traffic(kfile, w.name) if kfile else None
         roof = {"bound": "hbm", "achieved": dg.get("GB_s"), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dg.get("roofline_frac"), "kernel": kernel,
