@@ -119,3 +119,13 @@ def test_report_groups_match_the_planner():
         want = [{k: g[k] for k in ("rows", "cols", "batch", "path")}
                 for g in pkg.describe(w.shapes, mode=w.mode)["groups"]]
         assert bench.shape_groups(w.shapes, w.mode) == want, name
+
+
+def test_path_option():
+    """--path forces one kernel path on every group's plan (and is recorded in
+    the line's config); the default leaves the choice to the planner."""
+    class A:
+        path = "auto"
+    assert bench.plan_options(A()) == {}
+    A.path = "resident"
+    assert bench.plan_options(A()) == {"path": "resident"}

@@ -24,6 +24,7 @@ CASES = {
     "element_wise": [[100, 700], [700, 100], [2, 72, 333]],
     "empty_last_cta": [[80, 2049], [2049, 80]],
     "small_clusters": [[65, 65], [3, 128, 128], [70, 130], [120, 1536]],
+    "skinny_sizes": [[24, 4096], [4096, 40], [1, 300]],
 }
 
 
