@@ -24,7 +24,9 @@
 // computed; each writes its elements with j >= i in place and mirrors those
 // with j > i to (j, i).  Every element is written exactly once and the stored
 // matrix is exactly symmetric.  For m = 4096 (BN = 256) that is 272 of 512
-// tiles.
+// tiles.  Both operands of these two products come from the same matrix, so a
+// diagonal tile (whose B panel is its A panel) loads the panel once and reads
+// it as both operands.
 #include <cuda.h>
 
 #include <type_traits>
@@ -312,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = p.B * (OP == TC_UPDATE ? p.tiles_m * p.tiles_n : p.tiles_sym);
   const int kblocks = (p.K + BK - 1) / BK;
   constexpr bool kMN = OP == TC_UPDATE;  // B operand is N-contiguous (MN-major)
+  // GRAM and POLY read both operands from the same matrix (Y, or the
+  // symmetric A), so on a diagonal tile the B panel is the A panel
+  constexpr bool kSym = OP != TC_UPDATE;
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer ----
@@ -320,9 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int b, tm, tn;
         decode<OP, BN>(t, p, b, tm, tn);
+        const bool diag = kSym && BN == BM && tm == tn;  // B panel = A panel: load it once
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err, 1)) goto producer_done;
-          mbar_expect_tx(full(s), L::kStage);
+          mbar_expect_tx(full(s), diag ? L::kA : L::kStage);
           const uint32_t sa = saddr(smem + s * L::kStage);
           const uint32_t sb = sa + L::kA;
           tma_load_3d(sa, &mapA, full(s), kb * BK, tm * BM, b);
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
               tma_load_3d(sb + c * (64 * BK * 2), &mapB, full(s), tn * BN + c * 64, kb * BK, b);
-          } else {
+          } else if (!diag) {
             tma_load_3d(sb, &mapB, full(s), kb * BK, tn * BN, b);
           }
           if (++s == kStages) { s = 0; ph ^= 1; }
@@ -345,6 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int b, tm, tn;
+        decode<OP, BN>(t, p, b, tm, tn);
+        const bool diag = kSym && BN == BM && tm == tn;
         if (!mbar_wait(tempty(acc), aph ^ 1, abort_flag, p.err, 2)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -352,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(full(s), ph, abort_flag, p.err, 4)) goto mma_done;
           tc_fence_after();
           const uint32_t sa = saddr(smem + s * L::kStage);
-          const uint32_t sb = sa + L::kA;
+          const uint32_t sb = diag ? sa : sa + L::kA;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
@@ -539,6 +548,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int num_tiles = p.B * (OP == TC_UPDATE ? p.tiles_m * p.tiles_n : p.tiles_sym);
   const int kblocks = (p.K + BK - 1) / BK;
   constexpr bool kMN = OP == TC_UPDATE;  // B operand is N-contiguous (MN-major)
+  // GRAM and POLY read both operands from the same matrix (Y, or the
+  // symmetric A), so on a diagonal tile the B panel is the A panel
+  constexpr bool kSym = OP != TC_UPDATE;
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer (both CTAs) ----
@@ -549,10 +561,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
         decode<OP, BN, BM2>(t, p, b, tm, tn);
         const int arow = tm * BM2 + (int)rank * 128;  // this CTA's A rows
         const int bcol = tn * BN + (int)rank * 128;   // this CTA's half of the B tile
+        // on a diagonal tile each CTA's half of B is its own A rows: load them once
+        const bool diag = kSym && tm == tn;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(s), ph ^ 1, abort_flag, p.err, 1)) goto producer_done;
           const uint32_t fb = map_to(full(s), 0);
-          if (rank == 0) mbar_expect_tx(full(s), 2 * L::kStage);
+          if (rank == 0) mbar_expect_tx(full(s), 2 * (diag ? L::kA : L::kStage));
           const uint32_t sa = saddr(smem + s * L::kStage);
           const uint32_t sb = sa + L::kA;
           tma_load_3d_pair(sa, &mapA, fb, kb * BK, arow, b);
@@ -560,7 +574,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c)
               tma_load_3d_pair(sb + c * (64 * BK * 2), &mapB, fb, bcol + c * 64, kb * BK, b);
-          } else {
+          } else if (!diag) {
             tma_load_3d_pair(sb, &mapB, fb, kb * BK, bcol, b);
           }
           if (++s == kStages2) { s = 0; ph ^= 1; }
@@ -575,6 +589,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       for (int t = pair; t < num_tiles; t += npairs) {
+        int b, tm, tn;
+        decode<OP, BN, BM2>(t, p, b, tm, tn);
+        const bool diag = kSym && tm == tn;
         if (!mbar_wait(tempty(acc), aph ^ 1, abort_flag, p.err, 2)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -582,7 +599,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           if (!mbar_wait(full(s), ph, abort_flag, p.err, 4)) goto mma_done;
           tc_fence_after();
           const uint32_t sa = saddr(smem + s * L::kStage);
-          const uint32_t sb = sa + L::kA;
+          const uint32_t sb = diag ? sa : sa + L::kA;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
